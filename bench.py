@@ -1,0 +1,518 @@
+"""Benchmark: W8A8 INT8 linear throughput (quantize + GEMM + epilogue) at Llama-3-8B shapes.
+
+One step = the four linear layers of one Llama-3-8B decoder layer (QKV 6144x4096, O
+4096x4096, gate_up 28672x4096, down 4096x14336) applied to M = 4096 token rows: per layer
+the per-token activation quantizer and the INT8 GEMM with its fused epilogue.  value =
+2*M*sum(N*K) / time, in TOPS, whole job over all ranks.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--no-components]
+
+Under torchrun (N > 1) every rank runs its own batch (weak scaling, no data-path
+collective); rank 0 prints one JSON line.  `--impl reference` times the CPU oracle on a
+bounded sample of the same workload on the host cores.
+"""
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+if HERE not in sys.path:
+    sys.path.insert(0, HERE)
+
+METRIC = "W8A8 linear TOPS (quant+GEMM) at Llama-3-8B shapes; % of INT8 tensor peak"
+M_TOKENS = 4096
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    p = os.path.join(HERE, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+        pg = dist
+    elif torch.cuda.is_available():
+        torch.cuda.set_device(0)
+    return world, rank, local, pg
+
+
+def barrier(pg):
+    if pg is not None:
+        if torch.cuda.is_available():
+            pg.barrier(device_ids=[torch.cuda.current_device()])
+        else:
+            pg.barrier()
+
+
+def max_over_ranks(pg, v):
+    if pg is None:
+        return v
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(pg, v):
+    if pg is None:
+        return v
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([float(v)], dtype=torch.float64, device=dev)
+    pg.all_reduce(t, op=pg.ReduceOp.SUM)
+    return float(t.item())
+
+
+def step_ops(M=M_TOKENS):
+    from w8a8_int8_quantized_gb300 import workloads as wl
+    return sum(2.0 * M * N * K for _, N, K in wl.llama_shapes())
+
+
+# --------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.proc = None
+        self.gpu = gpu_index
+        self.out = None
+
+    def start(self):
+        try:
+            self.out = open(os.path.join("/tmp", f"w8a8_clocks_{os.getpid()}.csv"), "w+")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.out, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.out.seek(0)
+        rows = [r.strip().split(",") for r in self.out.read().strip().splitlines() if r.strip()]
+        self.out.close()
+        sm, smax, reasons = [], 0.0, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[1]))
+                smax = max(smax, float(r[2]))
+                for nm, v in zip(names, r[5:9]):
+                    if "Active" in v and "Not" not in v:
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------- our arm
+class Timer:
+    """CUDA events on the launching (current) stream."""
+
+    def __init__(self):
+        self.pairs = []
+
+    def mark(self):
+        e = torch.cuda.Event(enable_timing=True)
+        e.record()
+        return e
+
+    @staticmethod
+    def total(pairs):
+        return sum(a.elapsed_time(b) for a, b in pairs)
+
+
+def run_ours(args, world, rank, pg):
+    import w8a8_int8_quantized_gb300 as w8
+    from w8a8_int8_quantized_gb300 import workloads as wl
+    dev = "cuda"
+    peaks, peak_src = load_peaks()
+    seed = 1 + rank
+    layers = []
+    for name, N, K in wl.llama_shapes():
+        x = wl.llama_activations(M_TOKENS, K, seed=seed, stream=10 + N % 97).to(dev)
+        w = torch.randn(N, K, device=dev, generator=torch.Generator(device=dev).manual_seed(seed * 31 + N),
+                        dtype=torch.float32).mul_(0.02).to(torch.bfloat16)
+        wq, sw = w8.quantize_weight(w)
+        del w
+        xq = torch.empty((M_TOKENS, K), dtype=torch.int8, device=dev)
+        sx = torch.empty(M_TOKENS, dtype=torch.float32, device=dev)
+        y = torch.empty((M_TOKENS, N), dtype=torch.bfloat16, device=dev)
+        layers.append(dict(name=name, N=N, K=K, x=x, wq=wq, sw=sw, xq=xq, sx=sx, y=y))
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    lib = w8.lib()
+    stream = torch.cuda.current_stream()
+    sptr = __import__("ctypes").c_void_p(stream.cuda_stream)
+    P = __import__("ctypes").c_void_p
+
+    def step(record):
+        for L in layers:
+            e0 = torch.cuda.Event(enable_timing=True) if record else None
+            e1 = torch.cuda.Event(enable_timing=True) if record else None
+            e2 = torch.cuda.Event(enable_timing=True) if record else None
+            if record:
+                e0.record()
+            rc = lib.w8a8_quantize_act(P(L["x"].data_ptr()), M_TOKENS, L["K"], L["K"], 0, P(L["xq"].data_ptr()),
+                                       P(L["sx"].data_ptr()), None, sptr)
+            if record:
+                e1.record()
+            rc |= lib.w8a8_scaled_mm(P(L["xq"].data_ptr()), P(L["wq"].data_ptr()), M_TOKENS, L["N"], L["K"], 0,
+                                     P(L["sx"].data_ptr()), None, None, 0, P(L["sw"].data_ptr()), None,
+                                     P(L["y"].data_ptr()), None, sptr)
+            if record:
+                e2.record()
+                L.setdefault("ev", []).append((e0, e1, e2))
+            if rc:
+                raise RuntimeError("library call failed")
+
+    for _ in range(args.warmup):
+        step(False)
+        flush.zero_()
+    torch.cuda.synchronize()
+    barrier(pg)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    wall0 = time.perf_counter()
+    step_events = []
+    for _ in range(args.steps):
+        flush.zero_()           # L2 flush between steps, outside the timed events
+        s0 = torch.cuda.Event(enable_timing=True)
+        s1 = torch.cuda.Event(enable_timing=True)
+        s0.record()
+        step(True)
+        s1.record()
+        step_events.append((s0, s1))
+    torch.cuda.synchronize()
+    wall = time.perf_counter() - wall0
+    clk = clocks.stop()
+    barrier(pg)
+    torch.cuda.synchronize()
+    ms_total = sum(a.elapsed_time(b) for a, b in step_events)
+    ms_total = max_over_ranks(pg, ms_total)
+    ops = step_ops() * args.steps * world
+    value = ops / (ms_total * 1e-3) / 1e12
+    # per-kernel live timings (GEMM = dominant kernel)
+    gemm_ms = 0.0
+    quant_ms = 0.0
+    gemm_flops = 0.0
+    quant_bytes = 0.0
+    per_layer = {}
+    for L in layers:
+        gq = sum(a.elapsed_time(b) for a, b, _ in L["ev"])
+        gg = sum(b.elapsed_time(c) for _, b, c in L["ev"])
+        n = len(L["ev"])
+        quant_ms += gq
+        gemm_ms += gg
+        gemm_flops += 2.0 * M_TOKENS * L["N"] * L["K"] * n
+        quant_bytes += (M_TOKENS * L["K"] * 3 + M_TOKENS * 4) * n
+        per_layer[L["name"]] = {
+            "N": L["N"], "K": L["K"],
+            "gemm_us": round(gg / n * 1e3, 2), "quant_us": round(gq / n * 1e3, 2),
+            "gemm_tflops": round(2.0 * M_TOKENS * L["N"] * L["K"] / (gg / n * 1e-3) / 1e12, 1),
+            "linear_tops": round(2.0 * M_TOKENS * L["N"] * L["K"] / ((gg + gq) / n * 1e-3) / 1e12, 1),
+        }
+    achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    roofline = {
+        "bound": "tensor", "kernel": "gemm_tc_kernel (tcgen05 kind::f16, int8 operands exact in fp16)",
+        "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
+        "traffic": None,
+        "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)",
+        "per_launch_flops": "2*M*N*K of each GEMM launch (M=4096)",
+    }
+    quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9
+    e2e = run_e2e(args, layers, w8, world, pg)
+    comps = None
+    if not args.no_components and rank == 0:
+        comps = components(w8, wl, peaks)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded; random-init weights)",
+        "config": {"workload": "llama3-8b-decoder-linears", "M": M_TOKENS,
+                   "shapes": [[n, N, K] for n, N, K in wl.llama_shapes()],
+                   "act": "dynamic per-token symmetric int8", "weight": "per-channel symmetric int8",
+                   "l2": "flushed between steps (256 MiB write outside the timed events)",
+                   "parallelism": f"replicas x{world} (independent batches)"},
+        "e2e": e2e,
+        "gpu_launches": 2 * len(layers) * args.steps,
+        "roofline": roofline,
+        "kernels": {"quantize_act_gbs": round(quant_gbs, 1), "quantize_act_frac_hbm": round(quant_gbs / float(
+            peaks.get("hbm_gbs", 6800.0)), 4), "per_layer": per_layer},
+        "clocks": clk,
+        "wall_s": round(wall, 3),
+    }
+    if comps is not None:
+        line["components"] = comps
+    return line
+
+
+def run_e2e(args, layers, w8, world, pg):
+    """Same step through the public API with host buffers: pinned H2D of x, the linear, D2H of y."""
+    hx = [L["x"].cpu().pin_memory() for L in layers]
+    hy = [torch.empty(L["y"].shape, dtype=torch.bfloat16).pin_memory() for L in layers]
+    ws = [torch.empty(max(w8.linear_workspace_size(M_TOKENS, L["K"]), 16), dtype=torch.uint8, device="cuda")
+          for L in layers]
+    dx = [torch.empty_like(L["x"]) for L in layers]
+
+    def step():
+        for i, L in enumerate(layers):
+            dx[i].copy_(hx[i], non_blocking=True)
+            w8.linear(dx[i], L["wq"], L["sw"], workspace=ws[i], out=L["y"])
+            hy[i].copy_(L["y"], non_blocking=True)
+
+    for _ in range(max(1, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    barrier(pg)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        step()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = max_over_ranks(pg, e0.elapsed_time(e1))
+    value = step_ops() * args.steps * world / (ms * 1e-3) / 1e12
+    return {"value": round(value, 2), "unit": "TOPS",
+            "h2d_bytes_per_step": int(sum(L["x"].numel() * 2 for L in layers)),
+            "d2h_bytes_per_step": int(sum(L["y"].numel() * 2 for L in layers))}
+
+
+def _time_launches(fn, reps=10, warm=2):
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    evs = []
+    for _ in range(reps):
+        a = torch.cuda.Event(enable_timing=True)
+        b = torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        evs.append((a, b))
+    torch.cuda.synchronize()
+    return statistics.median(a.elapsed_time(b) for a, b in evs)
+
+
+def components(w8, wl, peaks):
+    """Per-row measurements of the other hot-path steps (not part of `value`)."""
+    dev = "cuda"
+    hbm = float(peaks.get("hbm_gbs", 6800.0))
+    tf = float(peaks.get("bf16_tflops", 1900.0))
+    out = {}
+    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    # S1 / S2 quantizers at M = 8192
+    for K in (4096, 14336):
+        x = wl.llama_activations(8192, K, seed=5).to(dev)
+        for mode in ("dyn_sym", "dyn_asym"):
+            def f():
+                flush.zero_()
+            ms_flush = _time_launches(f)
+            ms = _time_launches(lambda: (flush.zero_(), w8.quantize_act(x, mode))) - ms_flush
+            b = 8192 * K * 3 + 8192 * 4 * (2 if mode == "dyn_asym" else 1)
+            out[f"quant_{mode}_M8192_K{K}"] = {"us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                                "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+        del x
+    # S7 weight quantizer on the gate_up weight
+    w = torch.randn(28672, 4096, device=dev, dtype=torch.float32).mul_(0.02).to(torch.bfloat16)
+    ms = _time_launches(lambda: w8.quantize_weight(w, with_azp_adj=True))
+    b = 28672 * 4096 * 3 + 28672 * 8
+    out["quant_weight_28672x4096"] = {"us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                      "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+    del w
+    # S8 requant: 64 x [6144, 4096] + 8 x [3000, 1500], one batched call
+    g = torch.Generator(device=dev).manual_seed(7)
+    mats = []
+    for N, K, cnt in ((6144, 4096, 64), (3000, 1500, 8)):
+        for _ in range(cnt):
+            c = torch.randn(N, K, device=dev, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
+            s = torch.exp(torch.empty((N + 127) // 128, (K + 127) // 128, device=dev).uniform_(
+                np.log(1e-4), np.log(1e-2), generator=g))
+            mats.append((c, s))
+    outs = [(torch.empty(c.shape, dtype=torch.int8, device=dev), torch.empty(c.shape[0], device=dev))
+            for c, _ in mats]
+    ms = _time_launches(lambda: w8.fp8block_to_int8_rowwise_batched(mats, outs), reps=5)
+    b = sum(c.numel() * 2 + c.shape[0] * 4 + s.numel() * 4 for c, s in mats)
+    out["requant_64x6144x4096_plus_8x3000x1500"] = {"us": round(ms * 1e3, 1),
+                                                    "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                                    "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+    del mats, outs
+    # S2/S3 asymmetric linears, K = N = 4096
+    for M in (128, 4096):
+        x = wl.asym_activations(M, 4096, seed=3).to(dev)
+        w = torch.randn(4096, 4096, device=dev).mul_(0.02).to(torch.bfloat16)
+        wq, sw, adj = w8.quantize_weight(w, with_azp_adj=True)
+        ws = torch.empty(w8.linear_workspace_size(M, 4096, "dyn_asym"), dtype=torch.uint8, device=dev)
+        yb = torch.empty(M, 4096, dtype=torch.bfloat16, device=dev)
+        ms = _time_launches(lambda: w8.linear(x, wq, sw, act_mode="dyn_asym", azp_adj=adj, workspace=ws, out=yb))
+        out[f"linear_dyn_asym_M{M}_4096x4096"] = {"us": round(ms * 1e3, 2),
+                                                  "TOPS": round(2 * M * 4096 * 4096 / (ms * 1e-3) / 1e12, 1)}
+    # small-M (weight streaming) linears on the gate_up shape
+    wq = torch.randint(-127, 128, (28672, 4096), dtype=torch.int8, device=dev)
+    sw = torch.rand(28672, device=dev)
+    for M in (1, 16, 128, 1024):
+        x = wl.llama_activations(M, 4096, seed=4).to(dev)
+        ws = torch.empty(max(w8.linear_workspace_size(M, 4096), 16), dtype=torch.uint8, device=dev)
+        yb = torch.empty(M, 28672, dtype=torch.bfloat16, device=dev)
+        f0 = _time_launches(lambda: flush.zero_())
+        ms = _time_launches(lambda: (flush.zero_(), w8.linear(x, wq, sw, workspace=ws, out=yb))) - f0
+        wbytes = 28672 * 4096
+        out[f"linear_M{M}_28672x4096"] = {"us": round(ms * 1e3, 2),
+                                          "TOPS": round(2 * M * 28672 * 4096 / (ms * 1e-3) / 1e12, 2),
+                                          "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1)}
+    # S9 MoE layer (4096 tokens, 32 experts, top-4)
+    md = moe_device_inputs(w8, wl)
+    ms = _time_launches(lambda: w8.moe_forward(*md["args"]), reps=5)
+    out["moe_T4096_E32_top4"] = {"us": round(ms * 1e3, 1), "TOPS": round(md["ops"] / (ms * 1e-3) / 1e12, 1),
+                                 "frac_tensor": round(md["ops"] / (ms * 1e-3) / 1e12 / tf, 3)}
+    return out
+
+
+def moe_device_inputs(w8, wl, T=4096, H=4096, E=32, topk=4, inter=1408):
+    """Routing from the seeded workload, expert weights drawn on the device, rows sorted by expert."""
+    dev = "cuda"
+    d = wl.moe_workload(T=T, H=H, E=E, topk=topk, inter=inter, seed=0, with_weights=False)
+    ids = d["topk_ids"].numpy().reshape(-1)
+    order = np.argsort(ids, kind="stable")
+    counts = np.bincount(ids, minlength=E)
+    seg = np.zeros(E + 1, np.int64)
+    seg[1:] = np.cumsum(counts)
+    row_of = np.zeros(T * topk, np.int64)
+    row_of[order] = np.arange(T * topk)
+    g = torch.Generator(device=dev).manual_seed(11)
+    w13 = torch.randn(E * 2 * inter, H, device=dev, generator=g).mul_(0.02).to(torch.bfloat16)
+    w2 = torch.randn(E * H, inter, device=dev, generator=g).mul_(0.02).to(torch.bfloat16)
+    w13q, s13 = w8.quantize_weight(w13)
+    w2q, s2 = w8.quantize_weight(w2)
+    del w13, w2
+    args = (d["x"].to(dev), torch.from_numpy(order // topk).to(dev), torch.from_numpy(seg).to(dev),
+            torch.from_numpy(row_of.reshape(T, topk)).to(dev), d["topk_w"].to(dev),
+            w13q.view(E, 2 * inter, H), s13.view(E, 2 * inter), w2q.view(E, H, inter), s2.view(E, H))
+    ops = 2.0 * T * topk * (2 * inter * H + H * inter)
+    return {"args": args, "ops": ops}
+
+
+# --------------------------------------------------------------------------- reference arm (CPU oracle)
+def run_reference(args, world, rank):
+    import oracle
+    from w8a8_int8_quantized_gb300 import workloads as wl
+    sample_rows = 32
+    prepared = []
+    for name, N, K in wl.llama_shapes():
+        x = wl.llama_activations(sample_rows, K, seed=1, stream=10 + N % 97)
+        w = wl.weight_bf16(N, K, seed=2)
+        rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+        prepared.append((wl.bits(x), rq, rs, N, K))
+    ops_per_rep = sum(2.0 * sample_rows * N * K for _, _, _, N, K in prepared)
+
+    def rep():
+        for xb, rq, rs, N, K in prepared:
+            oracle.w8a8_linear(xb, rq, rs)
+
+    for _ in range(args.warmup):
+        rep()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        rep()
+    dt = time.perf_counter() - t0
+    value = ops_per_rep * args.steps / dt / 1e12
+    cores = len(os.sched_getaffinity(0))
+    return {
+        "impl": "reference", "metric": METRIC, "value": round(value, 6), "unit": "TOPS", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
+        "data": "synthetic (seeded; random-init weights)",
+        "config": {"workload": "llama3-8b-decoder-linears", "M": M_TOKENS,
+                   "shapes": [[n, N, K] for n, N, K in wl.llama_shapes()]},
+        "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
+                         "sample": f"{sample_rows} of {M_TOKENS} token rows per layer, all four layers, per step"},
+        "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def cpu_baseline_leg():
+    """The oracle as it stands, on a bounded sample of the step (about 10 s of host work)."""
+    import oracle
+    from w8a8_int8_quantized_gb300 import workloads as wl
+    sample_rows = 32
+    prepared = []
+    for name, N, K in wl.llama_shapes():
+        x = wl.llama_activations(sample_rows, K, seed=1)
+        w = wl.weight_bf16(N, K, seed=2)
+        rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+        prepared.append((wl.bits(x), rq, rs, N, K))
+    ops = sum(2.0 * sample_rows * N * K for _, _, _, N, K in prepared)
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        for xb, rq, rs, N, K in prepared:
+            oracle.w8a8_linear(xb, rq, rs)
+        reps += 1
+        if time.perf_counter() - t0 > 8.0:
+            break
+    dt = time.perf_counter() - t0
+    return {"value": round(ops * reps / dt / 1e12, 6), "unit": "TOPS", "cores": len(os.sched_getaffinity(0)),
+            "kind": "oracle",
+            "sample": f"{sample_rows} token rows x 4 Llama-3-8B layers, repeated {reps}x (weights pre-quantized)"}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--no-components", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    world, rank, local, pg = dist_setup(args)
+    if args.impl == "reference":
+        if rank == 0:
+            print(json.dumps(run_reference(args, world, rank)), flush=True)
+        return
+    line = run_ours(args, world, rank, pg)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            line["cpu_baseline"] = cpu_baseline_leg()
+        print(json.dumps(line), flush=True)
+    if pg is not None:
+        pg.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

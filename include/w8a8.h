@@ -1,0 +1,229 @@
+/*
+ * w8a8.h -- C ABI of the GB300 (sm_103a) W8A8 INT8 quantized linear library.
+ *
+ * Sources cited below by short name:
+ *   [vLLM-W8A8]   "vLLM INT8 W8A8 量化实战：用 llm-compressor 制作 8 位权重与 8 位激活的推理模型"
+ *                 (blog.gitcode.com), sections 4.1 方案判定, 4.2 权重布局与 kernel 选择, 4.3 未匹配时的行为.
+ *   [SGLang-CT]   "[SGLang] W4A8, W8A8, W4A4: 혼합 정밀도 양자화 스킴", items 3 (W8A8 INT8) and
+ *                 4 (비대칭 양자화: AZP 보정), and the scheme file tree (MoE INT8).
+ *   [Kunlun-INT8] "MiniMax-M2.7 FP8 转昆仑芯 INT8" README, sections 转换关系 and 验证.
+ *
+ * Conventions shared by every entry point:
+ *   - All pointers are DEVICE pointers unless stated otherwise; the caller owns every
+ *     buffer.  No entry point allocates device memory: scratch, where needed, is a
+ *     caller-provided workspace whose size a *_workspace_size() query returns.
+ *   - Matrices are row-major.  bf16 tensors are passed as void* (2 bytes per element).
+ *   - Work is enqueued on `stream` and is asynchronous; nothing synchronizes.
+ *     Argument errors are detected on the host and returned before any launch.
+ *   - Device-side conditions (illegal FP8 block scales, a bounded wait that ran out) are
+ *     reported through an optional `int32_t* dev_status` word (device memory).  The
+ *     library only ever writes a non-zero w8a8_status code into it (never clears it);
+ *     the caller zeroes it and reads it after synchronizing.  NULL means "not reported".
+ *   - Only GPUs of compute capability 10.3 (GB300) are supported; others get
+ *     W8A8_ERR_UNSUPPORTED.  There is no CPU fallback.
+ *   - int32 accumulation is exact for K <= 131072 (|acc| <= 128*127*K < 2^31); larger K is
+ *     rejected with W8A8_ERR_INVALID_ARG.
+ */
+#ifndef W8A8_H
+#define W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes.  W8A8_ERR_UNSUPPORTED is the counterpart of the NotImplementedError a
+ * scheme lookup raises for an unsupported parameter combination ([vLLM-W8A8] 4.3). */
+typedef enum {
+  W8A8_OK = 0,
+  W8A8_ERR_INVALID_ARG = 1,   /* bad size, null pointer, bad mode */
+  W8A8_ERR_UNSUPPORTED = 2,   /* mode combination or device not supported */
+  W8A8_ERR_MISALIGNED = 3,    /* pointer or leading dimension breaks an alignment rule */
+  W8A8_ERR_BAD_SCALE = 4,     /* device side: illegal FP8 block scale / NaN code */
+  W8A8_ERR_TIMEOUT = 5,       /* device side: a bounded wait inside a kernel ran out */
+  W8A8_ERR_CUDA = 6,          /* a CUDA runtime/driver call failed */
+  W8A8_ERR_WORKSPACE = 7      /* workspace missing or too small */
+} w8a8_status;
+
+/* Activation quantization schemes ([vLLM-W8A8] 4.1: static per-tensor or dynamic
+ * per-token, symmetric or asymmetric activations). */
+typedef enum {
+  W8A8_ACT_DYN_TOKEN_SYM = 0,
+  W8A8_ACT_DYN_TOKEN_ASYM = 1,
+  W8A8_ACT_STATIC_TENSOR_SYM = 2,
+  W8A8_ACT_STATIC_TENSOR_ASYM = 3
+} w8a8_act_mode;
+
+/* Weight scale strategy ([vLLM-W8A8] 4.2: weight_scale [out_features, 1] for CHANNEL,
+ * one value per layer for TENSOR).  Weights are always symmetric ([vLLM-W8A8] 4.1). */
+typedef enum { W8A8_W_CHANNEL = 0, W8A8_W_TENSOR = 1 } w8a8_w_mode;
+
+/* Human-readable name of a status code (static storage, never NULL). */
+const char* w8a8_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int w8a8_version(void);
+
+/* GEMM engine selection for w8a8_scaled_mm / w8a8_linear / w8a8_grouped_mm, a tuning and
+ * testing control that applies to the calling host thread:
+ *   0 = automatic (the warp-MMA weight-streaming kernel for dense calls with M <= 16, the
+ *       tcgen05 kernel otherwise), 1 = always tcgen05, 2 = always the warp-MMA kernel.
+ * Both engines compute the same exact int32 sums and the same epilogue. */
+w8a8_status w8a8_set_gemm_engine(int engine);
+
+/*
+ * w8a8_quantize_act -- activation quantization ([SGLang-CT] item 3, per_token_quant_int8;
+ * per-row rule of [Kunlun-INT8] 转换关系; modes of [vLLM-W8A8] 4.1/4.2).
+ *   x      bf16 [M, K] with row stride ldx (elements, ldx >= K).
+ *   q      int8 [M, K] contiguous (output).
+ *   scale  DYN modes: float [M] output, s[m] = rowabsmax/127 (sym) or (max-min)/255 (asym);
+ *          STATIC modes: float [1] input (the calibrated input_scale).
+ *   zp     DYN_ASYM: int32 [M] output zero points; STATIC_ASYM: int32 [1] input
+ *          (input_zero_point, an int8 value); symmetric modes: ignored (may be NULL).
+ * Rounding: q = clamp(rint(x / s) (+ zp), lo, hi), IEEE float32 division, ties to even;
+ * [lo, hi] = [-127, 127] symmetric, [-128, 127] asymmetric.  All-zero rows give q = 0, s = 1.
+ * The static scale must be finite and positive (results are unspecified otherwise).
+ * M == 0 or K == 0 is a no-op returning W8A8_OK.
+ */
+w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, int mode,
+                              int8_t* q, float* scale, int32_t* zp, cudaStream_t stream);
+
+/*
+ * w8a8_scaled_mm -- INT8 x INT8 -> INT32 GEMM with the fused scale/azp/bias epilogue
+ * ([SGLang-CT] item 3: int8_scaled_mm(x_q, W, x_scale, w_scale, out_dtype, bias);
+ * item 4: azp_adj correction).
+ *   xq      int8 [M, K] contiguous (quantized activations).
+ *   wq      int8 [N, K] contiguous ([vLLM-W8A8] 4.2 layout [out_features, in_features]).
+ *   act_mode  which activation scheme produced xq (w8a8_act_mode):
+ *             DYN_TOKEN_SYM    s_x float [M]; zp, azp_adj unused.
+ *             DYN_TOKEN_ASYM   s_x float [M]; zp int32 [M]; azp_adj int32 [N] = sum_k wq[n,k].
+ *             STATIC_SYM       s_x float [1].
+ *             STATIC_ASYM      s_x float [1]; azp_adj int32 [N] premultiplied by the
+ *                              input zero point; zp unused.
+ *   w_mode  W8A8_W_CHANNEL: s_w float [N];  W8A8_W_TENSOR: s_w float [1].
+ *   bias    bf16 [N] or NULL.
+ *   y       bf16 [M, N] contiguous (output).
+ * Epilogue, float32 with one rounding per step and no fused multiply-add:
+ *   c = acc - zp[m]*azp_adj[n] (exact integer, rounded to float32);
+ *   y = bf16_rne( (s_x[m]*s_w[n]) * c (+ bias[n]) ).
+ * Requirements: K % 16 == 0; xq and wq 16-byte aligned; 1 <= K <= 131072.
+ * dev_status: optional (see conventions); a kernel whose internal wait ran out writes
+ * W8A8_ERR_TIMEOUT there and leaves y unspecified.
+ */
+w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
+                           int act_mode, const float* s_x, const int32_t* zp,
+                           const int32_t* azp_adj, int w_mode, const float* s_w,
+                           const void* bias, void* y, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * w8a8_linear -- the whole layer forward: quantize x (any act_mode) then w8a8_scaled_mm
+ * ([SGLang-CT] item 3 apply_weights; [vLLM-W8A8] 4.2 apply_weights(layer, x, bias)).
+ *   x bf16 [M, K] (row stride ldx); wq/s_w/azp_adj/bias as for w8a8_scaled_mm.
+ *   input_scale / input_zero_point: float [1] / int32 [1] for the static modes, else NULL.
+ *   workspace: device buffer of at least w8a8_linear_workspace_size(M, K, act_mode) bytes,
+ *   16-byte aligned; it holds the quantized activations and their scales between the
+ *   two kernels.
+ */
+size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode);
+w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int act_mode,
+                        const float* input_scale, const int32_t* input_zero_point,
+                        const int8_t* wq, int64_t N, int w_mode, const float* s_w,
+                        const int32_t* azp_adj, const void* bias, void* y,
+                        void* workspace, size_t workspace_bytes,
+                        int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * w8a8_quantize_weight -- per-output-channel symmetric weight quantization
+ * ([vLLM-W8A8] 4.2: int8 weight [out_features, in_features], float32 weight_scale
+ * [out_features, 1]; rule of [Kunlun-INT8] 转换关系: s = rowabsmax/127,
+ * q = clamp(round(W/s), -127, 127), all-zero row -> q = 0, s = 1).
+ *   w bf16 [N, K] contiguous;  wq int8 [N, K] (output);  s_w float [N] (output);
+ *   azp_adj int32 [N] (optional output, NULL to skip): sum_k wq[n, k] ([SGLang-CT] item 4).
+ */
+w8a8_status w8a8_quantize_weight(const void* w, int64_t N, int64_t K, int8_t* wq, float* s_w,
+                                 int32_t* azp_adj, cudaStream_t stream);
+
+/*
+ * w8a8_azp_adj -- azp_adj[n] = input_zero_point * sum_k wq[n, k] for an int8 weight that
+ * is already quantized ([SGLang-CT] item 4: computed once after loading; premultiplied by
+ * the zero point for the static scheme).  input_zero_point: int32 [1] device value, or
+ * NULL for the plain column sum used by the dynamic asymmetric scheme.
+ */
+w8a8_status w8a8_azp_adj(const int8_t* wq, int64_t N, int64_t K, const int32_t* input_zero_point,
+                         int32_t* azp_adj, cudaStream_t stream);
+
+/*
+ * fp8block_to_int8_rowwise -- FP8 E4M3 block-scaled weight -> INT8 weight with one float32
+ * scale per output row ([Kunlun-INT8] 转换关系):
+ *   Wf[i,j] = e4m3(w[i,j]) * scale_inv[i/128, j/128]   (the "_inv" scale multiplies)
+ *   s[i] = max_j |Wf[i,j]| / 127;  q = clamp(rint(Wf / s), -127, 127);
+ *   all-zero row -> q = 0, s = 1.
+ *   w         uint8 [N, K] E4M3 codes (the "fn" encoding: no infinities, 0x7F/0xFF NaN).
+ *   scale_inv float [ceil(N/128), ceil(K/128)] row-major.
+ *   q int8 [N, K], s float [N] (outputs).  Any K >= 1 is accepted, aligned or not.
+ * A row touching a non-finite or <= 0 block scale, holding a NaN code, or whose dequantized
+ * values overflow, gets q = 0, s = 1 and W8A8_ERR_BAD_SCALE is written to dev_status
+ * ([Kunlun-INT8] 验证 tests illegal scales).
+ */
+w8a8_status fp8block_to_int8_rowwise(const uint8_t* w, const float* scale_inv, int64_t N, int64_t K,
+                                     int8_t* q, float* s, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * fp8block_to_int8_rowwise_batched -- the same for `count` matrices in one launch per up to
+ * 64 matrices.  The four pointer arrays and the N/K arrays are HOST arrays of length count
+ * holding device pointers / sizes; they are read before the call returns.
+ */
+w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,
+                                             const float* const* scale_inv, const int64_t* N,
+                                             const int64_t* K, int8_t* const* q, float* const* s,
+                                             int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * w8a8_grouped_mm -- MoE expert GEMMs over token-sorted segments ([SGLang-CT] MoE INT8
+ * scheme; [Kunlun-INT8] W8A8 MoE method with per-channel symmetric expert weights and
+ * per-token dynamic symmetric activations).  Rows [seg[e], seg[e+1]) of xq_sorted belong to
+ * expert e and are multiplied by that expert's weight:
+ *   y[r, :] = bf16( s_x[r] * s_w[e, n] * sum_k xq_sorted[r, k] * w[e, n, k] ).
+ *   xq_sorted int8 [R, K];  s_x float [R];  w int8 [E, N, K];  s_w float [E, N];
+ *   seg_offsets int64 [E+1] (DEVICE array, non-decreasing, seg[0] = 0, seg[E] = R);
+ *   y bf16 [R, N].  R is seg[E]; max_rows is a host-side upper bound on R used to size the
+ *   launch (pass R when known).  Requirements as for w8a8_scaled_mm.
+ */
+w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int8_t* w,
+                            const float* s_w, const int64_t* seg_offsets, int E, int64_t max_rows,
+                            int64_t N, int64_t K, void* y, int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * w8a8_moe_quantize_gather -- per-token symmetric quantization of x rows taken in expert-
+ * sorted order: for r in [0, R): (xq_sorted[r], s_x[r]) = quantize(x[row_index[r]]).
+ *   x bf16 [T, K] (row stride ldx);  row_index int64 [R] (device);  xq_sorted int8 [R, K];
+ *   s_x float [R].  Same rounding as w8a8_quantize_act in mode DYN_TOKEN_SYM.
+ */
+w8a8_status w8a8_moe_quantize_gather(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                     const int64_t* row_index, int64_t R, int8_t* xq_sorted,
+                                     float* s_x, cudaStream_t stream);
+
+/*
+ * w8a8_silu_mul_quant -- glue between the two expert GEMMs: g = bf16(silu(h[:, :I]) * h[:, I:])
+ * in float32 (gate columns first), then per-row symmetric quantization of g.
+ *   h bf16 [R, 2I];  gq int8 [R, I];  s_g float [R].  I % 8 == 0.
+ */
+w8a8_status w8a8_silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, float* s_g,
+                                cudaStream_t stream);
+
+/*
+ * w8a8_moe_combine -- y[t, :] = bf16( sum_{j < topk} topk_w[t, j] * out[row_of[t, j], :] ),
+ * float32, slots in order, one multiply and one add per slot.
+ *   out bf16 [R, H];  row_of int64 [T, topk];  topk_w float [T, topk];  y bf16 [T, H].
+ */
+w8a8_status w8a8_moe_combine(const void* out, const int64_t* row_of, const float* topk_w,
+                             int64_t T, int topk, int64_t H, void* y, cudaStream_t stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* W8A8_H */

@@ -1,0 +1,81 @@
+"""The C-ABI library builds, loads, and exports every function include/w8a8.h declares.
+
+No compute call is made here (these run without a GPU).
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from w8a8_int8_quantized_gb300 import build as wbuild
+from w8a8_int8_quantized_gb300 import _binding
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def header_functions():
+    names = set()
+    inc = os.path.join(ROOT, "include")
+    for f in os.listdir(inc):
+        if not f.endswith(".h"):
+            continue
+        src = open(os.path.join(inc, f)).read()
+        src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", "", src)
+        src = re.sub(r"#[^\n]*", "", src)
+        for m in re.finditer(r"\b([A-Za-z_]\w*)\s*\(([^;{}]*)\)\s*;", src):
+            names.add(m.group(1))
+    return names
+
+
+@pytest.fixture(scope="module")
+def libpath():
+    return wbuild.build()
+
+
+def test_header_declares_the_entry_points():
+    names = header_functions()
+    for n in ["w8a8_quantize_act", "w8a8_scaled_mm", "w8a8_linear", "w8a8_quantize_weight", "w8a8_azp_adj",
+              "fp8block_to_int8_rowwise", "fp8block_to_int8_rowwise_batched", "w8a8_grouped_mm"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(libpath):
+    lib = ctypes.CDLL(libpath)
+    missing = [n for n in sorted(header_functions()) if not hasattr(lib, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_the_header():
+    assert set(_binding.SIGNATURES) == header_functions()
+
+
+def test_status_strings_without_gpu(libpath):
+    lib = ctypes.CDLL(libpath)
+    lib.w8a8_status_string.restype = ctypes.c_char_p
+    assert lib.w8a8_status_string(0) == b"ok"
+    assert lib.w8a8_status_string(4).startswith(b"illegal")
+    assert lib.w8a8_status_string(99) == b"unknown status"
+
+
+def test_host_side_argument_checks_need_no_gpu(libpath):
+    """Argument errors are returned before any CUDA call, so they work on a GPU-less host."""
+    lib = _binding.lib()
+    # K not a multiple of 16
+    assert lib.w8a8_scaled_mm(None, None, 4, 4, 24, 0, None, None, None, 0, None, None, None, None, None) == 3
+    # negative sizes / bad mode
+    assert lib.w8a8_quantize_act(None, -1, 4, 4, 0, None, None, None, None) == 1
+    assert lib.w8a8_quantize_act(None, 1, 4, 4, 9, None, None, None, None) == 1
+    # empty problems are no-ops
+    assert lib.w8a8_quantize_act(None, 0, 4, 4, 0, None, None, None, None) == 0
+    assert lib.w8a8_scaled_mm(None, None, 0, 4, 16, 0, None, None, None, 0, None, None, None, None, None) == 0
+    # asymmetric GEMM without azp_adj
+    p = ctypes.c_void_p(16)
+    assert lib.w8a8_scaled_mm(p, p, 4, 4, 16, 1, p, p, None, 0, p, None, p, None, None) == 1
+    # workspace too small
+    assert lib.w8a8_linear(p, 4, 16, 16, 0, None, None, p, 4, 0, p, None, None, p, p, 8, None, None) == 7
+    assert lib.w8a8_linear_workspace_size(4, 16, 0) == 256 + 256
+    assert lib.w8a8_set_gemm_engine(5) == 1
+    assert lib.w8a8_set_gemm_engine(0) == 0

@@ -1,0 +1,357 @@
+"""Parity of the CUDA kernels (through the C ABI) with the CPU oracle.
+
+Integer results (int8 codes, int32 zero points and column sums) and float32 scales must
+match bit for bit.  bf16 outputs must satisfy the stated tolerance -- |y - y_ref| <=
+1e-2*|y_ref| or <= 1e-3*||y_ref32[m, :]||_2 per row -- and, because the epilogue follows
+the oracle's float32 operation order, are also checked for exact equality where the
+inputs to the epilogue are identical.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_int8_quantized_gb300 as w8
+from w8a8_int8_quantized_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def npbits(t):
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def check_bf16(y_gpu, y_bits_ref, y32_ref, exact=True):
+    got = oracle.bf16_bits_to_f32(npbits(y_gpu)).astype(np.float64)
+    ref = oracle.bf16_bits_to_f32(y_bits_ref).astype(np.float64)
+    rownorm = np.linalg.norm(y32_ref.astype(np.float64), axis=1, keepdims=True)
+    err = np.abs(got - ref)
+    ok = (err <= 1e-2 * np.abs(ref)) | (err <= 1e-3 * rownorm)
+    assert ok.all(), f"{(~ok).sum()} outputs outside tolerance; max err {err.max()}"
+    if exact:
+        mism = (npbits(y_gpu) != y_bits_ref).sum()
+        assert mism == 0, f"{mism} bf16 outputs differ from the oracle bit pattern"
+
+
+@pytest.fixture(autouse=True)
+def _engine_reset():
+    w8.set_gemm_engine(0)
+    yield
+    w8.set_gemm_engine(0)
+
+
+# ------------------------------------------------------------------ quantizers
+
+@pytest.mark.parametrize("M,K", [(16, 512), (37, 4096), (5, 14336), (3, 1500), (2, 20000), (1, 8)])
+def test_quantize_act_dyn_sym(M, K):
+    x = wl.llama_activations(M, K, seed=M + K)
+    x[0, : min(K, 7)] = 0
+    if M > 2:
+        x[2] = 0  # all-zero row
+    q, s, _ = w8.quantize_act(x.to(DEV), "dyn_sym")
+    rq, rs = oracle.quantize_act_dynamic_symmetric(x.float().numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+
+
+@pytest.mark.parametrize("M,K", [(16, 512), (64, 4096), (3, 1500)])
+def test_quantize_act_dyn_asym(M, K):
+    x = wl.asym_activations(M, K, seed=K)
+    x[1] = 2.0          # constant row
+    if M > 2:
+        x[2] = 0.0      # zero row
+    q, s, zp = w8.quantize_act(x.to(DEV), "dyn_asym")
+    rq, rs, rz = oracle.quantize_act_dynamic_asymmetric(x.float().numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(zp.cpu().numpy(), rz)
+
+
+@pytest.mark.parametrize("M,K", [(16, 512), (128, 4096), (3, 1500)])
+def test_quantize_act_static(M, K):
+    x = wl.asym_activations(M, K, seed=K + 1)
+    xs = x.float().numpy()
+    sc, z = oracle.static_scale_from_tensor(xs)
+    scale = torch.tensor([sc], dtype=torch.float32, device=DEV)
+    zp = torch.tensor([z], dtype=torch.int32, device=DEV)
+    q, _, _ = w8.quantize_act(x.to(DEV), "static_sym", scale=scale)
+    np.testing.assert_array_equal(q.cpu().numpy(), oracle.quantize_act_static_symmetric(xs, sc))
+    q, _, _ = w8.quantize_act(x.to(DEV), "static_asym", scale=scale, zp=zp)
+    np.testing.assert_array_equal(q.cpu().numpy(), oracle.quantize_act_static_asymmetric(xs, sc, z))
+    # a tiny static scale drives every value into the clamp
+    tiny = torch.tensor([1e-30], dtype=torch.float32, device=DEV)
+    q, _, _ = w8.quantize_act(x.to(DEV), "static_asym", scale=tiny, zp=zp)
+    np.testing.assert_array_equal(q.cpu().numpy(), oracle.quantize_act_static_asymmetric(xs, np.float32(1e-30), z))
+
+
+@pytest.mark.parametrize("N,K", [(512, 512), (300, 4096), (64, 1500)])
+def test_quantize_weight_and_azp(N, K):
+    w = wl.weight_bf16(N, K, seed=N)
+    w[3] = 0
+    wq, s, adj = w8.quantize_weight(w.to(DEV), with_azp_adj=True)
+    rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+    np.testing.assert_array_equal(wq.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(adj.cpu().numpy(), oracle.azp_adj(rq))
+    z = torch.tensor([-37], dtype=torch.int32, device=DEV)
+    np.testing.assert_array_equal(w8.azp_adj(wq, z).cpu().numpy(), oracle.azp_adj(rq, -37))
+    np.testing.assert_array_equal(w8.azp_adj(wq).cpu().numpy(), oracle.azp_adj(rq))
+
+
+# ------------------------------------------------------------------ GEMM + epilogue
+
+def _gemm_case(M, N, K, seed, act="dyn_sym", bias=True, w_mode=w8.W_CHANNEL):
+    x = wl.asym_activations(M, K, seed=seed) if "asym" in act else wl.llama_activations(M, K, seed=seed)
+    w = wl.weight_bf16(N, K, seed=seed + 1)
+    b = wl.weight_bf16(1, N, seed=seed + 2, std=0.1)[0] if bias else None
+    xb = wl.bits(x)
+    rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+    if w_mode == w8.W_TENSOR:
+        rs = np.array([np.float32(rs.max())], dtype=np.float32)
+    inputs = dict(x=x, w=w, b=b, xb=xb, rq=rq, rs=rs)
+    return inputs
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+@pytest.mark.parametrize("M,N,K", [(16, 512, 512), (1, 256, 64), (300, 520, 1040), (129, 257, 2064),
+                                   (256, 512, 4096), (7, 1000, 4112)])
+def test_scaled_mm_dyn_sym(engine, M, N, K):
+    d = _gemm_case(M, N, K, seed=M * 7 + N)
+    w8.set_gemm_engine(engine)
+    xq, sx, _ = w8.quantize_act(d["x"].to(DEV), "dyn_sym")
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    bias = d["b"].to(DEV) if d["b"] is not None else None
+    y = w8.scaled_mm(xq, wq, sx, sw, "dyn_sym", bias=bias)
+    r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]) if d["b"] is not None else None)
+    check_bf16(y, r["y_bits"], r["y32"])
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+@pytest.mark.parametrize("act", ["dyn_asym", "static_sym", "static_asym"])
+@pytest.mark.parametrize("w_mode", [w8.W_CHANNEL, w8.W_TENSOR])
+def test_linear_modes(engine, act, w_mode):
+    M, N, K = 130, 384, 1088
+    d = _gemm_case(M, N, K, seed=11, act=act, w_mode=w_mode)
+    w8.set_gemm_engine(engine)
+    xs = d["x"].float().numpy()
+    sc, z = oracle.static_scale_from_tensor(xs)
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    bias = d["b"].to(DEV)
+    kw = {}
+    if act == "dyn_asym":
+        kw["azp_adj"] = w8.azp_adj(wq)
+    if act.startswith("static"):
+        kw["input_scale"] = torch.tensor([sc], dtype=torch.float32, device=DEV)
+    if act == "static_asym":
+        kw["input_zero_point"] = torch.tensor([z], dtype=torch.int32, device=DEV)
+        kw["azp_adj"] = w8.azp_adj(wq, kw["input_zero_point"])
+    y = w8.linear(d["x"].to(DEV), wq, sw, act_mode=act, bias=bias, w_mode=w_mode, **kw)
+    r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]), mode=act,
+                           input_scale=sc, input_zero_point=z)
+    check_bf16(y, r["y_bits"], r["y32"])
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+def test_gemm_extremes_exact(engine):
+    """Largest int32 magnitudes: acc = +-128*127*K at K = 14336 must be exact."""
+    w8.set_gemm_engine(engine)
+    M, N, K = 130, 260, 14336
+    xq = torch.full((M, K), -128, dtype=torch.int8)
+    xq[1::2] = 127
+    xq[5, ::3] = -1
+    wq = torch.full((N, K), 127, dtype=torch.int8)
+    wq[1::2] = -127
+    wq[7, 1000:] = 3
+    sx = torch.full((M,), 1.0, dtype=torch.float32)
+    sw = torch.full((N,), 2.0 ** -20, dtype=torch.float32)
+    zp = torch.arange(M, dtype=torch.int32) - 60
+    adj = torch.from_numpy(oracle.azp_adj(wq.numpy()))
+    y = w8.scaled_mm(xq.to(DEV), wq.to(DEV), sx.to(DEV), sw.to(DEV), "dyn_asym", zp=zp.to(DEV), azp_adj=adj.to(DEV))
+    acc = oracle.int8_gemm(xq.numpy(), wq.numpy())
+    yb, y32 = oracle.scaled_mm_epilogue(acc, sx.numpy(), sw.numpy(), zp=zp.numpy(), adj=adj.numpy())
+    check_bf16(y, yb, y32)
+
+
+def test_engines_agree_bitwise():
+    d = _gemm_case(48, 768, 3072, seed=5)
+    xq, sx, _ = w8.quantize_act(d["x"].to(DEV), "dyn_sym")
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    w8.set_gemm_engine(1)
+    a = w8.scaled_mm(xq, wq, sx, sw)
+    w8.set_gemm_engine(2)
+    b = w8.scaled_mm(xq, wq, sx, sw)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+# ------------------------------------------------------------------ tiny config (config 1)
+
+def test_tiny_linear_config():
+    d = wl.tiny_linear(seed=0)
+    wq, sw = w8.quantize_weight(d["w"].to(DEV))
+    rq, rs = oracle.quantize_weight_per_channel(d["w"].float().numpy())
+    np.testing.assert_array_equal(wq.cpu().numpy(), rq)
+    y = w8.linear(d["x"].to(DEV), wq, sw, bias=d["bias"].to(DEV))
+    r = oracle.w8a8_linear(wl.bits(d["x"]), rq, rs, bias_bits=wl.bits(d["bias"]))
+    check_bf16(y, r["y_bits"], r["y32"])
+
+
+# ------------------------------------------------------------------ Llama shapes at full size, sampled rows
+
+@pytest.mark.parametrize("name,N,K", wl.llama_shapes())
+def test_llama_full_size_sampled(name, N, K):
+    M = 4096
+    x = wl.llama_activations(M, K, seed=1)
+    w = wl.weight_bf16(N, K, seed=2)
+    wq, sw = w8.quantize_weight(w.to(DEV))
+    y = w8.linear(x.to(DEV), wq, sw)
+    torch.cuda.synchronize()
+    rows = np.random.default_rng(N + K).choice(M, 24, replace=False)
+    rows = np.concatenate([rows, [0, M - 1]])
+    rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+    np.testing.assert_array_equal(sw.cpu().numpy(), rs)
+    r = oracle.w8a8_linear(wl.bits(x)[rows], rq, rs)
+    check_bf16(y[torch.from_numpy(rows).to(DEV)], r["y_bits"], r["y32"])
+
+
+# ------------------------------------------------------------------ FP8 -> INT8 requant
+
+@pytest.mark.parametrize("N,K", [(256, 4096), (300, 1500), (129, 1500), (5, 17), (384, 512)])
+def test_fp8_requant(N, K):
+    codes, sinv, _ = wl.fp8_block_matrix(N, K, seed=3, stream=N + K, zero_frac=0.01)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, s = w8.fp8block_to_int8_rowwise(codes.to(DEV), sinv.to(DEV), status=st)
+    rq, rs, bad = oracle.fp8_block_to_int8_rowwise(codes.numpy(), sinv.numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    assert int(st.item()) == 0 and not bad.any()
+
+
+@pytest.mark.parametrize("bad_val", [0.0, -1.0, float("inf"), float("nan")])
+def test_fp8_requant_illegal_scale(bad_val):
+    codes, sinv, _ = wl.fp8_block_matrix(256, 384, seed=2, stream=9, zero_frac=0.0)
+    c, si = codes.clone(), sinv.clone()
+    si[1, 2] = bad_val
+    c[5, 7] = 0x7F
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, s = w8.fp8block_to_int8_rowwise(c.to(DEV), si.to(DEV), status=st)
+    rq, rs, bad = oracle.fp8_block_to_int8_rowwise(c.numpy(), si.numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    assert int(st.item()) == 4
+
+
+def test_fp8_requant_batched_mixed():
+    mats = [wl.fp8_block_matrix(*shape, seed=4, stream=i) for i, shape in
+            enumerate([(512, 4096), (300, 1500), (64, 4096), (3000, 1500), (130, 4112)])]
+    dev = [(c.to(DEV), s.to(DEV)) for c, s, _ in mats]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = w8.fp8block_to_int8_rowwise_batched(dev, status=st)
+    for (c, s, _), (q, sq) in zip(mats, outs):
+        rq, rs, _ = oracle.fp8_block_to_int8_rowwise(c.numpy(), s.numpy())
+        np.testing.assert_array_equal(q.cpu().numpy(), rq)
+        np.testing.assert_array_equal(sq.cpu().numpy(), rs)
+    assert int(st.item()) == 0
+
+
+def test_fp8_requant_full_config_sampled():
+    """The requant workload (64 x [6144,4096] + 8 x [3000,1500]) in its batched launch;
+    sampled rows of every matrix against the oracle, zero rows checked exactly."""
+    mats = wl.requant_workload(n_big=64, n_ragged=8)
+    dev = [(c.to(DEV), s.to(DEV)) for c, s, _ in mats]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = w8.fp8block_to_int8_rowwise_batched(dev, status=st)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(0)
+    for (c, s, zr), (q, sq) in zip(mats, outs):
+        N = c.shape[0]
+        rows = np.unique(np.concatenate([rng.choice(N, 6, replace=False), zr.numpy()[:2], [N - 1]]))
+        rb = (rows // 128)
+        # oracle on the sampled rows: give each row its own block-row of scales
+        rq = np.zeros((len(rows), c.shape[1]), np.int8)
+        rs = np.zeros(len(rows), np.float32)
+        cn, sn = c.numpy(), s.numpy()
+        for j, i in enumerate(rows):
+            qq, ss, _ = oracle.fp8_block_to_int8_rowwise(cn[i:i + 1], sn[rb[j]:rb[j] + 1])
+            rq[j], rs[j] = qq[0], ss[0]
+        idx = torch.from_numpy(rows).to(DEV)
+        np.testing.assert_array_equal(q[idx].cpu().numpy(), rq)
+        np.testing.assert_array_equal(sq[idx].cpu().numpy(), rs)
+        zrows = zr.to(DEV)
+        assert torch.all(sq[zrows] == 1.0) and not q[zrows].any()
+    assert int(st.item()) == 0
+
+
+# ------------------------------------------------------------------ MoE
+
+def _moe_setup(T, H, E, topk, inter, seed):
+    d = wl.moe_workload(T=T, H=H, E=E, topk=topk, inter=inter, seed=seed)
+    ids = d["topk_ids"].numpy()
+    tok, slot, seg = oracle.moe_sort(ids, E)
+    row_of = np.zeros((T, topk), np.int64)
+    row_of[tok, slot] = np.arange(len(tok))
+    w13q, s13 = w8.quantize_weight(d["w13"].reshape(E * 2 * inter, H).to(DEV))
+    w2q, s2 = w8.quantize_weight(d["w2"].reshape(E * H, inter).to(DEV))
+    dev = dict(x=d["x"].to(DEV), row_index=torch.from_numpy(tok).to(DEV), seg=torch.from_numpy(seg).to(DEV),
+               row_of=torch.from_numpy(row_of).to(DEV), topk_w=d["topk_w"].to(DEV),
+               w13=w13q.view(E, 2 * inter, H), s13=s13.view(E, 2 * inter), w2=w2q.view(E, H, inter),
+               s2=s2.view(E, H))
+    return d, dev, tok, seg
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+def test_moe_small_full_compare(engine):
+    w8.set_gemm_engine(engine)
+    T, H, E, k, inter = 96, 256, 8, 2, 128
+    d, dev, tok, seg = _moe_setup(T, H, E, k, inter, seed=7)
+    y, h, o = w8.moe_forward(dev["x"], dev["row_index"], dev["seg"], dev["row_of"], dev["topk_w"], dev["w13"],
+                             dev["s13"], dev["w2"], dev["s2"])
+    r = oracle.moe_forward(wl.bits(d["x"]), d["topk_ids"].numpy(), d["topk_w"].numpy(),
+                           dev["w13"].cpu().numpy(), dev["s13"].cpu().numpy(), dev["w2"].cpu().numpy(),
+                           dev["s2"].cpu().numpy())
+    # the first expert GEMM sees identical int8 inputs: exact
+    np.testing.assert_array_equal(npbits(h), r["h_bits"])
+    # after the fp32 SiLU glue, compare within the stated bf16 tolerance
+    y32 = oracle.bf16_bits_to_f32(r["y_bits"])
+    check_bf16(y, r["y_bits"], y32, exact=False)
+
+
+def test_moe_full_config_sampled():
+    T, H, E, k, inter = 4096, 4096, 32, 4, 1408
+    d, dev, tok, seg = _moe_setup(T, H, E, k, inter, seed=0)
+    assert seg[-1] == T * k
+    y, h, o = w8.moe_forward(dev["x"], dev["row_index"], dev["seg"], dev["row_of"], dev["topk_w"], dev["w13"],
+                             dev["s13"], dev["w2"], dev["s2"])
+    torch.cuda.synchronize()
+    rows = np.concatenate([np.random.default_rng(1).choice(T, 6, replace=False), [0, T - 1]])
+    r = oracle.moe_forward(wl.bits(d["x"]), d["topk_ids"].numpy(), d["topk_w"].numpy(),
+                           dev["w13"].cpu().numpy(), dev["s13"].cpu().numpy(), dev["w2"].cpu().numpy(),
+                           dev["s2"].cpu().numpy(), rows=rows)
+    sel_rows = np.nonzero(np.isin(tok, rows))[0]
+    np.testing.assert_array_equal(npbits(h)[sel_rows], r["h_bits"][sel_rows])
+    y32 = oracle.bf16_bits_to_f32(r["y_bits"][rows])
+    check_bf16(y[torch.from_numpy(rows).to(DEV)], r["y_bits"][rows], y32, exact=False)
+
+
+def test_grouped_mm_empty_segments():
+    E, N, K = 5, 256, 512
+    seg = torch.tensor([0, 0, 130, 130, 131, 300], dtype=torch.int64)
+    R = 300
+    xq = torch.randint(-127, 128, (R, K), dtype=torch.int8)
+    wq = torch.randint(-127, 128, (E, N, K), dtype=torch.int8)
+    sx = torch.rand(R, dtype=torch.float32)
+    sw = torch.rand(E, N, dtype=torch.float32) * 1e-3
+    y = w8.grouped_mm(xq.to(DEV), sx.to(DEV), wq.to(DEV), sw.to(DEV), seg.to(DEV))
+    for e in range(E):
+        a, b = int(seg[e]), int(seg[e + 1])
+        if a == b:
+            continue
+        acc = oracle.int8_gemm(xq[a:b].numpy(), wq[e].numpy())
+        yb, y32 = oracle.scaled_mm_epilogue(acc, sx[a:b].numpy(), sw[e].numpy())
+        check_bf16(y[a:b], yb, y32)

@@ -1,0 +1,290 @@
+"""ctypes binding of libw8a8.so: argument marshalling only.
+
+Every function here checks tensor devices/dtypes/shapes, allocates outputs with torch
+(device memory is PyTorch's job), and calls the C entry point of the same name on the
+current CUDA stream.  All arithmetic runs in the library's CUDA kernels; if the library
+is missing or fails to load, every call raises.
+"""
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libw8a8.so")
+
+ACT_DYN_TOKEN_SYM = 0
+ACT_DYN_TOKEN_ASYM = 1
+ACT_STATIC_TENSOR_SYM = 2
+ACT_STATIC_TENSOR_ASYM = 3
+W_CHANNEL = 0
+W_TENSOR = 1
+
+_ACT_NAMES = {"dyn_sym": 0, "dyn_asym": 1, "static_sym": 2, "static_asym": 3}
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_I = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+# name -> (restype, argtypes)
+SIGNATURES = {
+    "w8a8_status_string": (ctypes.c_char_p, [_I]),
+    "w8a8_version": (_I, []),
+    "w8a8_set_gemm_engine": (_I, [_I]),
+    "w8a8_quantize_act": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
+    "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "w8a8_linear_workspace_size": (_SZ, [_I64, _I64, _I]),
+    "w8a8_linear": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "w8a8_quantize_weight": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "w8a8_azp_adj": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "fp8block_to_int8_rowwise": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
+    "fp8block_to_int8_rowwise_batched": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "w8a8_grouped_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
+    "w8a8_moe_quantize_gather": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "w8a8_silu_mul_quant": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "w8a8_moe_combine": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _P]),
+}
+
+_lib = None
+
+
+class W8A8Error(RuntimeError):
+    def __init__(self, fn, code, msg):
+        super().__init__(f"{fn} failed: {msg} (status {code})")
+        self.code = code
+
+
+def lib():
+    """Load libw8a8.so (raises if it is not built or cannot be loaded)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m w8a8_int8_quantized_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in SIGNATURES.items():
+            f = getattr(L, name)
+            f.restype = res
+            f.argtypes = args
+        _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream():
+    return ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+
+
+def _check(name, code):
+    if code != 0:
+        raise W8A8Error(name, code, lib().w8a8_status_string(code).decode())
+
+
+def _need(t, dtype, name, dim=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if dim is not None and t.dim() != dim:
+        raise ValueError(f"{name} must have {dim} dims")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def _mode(m):
+    return _ACT_NAMES[m] if isinstance(m, str) else int(m)
+
+
+def set_gemm_engine(engine):
+    """0 automatic, 1 tcgen05, 2 warp-MMA (applies to the calling thread)."""
+    _check("w8a8_set_gemm_engine", lib().w8a8_set_gemm_engine(int(engine)))
+
+
+def quantize_act(x, mode="dyn_sym", scale=None, zp=None):
+    """Quantize bf16 activations [M, K].  Returns (q int8, scale float32, zp int32|None)."""
+    _need(x, torch.bfloat16, "x", 2)
+    m = _mode(mode)
+    M, K = x.shape
+    q = torch.empty((M, K), dtype=torch.int8, device=x.device)
+    if m in (ACT_DYN_TOKEN_SYM, ACT_DYN_TOKEN_ASYM):
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+        zp = torch.empty(M, dtype=torch.int32, device=x.device) if m == ACT_DYN_TOKEN_ASYM else None
+    else:
+        _need(scale, torch.float32, "scale")
+        if m == ACT_STATIC_TENSOR_ASYM:
+            _need(zp, torch.int32, "zp")
+    _check("w8a8_quantize_act", lib().w8a8_quantize_act(_ptr(x), M, K, K, m, _ptr(q), _ptr(scale), _ptr(zp),
+                                                        _stream()))
+    return q, scale, zp
+
+
+def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mode=W_CHANNEL, bias=None,
+              out=None, status=None):
+    """y[M, N] bf16 = epilogue(xq @ wq.T) (see w8a8_scaled_mm in include/w8a8.h)."""
+    _need(xq, torch.int8, "xq", 2)
+    _need(wq, torch.int8, "wq", 2)
+    M, K = xq.shape
+    N = wq.shape[0]
+    if wq.shape[1] != K:
+        raise ValueError("K mismatch")
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    code = lib().w8a8_scaled_mm(_ptr(xq), _ptr(wq), M, N, K, _mode(act_mode), _ptr(s_x), _ptr(zp), _ptr(azp_adj),
+                                int(w_mode), _ptr(s_w), _ptr(bias), _ptr(out), _ptr(status), _stream())
+    _check("w8a8_scaled_mm", code)
+    return out
+
+
+def linear_workspace_size(M, K, act_mode="dyn_sym"):
+    return int(lib().w8a8_linear_workspace_size(M, K, _mode(act_mode)))
+
+
+def linear(x, wq, s_w, act_mode="dyn_sym", input_scale=None, input_zero_point=None, azp_adj=None, bias=None,
+           w_mode=W_CHANNEL, workspace=None, out=None, status=None):
+    """Whole W8A8 linear: y = epilogue(quant(x) @ wq.T)."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(wq, torch.int8, "wq", 2)
+    M, K = x.shape
+    N = wq.shape[0]
+    m = _mode(act_mode)
+    need = linear_workspace_size(M, K, m)
+    if workspace is None:
+        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    if out is None:
+        out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    code = lib().w8a8_linear(_ptr(x), M, K, K, m, _ptr(input_scale), _ptr(input_zero_point), _ptr(wq), N,
+                             int(w_mode), _ptr(s_w), _ptr(azp_adj), _ptr(bias), _ptr(out), _ptr(workspace),
+                             workspace.numel(), _ptr(status), _stream())
+    _check("w8a8_linear", code)
+    return out
+
+
+def quantize_weight(w, with_azp_adj=False):
+    """Per-channel symmetric int8 weight.  Returns (wq, s_w[, azp_adj])."""
+    _need(w, torch.bfloat16, "w", 2)
+    N, K = w.shape
+    wq = torch.empty((N, K), dtype=torch.int8, device=w.device)
+    s = torch.empty(N, dtype=torch.float32, device=w.device)
+    adj = torch.empty(N, dtype=torch.int32, device=w.device) if with_azp_adj else None
+    _check("w8a8_quantize_weight", lib().w8a8_quantize_weight(_ptr(w), N, K, _ptr(wq), _ptr(s), _ptr(adj),
+                                                              _stream()))
+    return (wq, s, adj) if with_azp_adj else (wq, s)
+
+
+def azp_adj(wq, input_zero_point=None):
+    """azp_adj[n] = (zp *) sum_k wq[n, k], int32."""
+    _need(wq, torch.int8, "wq", 2)
+    N, K = wq.shape
+    out = torch.empty(N, dtype=torch.int32, device=wq.device)
+    _check("w8a8_azp_adj", lib().w8a8_azp_adj(_ptr(wq), N, K, _ptr(input_zero_point), _ptr(out), _stream()))
+    return out
+
+
+def fp8block_to_int8_rowwise(codes, scale_inv, status=None):
+    """FP8 E4M3 codes (uint8 [N, K]) + block scales -> (q int8 [N, K], s float32 [N])."""
+    _need(codes, torch.uint8, "codes", 2)
+    _need(scale_inv, torch.float32, "scale_inv", 2)
+    N, K = codes.shape
+    q = torch.empty((N, K), dtype=torch.int8, device=codes.device)
+    s = torch.empty(N, dtype=torch.float32, device=codes.device)
+    _check("fp8block_to_int8_rowwise", lib().fp8block_to_int8_rowwise(_ptr(codes), _ptr(scale_inv), N, K, _ptr(q),
+                                                                      _ptr(s), _ptr(status), _stream()))
+    return q, s
+
+
+def fp8block_to_int8_rowwise_batched(mats, outs=None, status=None):
+    """mats: list of (codes, scale_inv) CUDA tensors.  Returns list of (q, s)."""
+    n = len(mats)
+    if outs is None:
+        outs = []
+        for c, _ in mats:
+            outs.append((torch.empty(c.shape, dtype=torch.int8, device=c.device),
+                         torch.empty(c.shape[0], dtype=torch.float32, device=c.device)))
+    for c, si in mats:
+        _need(c, torch.uint8, "codes", 2)
+        _need(si, torch.float32, "scale_inv", 2)
+    arr = ctypes.c_void_p * n
+    ai = ctypes.c_int64 * n
+    w = arr(*[c.data_ptr() for c, _ in mats])
+    si = arr(*[s.data_ptr() for _, s in mats])
+    Ns = ai(*[c.shape[0] for c, _ in mats])
+    Ks = ai(*[c.shape[1] for c, _ in mats])
+    qs = arr(*[q.data_ptr() for q, _ in outs])
+    ss = arr(*[s.data_ptr() for _, s in outs])
+    code = lib().fp8block_to_int8_rowwise_batched(n, ctypes.cast(w, _P), ctypes.cast(si, _P), ctypes.cast(Ns, _P),
+                                                  ctypes.cast(Ks, _P), ctypes.cast(qs, _P), ctypes.cast(ss, _P),
+                                                  _ptr(status), _stream())
+    _check("fp8block_to_int8_rowwise_batched", code)
+    return outs
+
+
+def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None):
+    """Per-segment W8A8 GEMMs: rows [seg[e], seg[e+1]) use expert e's weight."""
+    _need(xq_sorted, torch.int8, "xq_sorted", 2)
+    _need(w, torch.int8, "w", 3)
+    _need(seg_offsets, torch.int64, "seg_offsets", 1)
+    R, K = xq_sorted.shape
+    E, N, K2 = w.shape
+    if K2 != K or seg_offsets.numel() != E + 1:
+        raise ValueError("shape mismatch")
+    if out is None:
+        out = torch.empty((R, N), dtype=torch.bfloat16, device=w.device)
+    code = lib().w8a8_grouped_mm(_ptr(xq_sorted), _ptr(s_x), _ptr(w), _ptr(s_w), _ptr(seg_offsets), E, R, N, K,
+                                 _ptr(out), _ptr(status), _stream())
+    _check("w8a8_grouped_mm", code)
+    return out
+
+
+def moe_quantize_gather(x, row_index):
+    _need(x, torch.bfloat16, "x", 2)
+    _need(row_index, torch.int64, "row_index", 1)
+    T, K = x.shape
+    R = row_index.numel()
+    q = torch.empty((R, K), dtype=torch.int8, device=x.device)
+    s = torch.empty(R, dtype=torch.float32, device=x.device)
+    _check("w8a8_moe_quantize_gather", lib().w8a8_moe_quantize_gather(_ptr(x), T, K, K, _ptr(row_index), R, _ptr(q),
+                                                                      _ptr(s), _stream()))
+    return q, s
+
+
+def silu_mul_quant(h):
+    _need(h, torch.bfloat16, "h", 2)
+    R, twoI = h.shape
+    inter = twoI // 2
+    q = torch.empty((R, inter), dtype=torch.int8, device=h.device)
+    s = torch.empty(R, dtype=torch.float32, device=h.device)
+    _check("w8a8_silu_mul_quant", lib().w8a8_silu_mul_quant(_ptr(h), R, inter, _ptr(q), _ptr(s), _stream()))
+    return q, s
+
+
+def moe_combine(out_rows, row_of, topk_w):
+    _need(out_rows, torch.bfloat16, "out", 2)
+    _need(row_of, torch.int64, "row_of", 2)
+    _need(topk_w, torch.float32, "topk_w", 2)
+    T, k = row_of.shape
+    H = out_rows.shape[1]
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=out_rows.device)
+    _check("w8a8_moe_combine", lib().w8a8_moe_combine(_ptr(out_rows), _ptr(row_of), _ptr(topk_w), T, k, H, _ptr(y),
+                                                      _stream()))
+    return y
+
+
+def moe_forward(x, row_index, seg_offsets, row_of, topk_w, w13, s13, w2, s2):
+    """MoE layer with W8A8 expert GEMMs over token-sorted segments (routing given).
+
+    x bf16 [T, H]; row_index int64 [R] (token of each sorted row); seg_offsets int64 [E+1];
+    row_of int64 [T, k] (sorted row of each (token, slot)); topk_w float32 [T, k];
+    w13 int8 [E, 2I, H] with s13 [E, 2I]; w2 int8 [E, H, I] with s2 [E, H].
+    """
+    xq, sx = moe_quantize_gather(x, row_index)
+    h = grouped_mm(xq, sx, w13, s13, seg_offsets)
+    gq, sg = silu_mul_quant(h)
+    o = grouped_mm(gq, sg, w2, s2, seg_offsets)
+    return moe_combine(o, row_of, topk_w), h, o

@@ -1,0 +1,523 @@
+// INT8 x INT8 -> INT32 GEMM on the sm_103a tensor cores, with the scale/azp/bias epilogue
+// fused ("[SGLang] W4A8, W8A8, W4A4", item 3: int8_scaled_mm; item 4: azp_adj).
+//
+// Engine.  GB300 has no integer tcgen05 MMA kind, and its legacy s8 warp MMA runs at a
+// small fraction of the fp16 tensor rate.  Every int8 value is exact in fp16, every
+// product of two is an integer of magnitude <= 128*127 = 16256 (exact in fp32), and fp32
+// sums of such integers stay exact while every partial sum is below 2^24.  So the kernel
+// runs the products as fp16 x fp16 -> fp32 `tcgen05.mma .kind::f16` into TMEM, in K
+// chunks of at most 1024 (1024 * 16256 < 2^24), and adds each chunk's exact fp32 result
+// into an int32 accumulator held in the epilogue warps' registers.  The result equals the
+// int32 GEMM exactly, for any int8 data.
+//
+// Data path per 128 x 256 output tile, K in steps of 64:
+//   TMA (int8 tiles, 24 KB/step) -> shared int8 ring (4 stages)
+//   4 converter warps: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152), written in the
+//     128-byte-swizzled K-major layout the MMA descriptors read -> fp16 ring (2 stages)
+//   1 thread issues 4 MMAs (M=128, N=256, K=16) per step into TMEM accumulator b
+//   (two 256-column accumulators alternate per 1024-K chunk)
+//   8 epilogue warps drain each chunk (tcgen05.ld), accumulate int32, and after the last
+//   chunk apply y = bf16((s_x*s_w) * f32(acc - zp*azp_adj) + bias) and store.
+// The CTA is persistent (one per SM) and walks a static list of (segment, m-tile, n-tile)
+// work items, so a grouped (MoE) launch and a dense launch are the same kernel.
+//
+// Every wait is bounded in time: a wait that runs out records W8A8_ERR_TIMEOUT, raises a
+// CTA-wide abort flag, and all roles leave their loops; the CTA then waits (bounded) for
+// its own outstanding TMA copies and MMAs before releasing TMEM and returning.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+namespace tc {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int S8 = 4;
+constexpr int S16 = 2;
+constexpr int CHUNK_STEPS = 16;  // 16 * 64 = 1024 K per exact fp32 chunk
+constexpr int A8 = BM * BK;
+constexpr int B8 = BN * BK;
+constexpr int STAGE8 = A8 + B8;
+constexpr int A16 = BM * BK * 2;
+constexpr int B16 = BN * BK * 2;
+constexpr int STAGE16 = A16 + B16;
+constexpr int DATA_BYTES = S8 * STAGE8 + S16 * STAGE16;
+constexpr int MAX_SEG = 1024;
+constexpr int NUM_THREADS = 512;
+constexpr int TMEM_COLS = 512;
+
+struct __align__(8) Bars {
+  uint64_t full8[S8];
+  uint64_t empty8[S8];
+  uint64_t full16[S16];
+  uint64_t empty16[S16];
+  uint64_t accfull[2];
+  uint64_t accempty[2];
+  uint64_t mma_done;
+  uint32_t tmem_base;
+  int32_t abort;
+  int32_t tiles_total;
+  int32_t pad;
+  int32_t tile_prefix[MAX_SEG + 1];
+};
+
+constexpr size_t SMEM_BYTES = 1024 + DATA_BYTES + sizeof(Bars);
+
+// ------------------------------------------------------------------ PTX wrappers
+__device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(b)), "r"(count));
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+  asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(su32(b)) : "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(su32(b)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(su32(b)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ uint64_t gtimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
+
+// Bounded wait.  Returns false (after recording a timeout and raising the abort flag) if
+// the phase did not complete within the limit, or if another role already aborted.
+__device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, Bars* bars, int32_t* status) {
+  if (mbar_try(b, parity)) return true;
+  const uint64_t t0 = gtimer();
+  for (uint32_t i = 1;; ++i) {
+    if (mbar_try(b, parity)) return true;
+    if ((i & 63) == 0) {
+      if (*(volatile int32_t*)&bars->abort) return false;
+      if (gtimer() - t0 > kWaitLimitNs) {
+        *(volatile int32_t*)&bars->abort = 1;
+        report_status(status, W8A8_ERR_TIMEOUT);
+        return false;
+      }
+    }
+  }
+}
+
+__device__ __forceinline__ void tma_load_2d(void* dst, const CUtensorMap* map, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::"r"(
+          su32(dst)),
+      "l"(map), "r"(x), "r"(y), "r"(su32(bar))
+      : "memory");
+}
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)1 << 16;            // leading byte offset: unused for swizzled K-major
+  d |= (uint64_t)(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 B
+  d |= (uint64_t)1 << 46;            // descriptor version (tcgen05)
+  d |= (uint64_t)2 << 61;            // 128-byte swizzle
+  return d;
+}
+
+// kind::f16, A = B = fp16, D = fp32, both K-major, M = 128, N = 256
+constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+
+__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+  asm volatile(
+      "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
+}
+__device__ __forceinline__ void mma_commit(uint64_t* bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(su32(bar))
+               : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+// int8 x 4 -> fp16 x 4, exact: (v ^ 0x80) is v + 128 as an unsigned byte; placing it in the
+// mantissa of 1024.0 (0x6400) gives 1024 + 128 + v, and subtracting 1152 leaves v.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+  uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+  const uint32_t bias = 0x64806480u;  // 1152.0 in both halves
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+// ------------------------------------------------------------------ work list
+struct Tile {
+  int e;
+  int64_t row0, row_end, n0;
+};
+
+__device__ __forceinline__ Tile decode_tile(int t, const Bars* bars, int E, const int64_t* seg, int64_t rows,
+                                            int64_t N, int nt_n) {
+  int lo = 0, hi = E - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (bars->tile_prefix[mid] <= t) lo = mid; else hi = mid - 1;
+  }
+  const int local = t - bars->tile_prefix[lo];
+  const int64_t s0 = seg ? seg[lo] : 0;
+  const int64_t s1 = seg ? seg[lo + 1] : rows;
+  const int64_t ntm = (s1 - s0 + BM - 1) / BM;
+  Tile r;
+  r.e = lo;
+  const int mt = (int)(local % ntm);
+  const int nt = (int)(local / ntm);
+  r.row0 = s0 + (int64_t)mt * BM;
+  r.row_end = s1;
+  r.n0 = (int64_t)nt * BN;
+  (void)nt_n;
+  (void)N;
+  return r;
+}
+
+struct KParams {
+  int64_t rows, N, K;
+  int E;
+  const int64_t* seg;
+  EpiParams ep;
+  __nv_bfloat16* y;
+  int32_t* status;
+};
+
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* ring8 = smem;
+  uint8_t* ring16 = smem + S8 * STAGE8;
+  Bars* bars = reinterpret_cast<Bars*>(smem + DATA_BYTES);
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nt_n = (int)((p.N + BN - 1) / BN);
+  const int nkb = (int)((p.K + BK - 1) / BK);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < S8; ++i) {
+      mbar_init(&bars->full8[i], 1);
+      mbar_init(&bars->empty8[i], 4);
+    }
+    for (int i = 0; i < S16; ++i) {
+      mbar_init(&bars->full16[i], 4);
+      mbar_init(&bars->empty16[i], 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&bars->accfull[i], 1);
+      mbar_init(&bars->accempty[i], 8);
+    }
+    mbar_init(&bars->mma_done, 1);
+    bars->abort = 0;
+    // work-list prefix over segments: tiles of segment e = ceil(rows_e / BM) * ceil(N / BN)
+    int acc = 0;
+    for (int e = 0; e < p.E; ++e) {
+      bars->tile_prefix[e] = acc;
+      const int64_t s0 = p.seg ? p.seg[e] : 0;
+      const int64_t s1 = p.seg ? p.seg[e + 1] : p.rows;
+      const int64_t len = s1 > s0 ? s1 - s0 : 0;
+      acc += (int)((len + BM - 1) / BM) * nt_n;
+    }
+    bars->tile_prefix[p.E] = acc;
+    bars->tiles_total = acc;
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+  }
+  if (warp == 2) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&bars->tmem_base)),
+                 "r"(TMEM_COLS));
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = bars->tmem_base;
+  const int tiles = bars->tiles_total;
+
+  if (warp == 0) {
+    // ---------------------------------------------------------------- TMA producer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
+    if (lane == 0) {
+      uint32_t it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows, p.N, nt_n);
+        const int32_t brow = (int32_t)((int64_t)tl.e * p.N + tl.n0);
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          const uint32_t s = it % S8, ph = (it / S8) & 1;
+          if (!wait_bar(&bars->empty8[s], ph ^ 1, bars, p.status)) { ok = false; break; }
+          uint8_t* st = ring8 + s * STAGE8;
+          mbar_expect_tx(&bars->full8[s], STAGE8);
+          tma_load_2d(st, &tmA, kb * BK, (int32_t)tl.row0, &bars->full8[s]);
+          tma_load_2d(st + A8, &tmB, kb * BK, brow, &bars->full8[s]);
+        }
+      }
+      // drain: every issued copy must have landed before the CTA may exit
+      const uint32_t issued = it;
+      const uint32_t first = issued > (uint32_t)S8 ? issued - S8 : 0;
+      for (uint32_t j = first; j < issued; ++j) {
+        const uint32_t s = j % S8, ph = (j / S8) & 1;
+        uint64_t t0 = gtimer();
+        while (!mbar_try(&bars->full8[s], ph)) {
+          if (gtimer() - t0 > kWaitLimitNs) { report_status(p.status, W8A8_ERR_TIMEOUT); break; }
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ---------------------------------------------------------------- MMA issuer
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
+    if (lane == 0) {
+      uint32_t it = 0, ch = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+        uint32_t b = 0;
+        for (int kb = 0; kb < nkb; ++kb, ++it) {
+          if (kb % CHUNK_STEPS == 0) {
+            b = ch & 1;
+            if (!wait_bar(&bars->accempty[b], ((ch >> 1) & 1) ^ 1, bars, p.status)) { ok = false; break; }
+            tc_fence_after();
+          }
+          const uint32_t s = it % S16, ph = (it / S16) & 1;
+          if (!wait_bar(&bars->full16[s], ph, bars, p.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t abase = su32(ring16 + s * STAGE16);
+          const uint32_t bbase = abase + A16;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            mma_f16(tmem + b * BN, desc_sw128(abase + kk * 32), desc_sw128(bbase + kk * 32),
+                    (kb % CHUNK_STEPS != 0 || kk != 0) ? 1u : 0u);
+          }
+          mma_commit(&bars->empty16[s]);
+          if (kb % CHUNK_STEPS == CHUNK_STEPS - 1 || kb == nkb - 1) {
+            mma_commit(&bars->accfull[b]);
+            ++ch;
+          }
+        }
+      }
+      // all MMAs issued by this thread complete before the CTA releases TMEM
+      mma_commit(&bars->mma_done);
+      uint64_t t0 = gtimer();
+      while (!mbar_try(&bars->mma_done, 0)) {
+        if (gtimer() - t0 > kWaitLimitNs) { report_status(p.status, W8A8_ERR_TIMEOUT); break; }
+      }
+    }
+  } else if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
+  } else if (warp < 8) {
+    // ---------------------------------------------------------------- converters
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n");
+    const int ct = threadIdx.x - 128;  // 0..127
+    uint32_t it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      for (int kb = 0; kb < nkb; ++kb, ++it) {
+        const uint32_t s8 = it % S8, ph8 = (it / S8) & 1;
+        const uint32_t s16 = it % S16, ph16 = (it / S16) & 1;
+        if (!wait_bar(&bars->full8[s8], ph8, bars, p.status)) { ok = false; break; }
+        if (!wait_bar(&bars->empty16[s16], ph16 ^ 1, bars, p.status)) { ok = false; break; }
+        const uint8_t* src = ring8 + s8 * STAGE8;
+        uint8_t* dst = ring16 + s16 * STAGE16;
+        // 1536 units of 16 int8: units 0..511 are A rows (128 x 4), 512..1535 B rows (256 x 4)
+#pragma unroll 4
+        for (int i = 0; i < 12; ++i) {
+          const int u = ct + 128 * i;
+          const int isB = u >= 512;
+          const int uu = isB ? u - 512 : u;
+          const int r = uu >> 2, sgm = uu & 3;
+          const uint4 v = *reinterpret_cast<const uint4*>(src + (isB ? A8 : 0) + r * 64 + sgm * 16);
+          uint32_t o[8];
+          i8x4_to_f16x4(v.x, o[0], o[1]);
+          i8x4_to_f16x4(v.y, o[2], o[3]);
+          i8x4_to_f16x4(v.z, o[4], o[5]);
+          i8x4_to_f16x4(v.w, o[6], o[7]);
+          uint8_t* rowp = dst + (isB ? A16 : 0) + r * 128;
+          const int c0 = (2 * sgm) ^ (r & 7), c1 = (2 * sgm + 1) ^ (r & 7);
+          *reinterpret_cast<uint4*>(rowp + c0 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(rowp + c1 * 16) = make_uint4(o[4], o[5], o[6], o[7]);
+        }
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&bars->empty8[s8]);
+          mbar_arrive(&bars->full16[s16]);
+        }
+      }
+    }
+  } else {
+    // ---------------------------------------------------------------- epilogue (8 warps)
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n");
+    const int q = warp & 3;            // TMEM lane quadrant this warp may access
+    const int h = (warp - 8) >> 2;     // column half
+    uint32_t ch = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+      const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows, p.N, nt_n);
+      const int nch = (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
+      int32_t acc[128];
+      for (int c = 0; c < nch; ++c, ++ch) {
+        const uint32_t b = ch & 1;
+        if (!wait_bar(&bars->accfull[b], (ch >> 1) & 1, bars, p.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * BN + h * 128;
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          uint32_t r[32];
+          tmem_ld32(tbase + j * 32, r);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const int32_t v = __float2int_rn(__uint_as_float(r[i]));
+            acc[j * 32 + i] = (c == 0) ? v : acc[j * 32 + i] + v;
+          }
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&bars->accempty[b]);
+      }
+      if (!ok) break;
+      const int64_t m = tl.row0 + q * 32 + lane;
+      if (m < tl.row_end) {
+        EpiParams ep = p.ep;
+        if (ep.w_mode == W8A8_W_CHANNEL) ep.s_w = p.ep.s_w + (int64_t)tl.e * p.N;
+        const float sx = epi_row_scale(ep, m);
+        const int zpm = epi_row_zp(ep, m);
+        const int64_t nb = tl.n0 + h * 128;
+        __nv_bfloat16* yrow = p.y + m * p.N;
+        const bool vec = ((p.N & 7) == 0);
+#pragma unroll
+        for (int gI = 0; gI < 16; ++gI) {
+          const int64_t n = nb + gI * 8;
+          if (vec && n + 8 <= p.N) {
+            float f[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) f[i] = epi_apply(ep, acc[gI * 8 + i], sx, zpm, n + i);
+            uint4 o;
+            o.x = pack_bf16x2(f[0], f[1]);
+            o.y = pack_bf16x2(f[2], f[3]);
+            o.z = pack_bf16x2(f[4], f[5]);
+            o.w = pack_bf16x2(f[6], f[7]);
+            *reinterpret_cast<uint4*>(yrow + n) = o;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+              if (n + i < p.N) yrow[n + i] = __float2bfloat16_rn(epi_apply(ep, acc[gI * 8 + i], sx, zpm, n + i));
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 2) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TMEM_COLS));
+  }
+}
+
+}  // namespace tc
+
+// ------------------------------------------------------------------ host side
+static PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+static std::once_flag g_encode_once;
+
+static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode;
+}
+
+static bool make_map_i8(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+  auto enc = get_encode();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint32_t box[2] = {(cuuint32_t)tc::BK, box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+int gemm_tc_max_segments() { return tc::MAX_SEG; }
+
+cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
+  if (g.E > tc::MAX_SEG) return cudaErrorNotSupported;
+  if (g.rows == 0 || g.N == 0) return cudaSuccess;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  static int s_attr_dev = -1;
+  static int s_sms = 0;
+  if (s_attr_dev != dev) {
+    e = cudaFuncSetAttribute(tc::gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    s_attr_dev = dev;
+  }
+  CUtensorMap ma, mb;
+  if (!make_map_i8(&ma, g.a, g.rows, g.K, tc::BM)) return cudaErrorInvalidValue;
+  if (!make_map_i8(&mb, g.w, (int64_t)g.E * g.N, g.K, tc::BN)) return cudaErrorInvalidValue;
+  tc::KParams p;
+  p.rows = g.rows;
+  p.N = g.N;
+  p.K = g.K;
+  p.E = g.E;
+  p.seg = g.seg;
+  p.ep.act_mode = g.act_mode;
+  p.ep.w_mode = g.w_mode;
+  p.ep.s_x = g.s_x;
+  p.ep.zp = g.zp;
+  p.ep.azp = g.azp;
+  p.ep.s_w = g.s_w;
+  p.ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
+  p.y = static_cast<__nv_bfloat16*>(g.y);
+  p.status = g.status;
+  // upper bound on work items (exact for a dense launch)
+  const int64_t nt_n = (g.N + tc::BN - 1) / tc::BN;
+  const int64_t tiles_ub = g.seg ? ((g.rows + tc::BM - 1) / tc::BM + g.E) * nt_n : ((g.rows + tc::BM - 1) / tc::BM) * nt_n;
+  const int grid = (int)(tiles_ub < s_sms ? tiles_ub : s_sms);
+  tc::gemm_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8

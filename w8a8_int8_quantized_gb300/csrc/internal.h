@@ -1,0 +1,71 @@
+// Internal launcher declarations shared between the C-ABI layer and the kernels.
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#include "w8a8.h"
+
+namespace w8a8 {
+
+struct EpiParams;
+
+// quant.cu
+cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t ldx,
+                       const int64_t* row_index, int8_t* q, float* scale, int32_t* zp,
+                       int32_t* sum_out, cudaStream_t st);
+cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, int32_t* out,
+                     cudaStream_t st);
+cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, float* sg, cudaStream_t st);
+cudaError_t moe_combine(const void* out, const int64_t* row_of, const float* tw, int64_t T, int topk,
+                        int64_t H, void* y, cudaStream_t st);
+
+// requant.cu
+struct ReqMat {
+  const uint8_t* w;
+  const float* sinv;
+  int8_t* q;
+  float* s;
+  int64_t row0;  // first global row of this matrix in the batch
+  int32_t N;
+  int32_t K;
+  int32_t vec;   // 1: 16-byte vector path
+  int32_t pad;
+};
+constexpr int kReqMaxBatch = 64;
+struct ReqBatch {
+  int32_t count;
+  int32_t pad;
+  int64_t total_rows;
+  ReqMat m[kReqMaxBatch];
+};
+static_assert(sizeof(ReqBatch) <= 4096, "kernel parameter block must stay within 4 KB");
+cudaError_t requant_batch(const ReqBatch& b, int32_t* st, cudaStream_t stream);
+bool requant_vec_ok(const uint8_t* w, const int8_t* q, int64_t K);
+
+// GEMM problem description shared by both GEMM engines.  Rows of A are grouped into
+// segments; segment e multiplies weight rows [e*N, (e+1)*N).  A dense GEMM is one segment.
+struct GemmArgs {
+  const int8_t* a;      // [rows, K]
+  const int8_t* w;      // [E*N, K]
+  int64_t rows;         // rows of A (dense M, or an upper bound for grouped)
+  int64_t N, K;
+  int E;                // number of segments
+  const int64_t* seg;   // device [E+1] or nullptr (dense: one segment [0, rows))
+  int act_mode, w_mode;
+  const float* s_x;
+  const int32_t* zp;
+  const int32_t* azp;
+  const float* s_w;     // [E*N] (channel) or [1] (tensor)
+  const void* bias;     // [N] or nullptr
+  void* y;              // [rows, N] bf16
+  int32_t* status;
+};
+
+// gemm_small.cu: mma.sync s8 weight-streaming kernel (small M)
+cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st);
+// gemm_tc.cu: tcgen05 kernel; returns cudaErrorNotSupported when it cannot run
+cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st);
+int gemm_tc_max_segments();
+
+}  // namespace w8a8

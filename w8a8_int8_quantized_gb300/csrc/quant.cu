@@ -1,0 +1,403 @@
+// Row-wise quantizers: activations (dynamic/static, symmetric/asymmetric), per-channel
+// weights (+ azp_adj column sums), the MoE gather-quantizer, the SiLU*up glue quantizer
+// and the MoE combine.
+//
+// Layout: one CTA per row.  A row is read once with 16-byte loads and kept in registers
+// (up to 8 x 16 B per thread), reduced (absmax or min/max) with warp shuffles plus one
+// shared-memory step, and quantized from registers, so each element crosses HBM once in
+// each direction (2 B read + 1 B written).  Rows too long for the register cache, or not
+// 16-byte aligned, take a two-pass loop that re-reads the row (from L2).
+//
+// The rounding rule is the per-row rule of "MiniMax-M2.7 FP8 转昆仑芯 INT8" (转换关系):
+// s = absmax/127, q = clamp(round(x/s), -127, 127), zero row -> q = 0, s = 1; with
+// IEEE float32 division and ties-to-even rounding.
+#include "common.cuh"
+#include "internal.h"
+
+namespace w8a8 {
+
+constexpr int kMaxVec = 8;  // 16-byte vectors cached per thread
+
+struct RowStats {
+  float a, b;  // sym: a = absmax; asym: a = min, b = max
+};
+
+template <int THREADS>
+__device__ __forceinline__ float block_reduce_max(float v, float* sh) {
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  v = sh[0];
+#pragma unroll
+  for (int i = 1; i < THREADS / 32; ++i) v = fmaxf(v, sh[i]);
+  return v;
+}
+
+template <int THREADS>
+__device__ __forceinline__ float block_reduce_min(float v, float* sh) {
+  for (int o = 16; o > 0; o >>= 1) v = fminf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  v = sh[0];
+#pragma unroll
+  for (int i = 1; i < THREADS / 32; ++i) v = fminf(v, sh[i]);
+  return v;
+}
+
+template <int THREADS>
+__device__ __forceinline__ int block_reduce_sum_i(int v, int* sh) {
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  const int w = threadIdx.x / 32, l = threadIdx.x % 32;
+  __syncthreads();
+  if (l == 0) sh[w] = v;
+  __syncthreads();
+  v = 0;
+#pragma unroll
+  for (int i = 0; i < THREADS / 32; ++i) v += sh[i];
+  return v;
+}
+
+// Scale and zero point of one row from its statistics.  Returns kind: 0 = symmetric
+// rule with scale s, 1 = affine rule with (s, zp).
+struct RowQuant {
+  float s;
+  int zp;
+  int affine;
+};
+
+__device__ __forceinline__ RowQuant row_quant_sym(float absmax) {
+  RowQuant r;
+  r.s = (absmax == 0.f) ? 1.f : __fdiv_rn(absmax, 127.f);
+  r.zp = 0;
+  r.affine = 0;
+  return r;
+}
+
+__device__ __forceinline__ RowQuant row_quant_asym(float lo, float hi) {
+  RowQuant r;
+  if (hi == lo) {
+    r.s = (hi == 0.f) ? 1.f : __fdiv_rn(fabsf(hi), 127.f);
+    r.zp = 0;
+    r.affine = 0;
+  } else {
+    r.s = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
+    r.zp = __float2int_rn(__fsub_rn(-128.f, __fdiv_rn(lo, r.s)));
+    r.affine = 1;
+  }
+  return r;
+}
+
+__device__ __forceinline__ int apply_rq(const RowQuant& r, float x) {
+  return r.affine ? quant_asym(x, r.s, r.zp) : quant_sym(x, r.s);
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f) {
+  f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
+  f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
+  f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
+  f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
+}
+
+__device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
+  uint4 r;
+  asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0,%1,%2,%3}, [%4];\n"
+               : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+  return r;
+}
+
+// ---------------------------------------------------------------------------
+// Vector path: K % 8 == 0, ldx % 8 == 0, 16-byte aligned rows, K <= 8*kMaxVec*THREADS.
+// MODE: w8a8_act_mode.  row_index: optional gather (MoE), sum_out: optional per-row sum
+// of q (weight azp_adj).
+// ---------------------------------------------------------------------------
+template <int MODE, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
+               const int64_t* __restrict__ row_index, int8_t* __restrict__ q,
+               float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out) {
+  __shared__ float sh[THREADS / 32];
+  __shared__ int shi[THREADS / 32];
+  const int64_t row = blockIdx.x;
+  const int64_t src = row_index ? row_index[row] : row;
+  const uint4* xr = reinterpret_cast<const uint4*>(x + src * ldx);
+  const int nvec = (int)(K / 8);
+  uint4 v[kMaxVec];
+  float r0 = (MODE == W8A8_ACT_DYN_TOKEN_ASYM) ? __int_as_float(0x7f800000) : 0.f;  // min or absmax
+  float r1 = __int_as_float(0xff800000);                                              // max
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nvec) {
+      v[i] = ldg_stream(xr + idx);
+      if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+        float f[8];
+        unpack8(v[i], f);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          if (MODE == W8A8_ACT_DYN_TOKEN_SYM) r0 = fmaxf(r0, fabsf(f[j]));
+          else { r0 = fminf(r0, f[j]); r1 = fmaxf(r1, f[j]); }
+        }
+      }
+    }
+  }
+  RowQuant rq;
+  if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
+    rq = row_quant_sym(block_reduce_max<THREADS>(r0, sh));
+  } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+    const float lo = block_reduce_min<THREADS>(r0, sh);
+    const float hi = block_reduce_max<THREADS>(r1, sh);
+    rq = row_quant_asym(lo, hi);
+  } else {
+    rq.s = scale[0];
+    rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
+    rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
+  }
+  int qsum = 0;
+  uint2* qr = reinterpret_cast<uint2*>(q + row * K);
+#pragma unroll
+  for (int i = 0; i < kMaxVec; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nvec) {
+      float f[8];
+      unpack8(v[i], f);
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        c[j] = apply_rq(rq, f[j]);
+        qsum += c[j];
+      }
+      uint2 o;
+      o.x = pack4_i8(c[0], c[1], c[2], c[3]);
+      o.y = pack4_i8(c[4], c[5], c[6], c[7]);
+      qr[idx] = o;
+    }
+  }
+  if (threadIdx.x == 0) {
+    if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
+    if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
+  }
+  if (sum_out) {
+    const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
+    if (threadIdx.x == 0) sum_out[row] = tot;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Generic path: any K, any alignment.  Two passes over the row.
+// ---------------------------------------------------------------------------
+template <int MODE, int THREADS>
+__global__ void __launch_bounds__(THREADS)
+quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
+                   const int64_t* __restrict__ row_index, int8_t* __restrict__ q,
+                   float* __restrict__ scale, int32_t* __restrict__ zp,
+                   int32_t* __restrict__ sum_out) {
+  __shared__ float sh[THREADS / 32];
+  __shared__ int shi[THREADS / 32];
+  const int64_t row = blockIdx.x;
+  const int64_t src = row_index ? row_index[row] : row;
+  const __nv_bfloat16* xr = x + src * ldx;
+  RowQuant rq;
+  if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
+    float a = 0.f;
+    for (int64_t k = threadIdx.x; k < K; k += THREADS) a = fmaxf(a, fabsf(__bfloat162float(xr[k])));
+    rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
+  } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+    float lo = __int_as_float(0x7f800000), hi = __int_as_float(0xff800000);
+    for (int64_t k = threadIdx.x; k < K; k += THREADS) {
+      const float f = __bfloat162float(xr[k]);
+      lo = fminf(lo, f);
+      hi = fmaxf(hi, f);
+    }
+    lo = block_reduce_min<THREADS>(lo, sh);
+    hi = block_reduce_max<THREADS>(hi, sh);
+    rq = row_quant_asym(lo, hi);
+  } else {
+    rq.s = scale[0];
+    rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
+    rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
+  }
+  int qsum = 0;
+  for (int64_t k = threadIdx.x; k < K; k += THREADS) {
+    const int c = apply_rq(rq, __bfloat162float(xr[k]));
+    q[row * K + k] = (int8_t)c;
+    qsum += c;
+  }
+  if (threadIdx.x == 0) {
+    if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
+    if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
+  }
+  if (sum_out) {
+    const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
+    if (threadIdx.x == 0) sum_out[row] = tot;
+  }
+}
+
+template <int MODE>
+static cudaError_t launch_quant_rows(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx,
+                                     const int64_t* row_index, int8_t* q, float* scale, int32_t* zp,
+                                     int32_t* sum_out, cudaStream_t st) {
+  const bool aligned = (K % 8 == 0) && (ldx % 8 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
+                       ((reinterpret_cast<uintptr_t>(q) & 7) == 0);
+  const int64_t nvec = K / 8;
+  if (aligned && nvec <= (int64_t)kMaxVec * 128) {
+    quant_rows_vec<MODE, 128><<<(unsigned)rows, 128, 0, st>>>(x, K, ldx, row_index, q, scale, zp, sum_out);
+  } else if (aligned && nvec <= (int64_t)kMaxVec * 256) {
+    quant_rows_vec<MODE, 256><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, scale, zp, sum_out);
+  } else {
+    quant_rows_generic<MODE, 256><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, scale, zp, sum_out);
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t ldx,
+                       const int64_t* row_index, int8_t* q, float* scale, int32_t* zp,
+                       int32_t* sum_out, cudaStream_t st) {
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  switch (mode) {
+    case W8A8_ACT_DYN_TOKEN_SYM:
+      return launch_quant_rows<W8A8_ACT_DYN_TOKEN_SYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+    case W8A8_ACT_DYN_TOKEN_ASYM:
+      return launch_quant_rows<W8A8_ACT_DYN_TOKEN_ASYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+    case W8A8_ACT_STATIC_TENSOR_SYM:
+      return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_SYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+    default:
+      return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_ASYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// azp_adj[n] = zp * sum_k wq[n, k] for an already-quantized weight.
+// ---------------------------------------------------------------------------
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
+row_sum_i8(const int8_t* __restrict__ w, int64_t K, const int32_t* __restrict__ zp,
+           int32_t* __restrict__ out) {
+  __shared__ int shi[THREADS / 32];
+  const int64_t row = blockIdx.x;
+  const int8_t* wr = w + row * K;
+  int s = 0;
+  if ((K % 16 == 0) && ((reinterpret_cast<uintptr_t>(w) & 15) == 0)) {
+    const uint4* v = reinterpret_cast<const uint4*>(wr);
+    for (int64_t i = threadIdx.x; i < K / 16; i += THREADS) {
+      const uint4 u = v[i];
+      const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+      for (int j = 0; j < 4; ++j) s = __dp4a((int)wd[j], 0x01010101, s);
+    }
+  } else {
+    for (int64_t k = threadIdx.x; k < K; k += THREADS) s += wr[k];
+  }
+  s = block_reduce_sum_i<THREADS>(s, shi);
+  if (threadIdx.x == 0) out[row] = zp ? s * zp[0] : s;
+}
+
+cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, int32_t* out,
+                     cudaStream_t st) {
+  row_sum_i8<256><<<(unsigned)N, 256, 0, st>>>(w, K, zp, out);
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// MoE glue: g = bf16(silu(gate) * up) then per-row symmetric quantization.
+// h row = [gate (I) | up (I)], I % 8 == 0.
+// ---------------------------------------------------------------------------
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS)
+silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t I, int8_t* __restrict__ gq,
+                      float* __restrict__ sg) {
+  __shared__ float sh[THREADS / 32];
+  const int64_t row = blockIdx.x;
+  const uint4* gate = reinterpret_cast<const uint4*>(h + row * 2 * I);
+  const uint4* up = reinterpret_cast<const uint4*>(h + row * 2 * I + I);
+  const int nvec = (int)(I / 8);
+  constexpr int NV = 4;
+  float g[NV][8];
+  float a = 0.f;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nvec) {
+      float fa[8], fb[8];
+      unpack8(gate[idx], fa);
+      unpack8(up[idx], fb);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float e = expf(-fa[j]);
+        const float sl = __fdiv_rn(fa[j], __fadd_rn(1.f, e));
+        const float v = __bfloat162float(__float2bfloat16_rn(__fmul_rn(sl, fb[j])));
+        g[i][j] = v;
+        a = fmaxf(a, fabsf(v));
+      }
+    }
+  }
+  const RowQuant rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
+  uint2* qr = reinterpret_cast<uint2*>(gq + row * I);
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    const int idx = threadIdx.x + i * THREADS;
+    if (idx < nvec) {
+      int c[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[j] = quant_sym(g[i][j], rq.s);
+      uint2 o;
+      o.x = pack4_i8(c[0], c[1], c[2], c[3]);
+      o.y = pack4_i8(c[4], c[5], c[6], c[7]);
+      qr[idx] = o;
+    }
+  }
+  if (threadIdx.x == 0) sg[row] = rq.s;
+}
+
+cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, float* sg, cudaStream_t st) {
+  const int64_t nvec = I / 8;
+  if (nvec <= 4 * 128) {
+    silu_mul_quant_kernel<128><<<(unsigned)R, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(h), I, gq, sg);
+  } else if (nvec <= 4 * 512) {
+    silu_mul_quant_kernel<512><<<(unsigned)R, 512, 0, st>>>(static_cast<const __nv_bfloat16*>(h), I, gq, sg);
+  } else {
+    return cudaErrorInvalidValue;
+  }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// MoE combine: y[t] = bf16( sum_j w[t,j] * out[row_of[t,j]] ), slots in order.
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(128)
+moe_combine_kernel(const __nv_bfloat16* __restrict__ out, const int64_t* __restrict__ row_of,
+                   const float* __restrict__ tw, int topk, int64_t H, __nv_bfloat16* __restrict__ y) {
+  const int64_t t = blockIdx.x;
+  const int nvec = (int)(H / 8);
+  for (int idx = threadIdx.x; idx < nvec; idx += blockDim.x) {
+    float acc[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc[j] = 0.f;
+    for (int s = 0; s < topk; ++s) {
+      const int64_t r = row_of[t * topk + s];
+      const float w = tw[t * topk + s];
+      float f[8];
+      unpack8(reinterpret_cast<const uint4*>(out + r * H)[idx], f);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc[j] = __fadd_rn(acc[j], __fmul_rn(w, f[j]));
+    }
+    uint4 o;
+    o.x = pack_bf16x2(acc[0], acc[1]);
+    o.y = pack_bf16x2(acc[2], acc[3]);
+    o.z = pack_bf16x2(acc[4], acc[5]);
+    o.w = pack_bf16x2(acc[6], acc[7]);
+    reinterpret_cast<uint4*>(y + t * H)[idx] = o;
+  }
+}
+
+cudaError_t moe_combine(const void* out, const int64_t* row_of, const float* tw, int64_t T, int topk,
+                        int64_t H, void* y, cudaStream_t st) {
+  moe_combine_kernel<<<(unsigned)T, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(out), row_of, tw, topk, H,
+                                                  static_cast<__nv_bfloat16*>(y));
+  return cudaGetLastError();
+}
+
+}  // namespace w8a8
