@@ -106,17 +106,24 @@ w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, 
  *   w_mode  W8A8_W_CHANNEL: s_w float [N];  W8A8_W_TENSOR: s_w float [1].
  *   bias    bf16 [N] or NULL.
  *   y       bf16 [M, N] contiguous (output).
+ *   workspace  device scratch of at least w8a8_scaled_mm_workspace_size(M, K) bytes,
+ *              256-byte aligned (the tensor-core engine stages the activations there as
+ *              fp16 integer codes with their row L1 norms).  May be NULL only when the
+ *              warp-MMA engine runs (M <= 16 under automatic selection).
  * Epilogue, float32 with one rounding per step and no fused multiply-add:
  *   c = acc - zp[m]*azp_adj[n] (exact integer, rounded to float32);
  *   y = bf16_rne( (s_x[m]*s_w[n]) * c (+ bias[n]) ).
- * Requirements: K % 16 == 0; xq and wq 16-byte aligned; 1 <= K <= 131072.
+ * The int32 accumulation is exact for all int8 inputs.
+ * Requirements: K % 16 == 0; xq, wq and y 16-byte aligned; 1 <= K <= 131072.
  * dev_status: optional (see conventions); a kernel whose internal wait ran out writes
  * W8A8_ERR_TIMEOUT there and leaves y unspecified.
  */
+size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t K);
 w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
                            int act_mode, const float* s_x, const int32_t* zp,
                            const int32_t* azp_adj, int w_mode, const float* s_w,
-                           const void* bias, void* y, int32_t* dev_status, cudaStream_t stream);
+                           const void* bias, void* y, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, cudaStream_t stream);
 
 /*
  * w8a8_linear -- the whole layer forward: quantize x (any act_mode) then w8a8_scaled_mm
@@ -124,8 +131,8 @@ w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_
  *   x bf16 [M, K] (row stride ldx); wq/s_w/azp_adj/bias as for w8a8_scaled_mm.
  *   input_scale / input_zero_point: float [1] / int32 [1] for the static modes, else NULL.
  *   workspace: device buffer of at least w8a8_linear_workspace_size(M, K, act_mode) bytes,
- *   16-byte aligned; it holds the quantized activations and their scales between the
- *   two kernels.
+ *   256-byte aligned; it holds the quantized activations (in the format the selected GEMM
+ *   engine reads), their scales and zero points between the two kernels.
  */
 size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode);
 w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int act_mode,
@@ -190,11 +197,15 @@ w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,
  *   xq_sorted int8 [R, K];  s_x float [R];  w int8 [E, N, K];  s_w float [E, N];
  *   seg_offsets int64 [E+1] (DEVICE array, non-decreasing, seg[0] = 0, seg[E] = R);
  *   y bf16 [R, N].  R is seg[E]; max_rows is a host-side upper bound on R used to size the
- *   launch (pass R when known).  Requirements as for w8a8_scaled_mm.
+ *   launch and the workspace (pass R when known).  workspace: at least
+ *   w8a8_grouped_mm_workspace_size(max_rows, K) bytes, 256-byte aligned.  E <= 1024.
+ *   Requirements as for w8a8_scaled_mm.
  */
+size_t w8a8_grouped_mm_workspace_size(int64_t max_rows, int64_t K);
 w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int8_t* w,
                             const float* s_w, const int64_t* seg_offsets, int E, int64_t max_rows,
-                            int64_t N, int64_t K, void* y, int32_t* dev_status, cudaStream_t stream);
+                            int64_t N, int64_t K, void* y, void* workspace, size_t workspace_bytes,
+                            int32_t* dev_status, cudaStream_t stream);
 
 /*
  * w8a8_moe_quantize_gather -- per-token symmetric quantization of x rows taken in expert-
@@ -221,6 +232,44 @@ w8a8_status w8a8_silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq,
  */
 w8a8_status w8a8_moe_combine(const void* out, const int64_t* row_of, const float* topk_w,
                              int64_t T, int topk, int64_t H, void* y, cudaStream_t stream);
+
+/*
+ * Packed activations.  The tensor-core GEMM engine reads activations as fp16 integer codes
+ * (every int8 value is exact in fp16) together with each row's L1 norm sum_k |q[r, k]|,
+ * which tells the GEMM whether a single fp32 pass over K is provably exact.  The "packed"
+ * entry points produce and consume that format in one caller buffer of
+ * w8a8_act_packed_size(M, K) bytes (256-byte aligned): fp16 codes [M, K] row-major, then
+ * int32 norms [M] at byte offset roundup(M*K*2, 256).  The codes are the same integers the
+ * int8 entry points produce; only their storage differs.  w8a8_linear runs
+ * w8a8_quantize_act_packed followed by w8a8_scaled_mm_packed (for M > 16).
+ * K % 16 == 0 for every packed entry point.
+ */
+size_t w8a8_act_packed_size(int64_t M, int64_t K);
+
+/* w8a8_quantize_act with the packed output; scale / zp exactly as for w8a8_quantize_act. */
+w8a8_status w8a8_quantize_act_packed(const void* x, int64_t M, int64_t K, int64_t ldx, int mode,
+                                     void* packed, float* scale, int32_t* zp, cudaStream_t stream);
+
+/* w8a8_scaled_mm reading packed activations (no workspace: nothing is staged). */
+w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t M, int64_t N,
+                                  int64_t K, int act_mode, const float* s_x, const int32_t* zp,
+                                  const int32_t* azp_adj, int w_mode, const float* s_w,
+                                  const void* bias, void* y, int32_t* dev_status,
+                                  cudaStream_t stream);
+
+/* w8a8_grouped_mm reading packed activations. */
+w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const int8_t* w,
+                                   const float* s_w, const int64_t* seg_offsets, int E,
+                                   int64_t max_rows, int64_t N, int64_t K, void* y,
+                                   int32_t* dev_status, cudaStream_t stream);
+
+/* w8a8_moe_quantize_gather / w8a8_silu_mul_quant writing packed activations
+ * (packed holds R rows; for the SiLU glue K is I). */
+w8a8_status w8a8_moe_quantize_gather_packed(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                            const int64_t* row_index, int64_t R, void* packed,
+                                            float* s_x, cudaStream_t stream);
+w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void* packed,
+                                       float* s_g, cudaStream_t stream);
 
 #ifdef __cplusplus
 }

@@ -87,6 +87,36 @@ def test_quantize_act_static(M, K):
     np.testing.assert_array_equal(q.cpu().numpy(), oracle.quantize_act_static_asymmetric(xs, np.float32(1e-30), z))
 
 
+@pytest.mark.parametrize("mode", ["dyn_sym", "dyn_asym", "static_sym", "static_asym"])
+@pytest.mark.parametrize("M,K", [(16, 512), (37, 4096), (3, 14336)])
+def test_quantize_act_packed(mode, M, K):
+    """The packed format holds the same integer codes as fp16, plus each row's L1 norm."""
+    x = (wl.asym_activations if "asym" in mode else wl.llama_activations)(M, K, seed=M + 3)
+    if M > 2:
+        x[2] = 0
+    xs = x.float().numpy()
+    sc, z = oracle.static_scale_from_tensor(xs)
+    kw = {}
+    if mode.startswith("static"):
+        kw["scale"] = torch.tensor([sc], dtype=torch.float32, device=DEV)
+        kw["zp"] = torch.tensor([z], dtype=torch.int32, device=DEV)
+    pa = w8.quantize_act_packed(x.to(DEV), mode, **kw)
+    if mode == "dyn_sym":
+        rq, rs = oracle.quantize_act_dynamic_symmetric(xs)
+    elif mode == "dyn_asym":
+        rq, rs, rz = oracle.quantize_act_dynamic_asymmetric(xs)
+        np.testing.assert_array_equal(pa.zp.cpu().numpy(), rz)
+    elif mode == "static_sym":
+        rq, rs = oracle.quantize_act_static_symmetric(xs, sc), None
+    else:
+        rq, rs = oracle.quantize_act_static_asymmetric(xs, sc, z), None
+    codes = pa.codes().float().cpu().numpy()
+    np.testing.assert_array_equal(codes, rq.astype(np.float32))
+    np.testing.assert_array_equal(pa.norms().cpu().numpy(), np.abs(rq.astype(np.int64)).sum(1))
+    if rs is not None:
+        np.testing.assert_array_equal(pa.scale.cpu().numpy(), rs)
+
+
 @pytest.mark.parametrize("N,K", [(512, 512), (300, 4096), (64, 1500)])
 def test_quantize_weight_and_azp(N, K):
     w = wl.weight_bf16(N, K, seed=N)
@@ -175,6 +205,53 @@ def test_gemm_extremes_exact(engine):
     acc = oracle.int8_gemm(xq.numpy(), wq.numpy())
     yb, y32 = oracle.scaled_mm_epilogue(acc, sx.numpy(), sw.numpy(), zp=zp.numpy(), adj=adj.numpy())
     check_bf16(y, yb, y32)
+
+
+@pytest.mark.parametrize("K,fill", [(1024, 127), (1040, None), (1040, "edge"), (4096, "mixed")])
+def test_gemm_single_pass_bound(K, fill):
+    """Tiles whose activation rows have L1 norm < 2^17 run one fp32 pass over K; rows at or
+    above the bound switch the whole tile to 1024-K chunks.  Both must be exact."""
+    M, N = 300, 272
+    rng = np.random.default_rng(K)
+    xq = rng.integers(-3, 4, size=(M, K)).astype(np.int8)
+    if fill == 127:
+        xq[:] = 127                       # norm 130048 < 2^17: single pass, |acc| = 127*127*1024
+    elif fill == "edge":
+        xq[:] = 0
+        xq[0, :1032] = 127                # norm 131064 + 7 = 131071: single pass
+        xq[0, 1032:1039] = 1
+        xq[258, :1032] = 127              # norm 131072, second row tile: chunked
+        xq[258, 1032:1040] = 1
+        xq[260, :] = -128
+    elif fill == "mixed":
+        xq[7, :] = -128                   # one big row forces chunks for its tile only
+    wq = np.full((N, K), 127, dtype=np.int8)
+    wq[1::3] = -127
+    wq[5] = rng.integers(-127, 128, size=K).astype(np.int8)
+    sx = np.full(M, 2.0 ** -10, dtype=np.float32)
+    sw = np.full(N, 2.0 ** -12, dtype=np.float32)
+    w8.set_gemm_engine(1)
+    y = w8.scaled_mm(torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV), torch.from_numpy(sx).to(DEV),
+                     torch.from_numpy(sw).to(DEV))
+    acc = oracle.int8_gemm(xq, wq)
+    yb, y32 = oracle.scaled_mm_epilogue(acc, sx, sw)
+    check_bf16(y, yb, y32)
+
+
+def test_packed_linear_matches_int8_path():
+    d = _gemm_case(200, 512, 2048, seed=21)
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    pa = w8.quantize_act_packed(d["x"].to(DEV))
+    y1 = w8.scaled_mm_packed(pa, wq, sw, bias=d["b"].to(DEV))
+    xq, sx, _ = w8.quantize_act(d["x"].to(DEV))
+    y2 = w8.scaled_mm(xq, wq, sx, sw, bias=d["b"].to(DEV))
+    y3 = w8.linear(d["x"].to(DEV), wq, sw, bias=d["b"].to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+    r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]))
+    check_bf16(y1, r["y_bits"], r["y32"])
 
 
 def test_engines_agree_bitwise():
@@ -348,6 +425,10 @@ def test_grouped_mm_empty_segments():
     sx = torch.rand(R, dtype=torch.float32)
     sw = torch.rand(E, N, dtype=torch.float32) * 1e-3
     y = w8.grouped_mm(xq.to(DEV), sx.to(DEV), wq.to(DEV), sw.to(DEV), seg.to(DEV))
+    w8.set_gemm_engine(2)
+    y2 = w8.grouped_mm(xq.to(DEV), sx.to(DEV), wq.to(DEV), sw.to(DEV), seg.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
     for e in range(E):
         a, b = int(seg[e]), int(seg[e + 1])
         if a == b:

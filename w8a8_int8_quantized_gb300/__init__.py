@@ -12,7 +12,14 @@ from ._binding import (  # noqa: F401
     ACT_STATIC_TENSOR_ASYM,
     ACT_STATIC_TENSOR_SYM,
     LIB_PATH,
+    PackedActivations,
     SIGNATURES,
+    act_packed_size,
+    grouped_mm_packed,
+    moe_quantize_gather_packed,
+    quantize_act_packed,
+    scaled_mm_packed,
+    silu_mul_quant_packed,
     W8A8Error,
     W_CHANNEL,
     W_TENSOR,

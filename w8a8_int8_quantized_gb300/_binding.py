@@ -34,17 +34,25 @@ SIGNATURES = {
     "w8a8_version": (_I, []),
     "w8a8_set_gemm_engine": (_I, [_I]),
     "w8a8_quantize_act": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
-    "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "w8a8_scaled_mm_workspace_size": (_SZ, [_I64, _I64]),
+    "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P, _P]),
     "w8a8_linear_workspace_size": (_SZ, [_I64, _I64, _I]),
     "w8a8_linear": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "w8a8_quantize_weight": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
     "w8a8_azp_adj": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "fp8block_to_int8_rowwise": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
     "fp8block_to_int8_rowwise_batched": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P]),
-    "w8a8_grouped_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
+    "w8a8_grouped_mm_workspace_size": (_SZ, [_I64, _I64]),
+    "w8a8_grouped_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _SZ, _P, _P]),
     "w8a8_moe_quantize_gather": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     "w8a8_silu_mul_quant": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_combine": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _P]),
+    "w8a8_act_packed_size": (_SZ, [_I64, _I64]),
+    "w8a8_quantize_act_packed": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
+    "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
+    "w8a8_moe_quantize_gather_packed": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "w8a8_silu_mul_quant_packed": (_I, [_P, _I64, _I64, _P, _P, _P]),
 }
 
 _lib = None
@@ -125,8 +133,14 @@ def quantize_act(x, mode="dyn_sym", scale=None, zp=None):
     return q, scale, zp
 
 
+def _workspace(nbytes, device, given):
+    if given is not None:
+        return given
+    return torch.empty(max(int(nbytes), 256), dtype=torch.uint8, device=device)
+
+
 def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mode=W_CHANNEL, bias=None,
-              out=None, status=None):
+              out=None, status=None, workspace=None):
     """y[M, N] bf16 = epilogue(xq @ wq.T) (see w8a8_scaled_mm in include/w8a8.h)."""
     _need(xq, torch.int8, "xq", 2)
     _need(wq, torch.int8, "wq", 2)
@@ -136,8 +150,10 @@ def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mod
         raise ValueError("K mismatch")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
+    ws = _workspace(lib().w8a8_scaled_mm_workspace_size(M, K), xq.device, workspace)
     code = lib().w8a8_scaled_mm(_ptr(xq), _ptr(wq), M, N, K, _mode(act_mode), _ptr(s_x), _ptr(zp), _ptr(azp_adj),
-                                int(w_mode), _ptr(s_w), _ptr(bias), _ptr(out), _ptr(status), _stream())
+                                int(w_mode), _ptr(s_w), _ptr(bias), _ptr(out), _ptr(ws), ws.numel(), _ptr(status),
+                                _stream())
     _check("w8a8_scaled_mm", code)
     return out
 
@@ -154,9 +170,7 @@ def linear(x, wq, s_w, act_mode="dyn_sym", input_scale=None, input_zero_point=No
     M, K = x.shape
     N = wq.shape[0]
     m = _mode(act_mode)
-    need = linear_workspace_size(M, K, m)
-    if workspace is None:
-        workspace = torch.empty(max(need, 16), dtype=torch.uint8, device=x.device)
+    workspace = _workspace(linear_workspace_size(M, K, m), x.device, workspace)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     code = lib().w8a8_linear(_ptr(x), M, K, K, m, _ptr(input_scale), _ptr(input_zero_point), _ptr(wq), N,
@@ -225,7 +239,7 @@ def fp8block_to_int8_rowwise_batched(mats, outs=None, status=None):
     return outs
 
 
-def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None):
+def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None, workspace=None):
     """Per-segment W8A8 GEMMs: rows [seg[e], seg[e+1]) use expert e's weight."""
     _need(xq_sorted, torch.int8, "xq_sorted", 2)
     _need(w, torch.int8, "w", 3)
@@ -236,8 +250,9 @@ def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None):
         raise ValueError("shape mismatch")
     if out is None:
         out = torch.empty((R, N), dtype=torch.bfloat16, device=w.device)
+    ws = _workspace(lib().w8a8_grouped_mm_workspace_size(R, K), w.device, workspace)
     code = lib().w8a8_grouped_mm(_ptr(xq_sorted), _ptr(s_x), _ptr(w), _ptr(s_w), _ptr(seg_offsets), E, R, N, K,
-                                 _ptr(out), _ptr(status), _stream())
+                                 _ptr(out), _ptr(ws), ws.numel(), _ptr(status), _stream())
     _check("w8a8_grouped_mm", code)
     return out
 
@@ -276,15 +291,105 @@ def moe_combine(out_rows, row_of, topk_w):
     return y
 
 
+class PackedActivations:
+    """Quantized activations in the tensor-core engine's format (fp16 codes + row L1 norms).
+
+    buf: uint8 CUDA tensor of w8a8_act_packed_size(M, K) bytes; scale / zp as produced by the
+    quantizer.  codes() and norms() are views for inspection.
+    """
+
+    def __init__(self, buf, M, K, scale, zp=None):
+        self.buf, self.M, self.K, self.scale, self.zp = buf, M, K, scale, zp
+
+    def codes(self):
+        return self.buf[: self.M * self.K * 2].view(torch.float16).view(self.M, self.K)
+
+    def norms(self):
+        off = (self.M * self.K * 2 + 255) // 256 * 256
+        return self.buf[off: off + 4 * self.M].view(torch.int32)
+
+
+def act_packed_size(M, K):
+    return int(lib().w8a8_act_packed_size(M, K))
+
+
+def _packed_buf(M, K, device, buf):
+    return buf if buf is not None else torch.empty(max(act_packed_size(M, K), 256), dtype=torch.uint8, device=device)
+
+
+def quantize_act_packed(x, mode="dyn_sym", scale=None, zp=None, buf=None):
+    """Quantize bf16 activations into the packed format.  Returns PackedActivations."""
+    _need(x, torch.bfloat16, "x", 2)
+    m = _mode(mode)
+    M, K = x.shape
+    if m in (ACT_DYN_TOKEN_SYM, ACT_DYN_TOKEN_ASYM):
+        scale = torch.empty(M, dtype=torch.float32, device=x.device)
+        zp = torch.empty(M, dtype=torch.int32, device=x.device) if m == ACT_DYN_TOKEN_ASYM else None
+    pk = _packed_buf(M, K, x.device, buf)
+    _check("w8a8_quantize_act_packed", lib().w8a8_quantize_act_packed(_ptr(x), M, K, K, m, _ptr(pk), _ptr(scale),
+                                                                      _ptr(zp), _stream()))
+    return PackedActivations(pk, M, K, scale, zp)
+
+
+def scaled_mm_packed(pa, wq, s_w, act_mode="dyn_sym", azp_adj=None, w_mode=W_CHANNEL, bias=None, out=None,
+                     status=None):
+    """y = epilogue(A @ wq.T) with A given as PackedActivations (scales taken from it)."""
+    _need(wq, torch.int8, "wq", 2)
+    N = wq.shape[0]
+    if out is None:
+        out = torch.empty((pa.M, N), dtype=torch.bfloat16, device=wq.device)
+    code = lib().w8a8_scaled_mm_packed(_ptr(pa.buf), _ptr(wq), pa.M, N, pa.K, _mode(act_mode), _ptr(pa.scale),
+                                       _ptr(pa.zp), _ptr(azp_adj), int(w_mode), _ptr(s_w), _ptr(bias), _ptr(out),
+                                       _ptr(status), _stream())
+    _check("w8a8_scaled_mm_packed", code)
+    return out
+
+
+def grouped_mm_packed(pa, w, s_w, seg_offsets, out=None, status=None):
+    _need(w, torch.int8, "w", 3)
+    E, N, K = w.shape
+    if out is None:
+        out = torch.empty((pa.M, N), dtype=torch.bfloat16, device=w.device)
+    code = lib().w8a8_grouped_mm_packed(_ptr(pa.buf), _ptr(pa.scale), _ptr(w), _ptr(s_w), _ptr(seg_offsets), E,
+                                        pa.M, N, K, _ptr(out), _ptr(status), _stream())
+    _check("w8a8_grouped_mm_packed", code)
+    return out
+
+
+def moe_quantize_gather_packed(x, row_index, buf=None):
+    _need(x, torch.bfloat16, "x", 2)
+    _need(row_index, torch.int64, "row_index", 1)
+    T, K = x.shape
+    R = row_index.numel()
+    pk = _packed_buf(R, K, x.device, buf)
+    s = torch.empty(R, dtype=torch.float32, device=x.device)
+    _check("w8a8_moe_quantize_gather_packed",
+           lib().w8a8_moe_quantize_gather_packed(_ptr(x), T, K, K, _ptr(row_index), R, _ptr(pk), _ptr(s), _stream()))
+    return PackedActivations(pk, R, K, s)
+
+
+def silu_mul_quant_packed(h, buf=None):
+    _need(h, torch.bfloat16, "h", 2)
+    R, twoI = h.shape
+    inter = twoI // 2
+    pk = _packed_buf(R, inter, h.device, buf)
+    s = torch.empty(R, dtype=torch.float32, device=h.device)
+    _check("w8a8_silu_mul_quant_packed",
+           lib().w8a8_silu_mul_quant_packed(_ptr(h), R, inter, _ptr(pk), _ptr(s), _stream()))
+    return PackedActivations(pk, R, inter, s)
+
+
 def moe_forward(x, row_index, seg_offsets, row_of, topk_w, w13, s13, w2, s2):
     """MoE layer with W8A8 expert GEMMs over token-sorted segments (routing given).
 
     x bf16 [T, H]; row_index int64 [R] (token of each sorted row); seg_offsets int64 [E+1];
     row_of int64 [T, k] (sorted row of each (token, slot)); topk_w float32 [T, k];
     w13 int8 [E, 2I, H] with s13 [E, 2I]; w2 int8 [E, H, I] with s2 [E, H].
+    Five launches: gather-quantize, expert GEMM 1, SiLU*up + quantize, expert GEMM 2, combine.
+    Returns (y [T, H], h [R, 2I], out [R, H]).
     """
-    xq, sx = moe_quantize_gather(x, row_index)
-    h = grouped_mm(xq, sx, w13, s13, seg_offsets)
-    gq, sg = silu_mul_quant(h)
-    o = grouped_mm(gq, sg, w2, s2, seg_offsets)
+    xa = moe_quantize_gather_packed(x, row_index)
+    h = grouped_mm_packed(xa, w13, s13, seg_offsets)
+    ga = silu_mul_quant_packed(h)
+    o = grouped_mm_packed(ga, w2, s2, seg_offsets)
     return moe_combine(o, row_of, topk_w), h, o

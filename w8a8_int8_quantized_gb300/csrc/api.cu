@@ -37,11 +37,27 @@ w8a8_status check_device() {
 bool valid_act_mode(int m) { return m >= W8A8_ACT_DYN_TOKEN_SYM && m <= W8A8_ACT_STATIC_TENSOR_ASYM; }
 bool valid_w_mode(int m) { return m == W8A8_W_CHANNEL || m == W8A8_W_TENSOR; }
 
-w8a8_status run_gemm(const GemmArgs& g, cudaStream_t st, bool small_ok) {
+bool use_small_engine(int64_t rows, bool dense) { return g_engine == 2 || (g_engine == 0 && dense && rows <= 16); }
+
+size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
+
+// Workspace of the tcgen05 engine: fp16 activation codes, then their row L1 norms.
+size_t ready_bytes(int64_t rows, int64_t K) { return a256((size_t)rows * (size_t)K * 2) + a256((size_t)rows * 4); }
+
+w8a8_status run_gemm(GemmArgs g, cudaStream_t st, void* ws, bool small, bool a_is_ready) {
   cudaError_t e;
-  const bool use_small = (g_engine == 2) || (g_engine == 0 && small_ok && g.seg == nullptr && g.rows <= 16);
-  if (use_small) e = gemm_small_m(g, st);
-  else e = gemm_tcgen05(g, st);
+  if (small) {
+    e = gemm_small_m(g, st);
+  } else {
+    uint8_t* w8 = static_cast<uint8_t*>(ws);
+    g.a16 = w8;
+    g.norms = reinterpret_cast<const int32_t*>(w8 + a256((size_t)g.rows * (size_t)g.K * 2));
+    if (!a_is_ready) {
+      e = to_gemm_ready(g.a, g.rows, g.K, w8, const_cast<int32_t*>(g.norms), st);
+      if (e != cudaSuccess) return W8A8_ERR_CUDA;
+    }
+    e = gemm_tcgen05(g, st);
+  }
   return cuda_status(e);
 }
 
@@ -96,18 +112,26 @@ w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, 
   if (!aligned(x, 2)) return W8A8_ERR_MISALIGNED;
   w8a8_status s = check_device();
   if (s != W8A8_OK) return s;
-  return cuda_status(quant_rows(mode, x, M, K, ldx, nullptr, q, scale, zp, nullptr, stream));
+  return cuda_status(quant_rows(mode, x, M, K, ldx, nullptr, q, nullptr, scale, zp, nullptr, nullptr, stream));
+}
+
+size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0) return 0;
+  return ready_bytes(M, K);
 }
 
 w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K, int act_mode,
                            const float* s_x, const int32_t* zp, const int32_t* azp_adj, int w_mode,
-                           const float* s_w, const void* bias, void* y, int32_t* dev_status,
-                           cudaStream_t stream) {
+                           const float* s_w, const void* bias, void* y, void* workspace, size_t workspace_bytes,
+                           int32_t* dev_status, cudaStream_t stream) {
   w8a8_status s = check_scaled_mm_args(xq, wq, M, N, K, act_mode, s_x, zp, azp_adj, w_mode, s_w, bias, y);
   if (s != W8A8_OK || M == 0 || N == 0) return s;
+  const bool small = use_small_engine(M, true);
+  if (!small && (!workspace || workspace_bytes < ready_bytes(M, K))) return W8A8_ERR_WORKSPACE;
+  if (!small && !aligned(workspace, 256)) return W8A8_ERR_MISALIGNED;
   s = check_device();
   if (s != W8A8_OK) return s;
-  GemmArgs g;
+  GemmArgs g{};
   g.a = xq;
   g.w = wq;
   g.rows = M;
@@ -124,16 +148,13 @@ w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
-  return run_gemm(g, stream, true);
+  return run_gemm(g, stream, workspace, small, false);
 }
 
 size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode) {
-  if (M <= 0 || K <= 0) return 0;
-  auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
-  size_t b = a256((size_t)M * (size_t)K);
-  if (act_mode == W8A8_ACT_DYN_TOKEN_SYM || act_mode == W8A8_ACT_DYN_TOKEN_ASYM) b += a256((size_t)M * 4);
-  if (act_mode == W8A8_ACT_DYN_TOKEN_ASYM) b += a256((size_t)M * 4);
-  return b;
+  if (M <= 0 || K <= 0 || !valid_act_mode(act_mode)) return 0;
+  // quantized activations (fp16 codes + norms for tcgen05, or int8 codes) + scales + zero points
+  return ready_bytes(M, K) + 2 * a256((size_t)M * 4);
 }
 
 w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int act_mode, const float* input_scale,
@@ -153,23 +174,25 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
   }
   const size_t need = w8a8_linear_workspace_size(M, K, act_mode);
   if (!workspace || workspace_bytes < need) return W8A8_ERR_WORKSPACE;
-  if (!aligned(workspace, 16) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(x, 2)) return W8A8_ERR_MISALIGNED;
+  if (!aligned(workspace, 256) || !aligned(wq, 16) || !aligned(y, 16) || !aligned(x, 2)) return W8A8_ERR_MISALIGNED;
   w8a8_status s = check_device();
   if (s != W8A8_OK) return s;
-  auto a256 = [](size_t v) { return (v + 255) & ~(size_t)255; };
+  const bool small = use_small_engine(M, true);
   uint8_t* ws = static_cast<uint8_t*>(workspace);
-  int8_t* q = reinterpret_cast<int8_t*>(ws);
-  size_t off = a256((size_t)M * (size_t)K);
+  size_t off = ready_bytes(M, K);
   float* sx = const_cast<float*>(input_scale);
   int32_t* zp = const_cast<int32_t*>(input_zero_point);
   if (!is_static) {
     sx = reinterpret_cast<float*>(ws + off);
-    off += a256((size_t)M * 4);
-    if (act_mode == W8A8_ACT_DYN_TOKEN_ASYM) zp = reinterpret_cast<int32_t*>(ws + off);
+    if (act_mode == W8A8_ACT_DYN_TOKEN_ASYM) zp = reinterpret_cast<int32_t*>(ws + off + a256((size_t)M * 4));
   }
-  cudaError_t e = quant_rows(act_mode, x, M, K, ldx, nullptr, q, sx, zp, nullptr, stream);
+  // the quantizer writes the GEMM engine's own activation format directly
+  int8_t* q = small ? reinterpret_cast<int8_t*>(ws) : nullptr;
+  void* q16 = small ? nullptr : ws;
+  int32_t* norms = small ? nullptr : reinterpret_cast<int32_t*>(ws + a256((size_t)M * (size_t)K * 2));
+  cudaError_t e = quant_rows(act_mode, x, M, K, ldx, nullptr, q, q16, sx, zp, nullptr, norms, stream);
   if (e != cudaSuccess) return W8A8_ERR_CUDA;
-  GemmArgs g;
+  GemmArgs g{};
   g.a = q;
   g.w = wq;
   g.rows = M;
@@ -186,7 +209,7 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
-  return run_gemm(g, stream, true);
+  return run_gemm(g, stream, workspace, small, true);
 }
 
 w8a8_status w8a8_quantize_weight(const void* w, int64_t N, int64_t K, int8_t* wq, float* s_w, int32_t* azp_adj,
@@ -197,7 +220,8 @@ w8a8_status w8a8_quantize_weight(const void* w, int64_t N, int64_t K, int8_t* wq
   if (!aligned(w, 2)) return W8A8_ERR_MISALIGNED;
   w8a8_status s = check_device();
   if (s != W8A8_OK) return s;
-  return cuda_status(quant_rows(W8A8_ACT_DYN_TOKEN_SYM, w, N, K, K, nullptr, wq, s_w, nullptr, azp_adj, stream));
+  return cuda_status(
+      quant_rows(W8A8_ACT_DYN_TOKEN_SYM, w, N, K, K, nullptr, wq, nullptr, s_w, nullptr, azp_adj, nullptr, stream));
 }
 
 w8a8_status w8a8_azp_adj(const int8_t* wq, int64_t N, int64_t K, const int32_t* input_zero_point, int32_t* azp_adj,
@@ -263,9 +287,14 @@ w8a8_status fp8block_to_int8_rowwise(const uint8_t* w, const float* scale_inv, i
   return fp8block_to_int8_rowwise_batched(1, &w, &scale_inv, &N, &K, &q, &s, dev_status, stream);
 }
 
+size_t w8a8_grouped_mm_workspace_size(int64_t R, int64_t K) {
+  if (R <= 0 || K <= 0) return 0;
+  return ready_bytes(R, K);
+}
+
 w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int8_t* w, const float* s_w,
                             const int64_t* seg_offsets, int E, int64_t max_rows, int64_t N, int64_t K, void* y,
-                            int32_t* dev_status, cudaStream_t stream) {
+                            void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
   if (E < 1 || E > gemm_tc_max_segments() || max_rows < 0 || N < 0 || K < 1 || K > kMaxK)
     return W8A8_ERR_INVALID_ARG;
   if (K % 16 != 0) return W8A8_ERR_MISALIGNED;
@@ -273,9 +302,12 @@ w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int
   if (!xq_sorted || !s_x || !w || !s_w || !seg_offsets || !y) return W8A8_ERR_INVALID_ARG;
   if (!aligned(xq_sorted, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(seg_offsets, 8))
     return W8A8_ERR_MISALIGNED;
+  const bool small = use_small_engine(max_rows, false);
+  if (!small && (!workspace || workspace_bytes < ready_bytes(max_rows, K))) return W8A8_ERR_WORKSPACE;
+  if (!small && !aligned(workspace, 256)) return W8A8_ERR_MISALIGNED;
   w8a8_status st = check_device();
   if (st != W8A8_OK) return st;
-  GemmArgs g;
+  GemmArgs g{};
   g.a = xq_sorted;
   g.w = w;
   g.rows = max_rows;
@@ -292,7 +324,7 @@ w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int
   g.bias = nullptr;
   g.y = y;
   g.status = dev_status;
-  return run_gemm(g, stream, false);
+  return run_gemm(g, stream, workspace, small, false);
 }
 
 w8a8_status w8a8_moe_quantize_gather(const void* x, int64_t T, int64_t K, int64_t ldx, const int64_t* row_index,
@@ -304,7 +336,8 @@ w8a8_status w8a8_moe_quantize_gather(const void* x, int64_t T, int64_t K, int64_
   w8a8_status st = check_device();
   if (st != W8A8_OK) return st;
   return cuda_status(
-      quant_rows(W8A8_ACT_DYN_TOKEN_SYM, x, R, K, ldx, row_index, xq_sorted, s_x, nullptr, nullptr, stream));
+      quant_rows(W8A8_ACT_DYN_TOKEN_SYM, x, R, K, ldx, row_index, xq_sorted, nullptr, s_x, nullptr, nullptr, nullptr,
+                 stream));
 }
 
 w8a8_status w8a8_silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, float* s_g, cudaStream_t stream) {
@@ -314,7 +347,7 @@ w8a8_status w8a8_silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq,
   if (I % 8 != 0 || !aligned(h, 16) || !aligned(gq, 8)) return W8A8_ERR_MISALIGNED;
   w8a8_status st = check_device();
   if (st != W8A8_OK) return st;
-  return cuda_status(silu_mul_quant(h, R, I, gq, s_g, stream));
+  return cuda_status(silu_mul_quant(h, R, I, gq, nullptr, nullptr, s_g, stream));
 }
 
 w8a8_status w8a8_moe_combine(const void* out, const int64_t* row_of, const float* topk_w, int64_t T, int topk,
@@ -326,6 +359,110 @@ w8a8_status w8a8_moe_combine(const void* out, const int64_t* row_of, const float
   w8a8_status st = check_device();
   if (st != W8A8_OK) return st;
   return cuda_status(moe_combine(out, row_of, topk_w, T, topk, H, y, stream));
+}
+
+// ---------------------------------------------------------------- packed activations
+size_t w8a8_act_packed_size(int64_t M, int64_t K) {
+  if (M <= 0 || K <= 0) return 0;
+  return ready_bytes(M, K);
+}
+
+w8a8_status w8a8_quantize_act_packed(const void* x, int64_t M, int64_t K, int64_t ldx, int mode, void* packed,
+                                     float* scale, int32_t* zp, cudaStream_t stream) {
+  if (M < 0 || K < 0 || !valid_act_mode(mode)) return W8A8_ERR_INVALID_ARG;
+  if (M == 0 || K == 0) return W8A8_OK;
+  if (ldx < K || !x || !packed || !scale || M > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+  if ((mode == W8A8_ACT_DYN_TOKEN_ASYM || mode == W8A8_ACT_STATIC_TENSOR_ASYM) && !zp) return W8A8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || !aligned(packed, 256) || !aligned(x, 2)) return W8A8_ERR_MISALIGNED;
+  w8a8_status s = check_device();
+  if (s != W8A8_OK) return s;
+  uint8_t* pk = static_cast<uint8_t*>(packed);
+  int32_t* norms = reinterpret_cast<int32_t*>(pk + a256((size_t)M * (size_t)K * 2));
+  return cuda_status(quant_rows(mode, x, M, K, ldx, nullptr, nullptr, pk, scale, zp, nullptr, norms, stream));
+}
+
+w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t M, int64_t N, int64_t K, int act_mode,
+                                  const float* s_x, const int32_t* zp, const int32_t* azp_adj, int w_mode,
+                                  const float* s_w, const void* bias, void* y, int32_t* dev_status,
+                                  cudaStream_t stream) {
+  const int8_t* dummy = static_cast<const int8_t*>(packed);
+  w8a8_status s = check_scaled_mm_args(dummy, wq, M, N, K, act_mode, s_x, zp, azp_adj, w_mode, s_w, bias, y);
+  if (s != W8A8_OK || M == 0 || N == 0) return s;
+  if (!aligned(packed, 256)) return W8A8_ERR_MISALIGNED;
+  s = check_device();
+  if (s != W8A8_OK) return s;
+  GemmArgs g{};
+  g.w = wq;
+  g.rows = M;
+  g.N = N;
+  g.K = K;
+  g.E = 1;
+  g.act_mode = act_mode;
+  g.w_mode = w_mode;
+  g.s_x = s_x;
+  g.zp = zp;
+  g.azp = azp_adj;
+  g.s_w = s_w;
+  g.bias = bias;
+  g.y = y;
+  g.status = dev_status;
+  return run_gemm(g, stream, const_cast<void*>(packed), false, true);
+}
+
+w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const int8_t* w, const float* s_w,
+                                   const int64_t* seg_offsets, int E, int64_t max_rows, int64_t N, int64_t K,
+                                   void* y, int32_t* dev_status, cudaStream_t stream) {
+  if (E < 1 || E > gemm_tc_max_segments() || max_rows < 0 || N < 0 || K < 1 || K > kMaxK)
+    return W8A8_ERR_INVALID_ARG;
+  if (K % 16 != 0) return W8A8_ERR_MISALIGNED;
+  if (max_rows == 0 || N == 0) return W8A8_OK;
+  if (!packed || !s_x || !w || !s_w || !seg_offsets || !y) return W8A8_ERR_INVALID_ARG;
+  if (!aligned(packed, 256) || !aligned(w, 16) || !aligned(y, 16) || !aligned(seg_offsets, 8))
+    return W8A8_ERR_MISALIGNED;
+  w8a8_status st = check_device();
+  if (st != W8A8_OK) return st;
+  GemmArgs g{};
+  g.w = w;
+  g.rows = max_rows;
+  g.N = N;
+  g.K = K;
+  g.E = E;
+  g.seg = seg_offsets;
+  g.act_mode = W8A8_ACT_DYN_TOKEN_SYM;
+  g.w_mode = W8A8_W_CHANNEL;
+  g.s_x = s_x;
+  g.s_w = s_w;
+  g.y = y;
+  g.status = dev_status;
+  return run_gemm(g, stream, const_cast<void*>(packed), false, true);
+}
+
+w8a8_status w8a8_moe_quantize_gather_packed(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                            const int64_t* row_index, int64_t R, void* packed, float* s_x,
+                                            cudaStream_t stream) {
+  if (T < 0 || K < 0 || R < 0 || R > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+  if (R == 0 || K == 0) return W8A8_OK;
+  if (!x || !row_index || !packed || !s_x || ldx < K || T == 0) return W8A8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || !aligned(x, 2) || !aligned(row_index, 8) || !aligned(packed, 256)) return W8A8_ERR_MISALIGNED;
+  w8a8_status st = check_device();
+  if (st != W8A8_OK) return st;
+  uint8_t* pk = static_cast<uint8_t*>(packed);
+  int32_t* norms = reinterpret_cast<int32_t*>(pk + a256((size_t)R * (size_t)K * 2));
+  return cuda_status(quant_rows(W8A8_ACT_DYN_TOKEN_SYM, x, R, K, ldx, row_index, nullptr, pk, s_x, nullptr, nullptr,
+                                norms, stream));
+}
+
+w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void* packed, float* s_g,
+                                       cudaStream_t stream) {
+  if (R < 0 || I < 0 || R > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+  if (R == 0 || I == 0) return W8A8_OK;
+  if (!h || !packed || !s_g || I > 16384) return W8A8_ERR_INVALID_ARG;
+  if (I % 16 != 0 || !aligned(h, 16) || !aligned(packed, 256)) return W8A8_ERR_MISALIGNED;
+  w8a8_status st = check_device();
+  if (st != W8A8_OK) return st;
+  uint8_t* pk = static_cast<uint8_t*>(packed);
+  int32_t* norms = reinterpret_cast<int32_t*>(pk + a256((size_t)R * (size_t)I * 2));
+  return cuda_status(silu_mul_quant(h, R, I, nullptr, pk, norms, s_g, stream));
 }
 
 }  // extern "C"

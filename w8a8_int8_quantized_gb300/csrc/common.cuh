@@ -37,6 +37,12 @@ __device__ __forceinline__ uint32_t pack4_i8(int a, int b, int c, int d) {
          ((uint32_t)(d & 0xFF) << 24);
 }
 
+// two small integers (|v| <= 2048, exact in fp16) packed as fp16x2
+__device__ __forceinline__ uint32_t pack_f16x2(int lo, int hi) {
+  __half2 v = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);

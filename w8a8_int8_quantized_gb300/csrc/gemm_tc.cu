@@ -3,27 +3,37 @@
 //
 // Engine.  GB300 has no integer tcgen05 MMA kind, and its legacy s8 warp MMA runs at a
 // small fraction of the fp16 tensor rate.  Every int8 value is exact in fp16, every
-// product of two is an integer of magnitude <= 128*127 = 16256 (exact in fp32), and fp32
-// sums of such integers stay exact while every partial sum is below 2^24.  So the kernel
-// runs the products as fp16 x fp16 -> fp32 `tcgen05.mma .kind::f16` into TMEM, in K
-// chunks of at most 1024 (1024 * 16256 < 2^24), and adds each chunk's exact fp32 result
-// into an int32 accumulator held in the epilogue warps' registers.  The result equals the
-// int32 GEMM exactly, for any int8 data.
+// product of two is an integer of magnitude <= 128*128, and an fp32 sum of such integers
+// is exact while every partial sum stays within 2^24.  So the products run as
+// fp16 x fp16 -> fp32 `tcgen05.mma .kind::f16` into TMEM, and exactness is guaranteed per
+// output tile in one of two ways:
+//   - single pass: if every activation row r of the tile has sum_k |a[r,k]| < 2^17, then
+//     |any partial sum| <= 2^17 * 128 = 2^24 and the fp32 accumulator over the whole K is
+//     exact (the activation producer writes these row L1 norms next to the fp16 codes);
+//   - chunked: otherwise the K loop is cut into chunks of 1024 (1024 * 128 * 128 = 2^24),
+//     each chunk goes to a fresh TMEM accumulator, and the epilogue adds the chunks'
+//     exact fp32 results into int32 registers.
+// Either way the result equals the int32 GEMM exactly, for any int8 data.
 //
-// Data path per 128 x 256 output tile, K in steps of 64:
-//   TMA (int8 tiles, 24 KB/step) -> shared int8 ring (4 stages)
-//   4 converter warps: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152), written in the
-//     128-byte-swizzled K-major layout the MMA descriptors read -> fp16 ring (2 stages)
-//   1 thread issues 4 MMAs (M=128, N=256, K=16) per step into TMEM accumulator b
-//   (two 256-column accumulators alternate per 1024-K chunk)
-//   8 epilogue warps drain each chunk (tcgen05.ld), accumulate int32, and after the last
-//   chunk apply y = bf16((s_x*s_w) * f32(acc - zp*azp_adj) + bias) and store.
-// The CTA is persistent (one per SM) and walks a static list of (segment, m-tile, n-tile)
-// work items, so a grouped (MoE) launch and a dense launch are the same kernel.
+// Shape.  CTA pairs (cluster of 2, `cta_group::2`) compute 256 x 256 output tiles with
+// M = 256, N = 256, K = 16 MMAs issued by one thread of the even CTA.  Each CTA holds its
+// own 128 activation rows and its 128-row half of the weight tile, so a CTA converts only
+// 128 x 64 weight bytes per K step.
+//   activations: fp16 integer codes [rows, K] -> TMA, 128-byte swizzle, straight into the
+//                MMA operand ring (5 stages x 32 KB)
+//   weights:     int8 [E*N, K] -> TMA -> int8 staging ring (6 stages x 8 KB) -> 4 converter
+//                warps: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152) into the swizzled
+//                operand layout
+//   accumulator: two 256-column fp32 TMEM buffers per CTA, alternating per chunk/tile
+//   epilogue:    8 warps per CTA read TMEM, apply y = bf16((s_x*s_w) * f32(acc - zp*azp_adj)
+//                + bias), store.
+// The pair is persistent and walks a static list of (segment, row tile, column tile) work
+// items, so grouped (MoE) and dense launches are the same kernel.
 //
 // Every wait is bounded in time: a wait that runs out records W8A8_ERR_TIMEOUT, raises a
-// CTA-wide abort flag, and all roles leave their loops; the CTA then waits (bounded) for
-// its own outstanding TMA copies and MMAs before releasing TMEM and returning.
+// CTA-wide abort flag, and all roles leave their loops; each CTA then waits (bounded) for
+// its own outstanding TMA copies and MMAs, both CTAs meet at a cluster barrier, and TMEM is
+// released.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -35,30 +45,34 @@
 namespace w8a8 {
 namespace tc {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
+constexpr int BM = 256;        // activation rows per pair tile
+constexpr int BM_CTA = 128;    // activation rows per CTA
+constexpr int BN = 256;        // weight rows (output columns) per pair tile
+constexpr int BN_CTA = 128;    // weight rows converted and held per CTA
 constexpr int BK = 64;
-constexpr int S8 = 4;
-constexpr int S16 = 2;
-constexpr int CHUNK_STEPS = 16;  // 16 * 64 = 1024 K per exact fp32 chunk
-constexpr int A8 = BM * BK;
-constexpr int B8 = BN * BK;
-constexpr int STAGE8 = A8 + B8;
-constexpr int A16 = BM * BK * 2;
-constexpr int B16 = BN * BK * 2;
+constexpr int S16 = 5;
+constexpr int S8 = 6;
+constexpr int CHUNK_STEPS = 16;   // 16 * 64 = 1024 K per exact fp32 chunk
+constexpr int32_t kNormSingle = 131072;  // row L1 norm below 2^17 -> single pass is exact
+constexpr int A16 = BM_CTA * BK * 2;     // 16 KB
+constexpr int B16 = BN_CTA * BK * 2;     // 16 KB
 constexpr int STAGE16 = A16 + B16;
-constexpr int DATA_BYTES = S8 * STAGE8 + S16 * STAGE16;
+constexpr int B8 = BN_CTA * BK;          // 8 KB
+constexpr int DATA_BYTES = S16 * STAGE16 + S8 * B8;
 constexpr int MAX_SEG = 1024;
 constexpr int NUM_THREADS = 512;
 constexpr int TMEM_COLS = 512;
+constexpr int EPI_WARPS = 8;
+constexpr int CONV_WARPS = 4;
 
 struct __align__(8) Bars {
-  uint64_t full8[S8];
-  uint64_t empty8[S8];
-  uint64_t full16[S16];
-  uint64_t empty16[S16];
-  uint64_t accfull[2];
-  uint64_t accempty[2];
+  uint64_t full_a[S16];    // activation tile landed (TMA tx)
+  uint64_t full16[S16];    // both CTAs' operands ready (leader only; 2 x CONV_WARPS arrivals)
+  uint64_t empty16[S16];   // MMAs reading the stage finished (multicast commit)
+  uint64_t full8[S8];      // int8 weight tile landed (TMA tx)
+  uint64_t empty8[S8];     // converters done reading the int8 tile
+  uint64_t accfull[2];     // accumulator buffer ready (multicast commit)
+  uint64_t accempty[2];    // both CTAs drained the buffer (leader only; 2 x EPI_WARPS arrivals)
   uint64_t mma_done;
   uint32_t tmem_base;
   int32_t abort;
@@ -68,15 +82,45 @@ struct __align__(8) Bars {
 };
 
 constexpr size_t SMEM_BYTES = 1024 + DATA_BYTES + sizeof(Bars);
+static_assert(SMEM_BYTES <= 232448, "shared memory budget");
 
 // ------------------------------------------------------------------ PTX wrappers
 __device__ __forceinline__ uint32_t su32(const void* p) { return (uint32_t)__cvta_generic_to_shared(p); }
 
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_id() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ uint32_t cluster_count() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+  return r;
+}
+// shared::cluster address of the same shared variable in CTA `rank` of this cluster
+__device__ __forceinline__ uint32_t map_to(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
 __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(su32(b)), "r"(count));
 }
-__device__ __forceinline__ void mbar_arrive(uint64_t* b) {
+__device__ __forceinline__ void mbar_arrive_local(uint64_t* b) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(su32(b)) : "memory");
+}
+// arrive on a barrier given by its shared::cluster address (own CTA or the peer)
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(caddr) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(su32(b)), "r"(bytes)
@@ -85,7 +129,8 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(su32(b)), "r"(parity)
       : "memory");
@@ -100,7 +145,7 @@ __device__ __forceinline__ uint64_t gtimer() {
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s
 
 // Bounded wait.  Returns false (after recording a timeout and raising the abort flag) if
-// the phase did not complete within the limit, or if another role already aborted.
+// the phase did not complete within the limit, or if another role of this CTA aborted.
 __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, Bars* bars, int32_t* status) {
   if (mbar_try(b, parity)) return true;
   const uint64_t t0 = gtimer();
@@ -113,6 +158,17 @@ __device__ __forceinline__ bool wait_bar(uint64_t* b, uint32_t parity, Bars* bar
         report_status(status, W8A8_ERR_TIMEOUT);
         return false;
       }
+    }
+  }
+}
+
+// bounded wait used on the exit path (no abort short-cut)
+__device__ __forceinline__ void drain_wait(uint64_t* b, uint32_t parity, int32_t* status) {
+  const uint64_t t0 = gtimer();
+  while (!mbar_try(b, parity)) {
+    if (gtimer() - t0 > kWaitLimitNs) {
+      report_status(status, W8A8_ERR_TIMEOUT);
+      return;
     }
   }
 }
@@ -136,18 +192,23 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr) {
   return d;
 }
 
-// kind::f16, A = B = fp16, D = fp32, both K-major, M = 128, N = 256
+// kind::f16, A = B = fp16, D = fp32, both K-major, M = 256 (pair), N = 256
 constexpr uint32_t kIdesc = (1u << 4) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 
-__device__ __forceinline__ void mma_f16(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
+__device__ __forceinline__ void mma_f16_pair(uint32_t tmem_d, uint64_t da, uint64_t db, uint32_t accumulate) {
   asm volatile(
       "{\n.reg .pred p;\nsetp.ne.b32 p, %4, 0;\n"
-      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(tmem_d),
       "l"(da), "l"(db), "r"(kIdesc), "r"(accumulate));
 }
-__device__ __forceinline__ void mma_commit(uint64_t* bar) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(su32(bar))
-               : "memory");
+// arrive once on the barrier at this offset in both CTAs when all prior MMAs complete
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar) {
+  const uint16_t mask = 0x3;
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;\n" ::"r"(
+          su32(bar)),
+      "h"(mask)
+      : "memory");
 }
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
 __device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
@@ -169,8 +230,8 @@ __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.
 // mantissa of 1024.0 (0x6400) gives 1024 + 128 + v, and subtracting 1152 leaves v.
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
   const uint32_t x = w ^ 0x80808080u;
-  uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
-  uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
   const uint32_t bias = 0x64806480u;  // 1152.0 in both halves
   asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(a), "r"(bias));
   asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(b), "r"(bias));
@@ -182,8 +243,7 @@ struct Tile {
   int64_t row0, row_end, n0;
 };
 
-__device__ __forceinline__ Tile decode_tile(int t, const Bars* bars, int E, const int64_t* seg, int64_t rows,
-                                            int64_t N, int nt_n) {
+__device__ __forceinline__ Tile decode_tile(int t, const Bars* bars, int E, const int64_t* seg, int64_t rows) {
   int lo = 0, hi = E - 1;
   while (lo < hi) {
     const int mid = (lo + hi + 1) >> 1;
@@ -195,13 +255,9 @@ __device__ __forceinline__ Tile decode_tile(int t, const Bars* bars, int E, cons
   const int64_t ntm = (s1 - s0 + BM - 1) / BM;
   Tile r;
   r.e = lo;
-  const int mt = (int)(local % ntm);
-  const int nt = (int)(local / ntm);
-  r.row0 = s0 + (int64_t)mt * BM;
+  r.row0 = s0 + (int64_t)(local % ntm) * BM;
   r.row_end = s1;
-  r.n0 = (int64_t)nt * BN;
-  (void)nt_n;
-  (void)N;
+  r.n0 = (int64_t)(local / ntm) * BN;
   return r;
 }
 
@@ -209,39 +265,56 @@ struct KParams {
   int64_t rows, N, K;
   int E;
   const int64_t* seg;
+  const int32_t* norms;  // [rows] sum_k |a[r, k]|
   EpiParams ep;
   __nv_bfloat16* y;
   int32_t* status;
 };
 
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+// Whether the pair tile starting at row0 can run single pass (warp-wide, all lanes agree).
+__device__ __forceinline__ bool tile_single_pass(const KParams& p, const Tile& tl, int lane) {
+  int32_t mx = 0;
+#pragma unroll
+  for (int j = 0; j < BM / 32; ++j) {
+    const int64_t r = tl.row0 + lane + 32 * j;
+    if (r < tl.row_end) mx = max(mx, p.norms[r]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  return mx < kNormSingle;
+}
+
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring8 = smem;
-  uint8_t* ring16 = smem + S8 * STAGE8;
+  uint8_t* ring16 = smem;
+  uint8_t* ring8 = smem + S16 * STAGE16;
   Bars* bars = reinterpret_cast<Bars*>(smem + DATA_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = (int)cluster_id();
+  const int npairs = (int)cluster_count();
   const int nt_n = (int)((p.N + BN - 1) / BN);
   const int nkb = (int)((p.K + BK - 1) / BK);
 
   if (threadIdx.x == 0) {
+    for (int i = 0; i < S16; ++i) {
+      mbar_init(&bars->full_a[i], 1);
+      mbar_init(&bars->full16[i], 2 * CONV_WARPS);
+      mbar_init(&bars->empty16[i], 1);
+    }
     for (int i = 0; i < S8; ++i) {
       mbar_init(&bars->full8[i], 1);
-      mbar_init(&bars->empty8[i], 4);
-    }
-    for (int i = 0; i < S16; ++i) {
-      mbar_init(&bars->full16[i], 4);
-      mbar_init(&bars->empty16[i], 1);
+      mbar_init(&bars->empty8[i], CONV_WARPS);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->accfull[i], 1);
-      mbar_init(&bars->accempty[i], 8);
+      mbar_init(&bars->accempty[i], 2 * EPI_WARPS);
     }
     mbar_init(&bars->mma_done, 1);
     bars->abort = 0;
-    // work-list prefix over segments: tiles of segment e = ceil(rows_e / BM) * ceil(N / BN)
     int acc = 0;
     for (int e = 0; e < p.E; ++e) {
       bars->tile_prefix[e] = acc;
@@ -255,139 +328,158 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
   }
   if (warp == 2) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&bars->tmem_base)),
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(su32(&bars->tmem_base)),
                  "r"(TMEM_COLS));
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n");
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // both CTAs' barriers exist before any remote arrive or multicast commit
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const int tiles = bars->tiles_total;
 
   if (warp == 0) {
-    // ---------------------------------------------------------------- TMA producer
+    // ---------------------------------------------------------------- TMA producer (each CTA)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
     if (lane == 0) {
-      uint32_t it = 0;
+      uint32_t nb = 0, na = 0;  // weight / activation copies issued
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows, p.N, nt_n);
-        const int32_t brow = (int32_t)((int64_t)tl.e * p.N + tl.n0);
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          const uint32_t s = it % S8, ph = (it / S8) & 1;
-          if (!wait_bar(&bars->empty8[s], ph ^ 1, bars, p.status)) { ok = false; break; }
-          uint8_t* st = ring8 + s * STAGE8;
-          mbar_expect_tx(&bars->full8[s], STAGE8);
-          tma_load_2d(st, &tmA, kb * BK, (int32_t)tl.row0, &bars->full8[s]);
-          tma_load_2d(st + A8, &tmB, kb * BK, brow, &bars->full8[s]);
+      for (int t = pair; t < tiles && ok; t += npairs) {
+        const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
+        const int32_t arow = (int32_t)(tl.row0 + BM_CTA * rank);
+        const int32_t brow = (int32_t)((int64_t)tl.e * p.N + tl.n0 + BN_CTA * rank);
+        for (int kb = 0; kb < nkb; ++kb) {
+          const uint32_t s8 = nb % S8, ph8 = (nb / S8) & 1;
+          if (!wait_bar(&bars->empty8[s8], ph8 ^ 1, bars, p.status)) { ok = false; break; }
+          mbar_expect_tx(&bars->full8[s8], B8);
+          tma_load_2d(ring8 + s8 * B8, &tmB, kb * BK, brow, &bars->full8[s8]);
+          ++nb;
+          const uint32_t s16 = na % S16, ph16 = (na / S16) & 1;
+          if (!wait_bar(&bars->empty16[s16], ph16 ^ 1, bars, p.status)) { ok = false; break; }
+          mbar_expect_tx(&bars->full_a[s16], A16);
+          tma_load_2d(ring16 + s16 * STAGE16, &tmA, kb * BK, arow, &bars->full_a[s16]);
+          ++na;
         }
       }
-      // drain: every issued copy must have landed before the CTA may exit
-      const uint32_t issued = it;
-      const uint32_t first = issued > (uint32_t)S8 ? issued - S8 : 0;
-      for (uint32_t j = first; j < issued; ++j) {
-        const uint32_t s = j % S8, ph = (j / S8) & 1;
-        uint64_t t0 = gtimer();
-        while (!mbar_try(&bars->full8[s], ph)) {
-          if (gtimer() - t0 > kWaitLimitNs) { report_status(p.status, W8A8_ERR_TIMEOUT); break; }
-        }
-      }
+      // every issued copy must land before the CTA may exit
+      for (uint32_t j = (nb > (uint32_t)S8 ? nb - S8 : 0); j < nb; ++j)
+        drain_wait(&bars->full8[j % S8], (j / S8) & 1, p.status);
+      for (uint32_t j = (na > (uint32_t)S16 ? na - S16 : 0); j < na; ++j)
+        drain_wait(&bars->full_a[j % S16], (j / S16) & 1, p.status);
     }
   } else if (warp == 1) {
-    // ---------------------------------------------------------------- MMA issuer
+    // ---------------------------------------------------------------- MMA issuer (even CTA)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
-    if (lane == 0) {
+    if (rank == 0) {
       uint32_t it = 0, ch = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-        uint32_t b = 0;
-        for (int kb = 0; kb < nkb; ++kb, ++it) {
-          if (kb % CHUNK_STEPS == 0) {
-            b = ch & 1;
-            if (!wait_bar(&bars->accempty[b], ((ch >> 1) & 1) ^ 1, bars, p.status)) { ok = false; break; }
+      for (int t = pair; t < tiles && ok; t += npairs) {
+        const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
+        const int spc = tile_single_pass(p, tl, lane) ? nkb : CHUNK_STEPS;
+        if (lane == 0) {
+          uint32_t b = 0;
+          for (int kb = 0; kb < nkb; ++kb, ++it) {
+            if (kb % spc == 0) {
+              b = ch & 1;
+              if (!wait_bar(&bars->accempty[b], ((ch >> 1) & 1) ^ 1, bars, p.status)) { ok = false; break; }
+              tc_fence_after();
+            }
+            const uint32_t s = it % S16, ph = (it / S16) & 1;
+            if (!wait_bar(&bars->full16[s], ph, bars, p.status)) { ok = false; break; }
             tc_fence_after();
-          }
-          const uint32_t s = it % S16, ph = (it / S16) & 1;
-          if (!wait_bar(&bars->full16[s], ph, bars, p.status)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t abase = su32(ring16 + s * STAGE16);
-          const uint32_t bbase = abase + A16;
+            const uint32_t abase = su32(ring16 + s * STAGE16);
+            const uint32_t bbase = abase + A16;
 #pragma unroll
-          for (int kk = 0; kk < BK / 16; ++kk) {
-            mma_f16(tmem + b * BN, desc_sw128(abase + kk * 32), desc_sw128(bbase + kk * 32),
-                    (kb % CHUNK_STEPS != 0 || kk != 0) ? 1u : 0u);
-          }
-          mma_commit(&bars->empty16[s]);
-          if (kb % CHUNK_STEPS == CHUNK_STEPS - 1 || kb == nkb - 1) {
-            mma_commit(&bars->accfull[b]);
-            ++ch;
+            for (int kk = 0; kk < BK / 16; ++kk)
+              mma_f16_pair(tmem + b * BN, desc_sw128(abase + kk * 32), desc_sw128(bbase + kk * 32),
+                           (kb % spc != 0 || kk != 0) ? 1u : 0u);
+            mma_commit_pair(&bars->empty16[s]);
+            if (kb % spc == spc - 1 || kb == nkb - 1) {
+              mma_commit_pair(&bars->accfull[b]);
+              ++ch;
+            }
           }
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
       }
-      // all MMAs issued by this thread complete before the CTA releases TMEM
-      mma_commit(&bars->mma_done);
-      uint64_t t0 = gtimer();
-      while (!mbar_try(&bars->mma_done, 0)) {
-        if (gtimer() - t0 > kWaitLimitNs) { report_status(p.status, W8A8_ERR_TIMEOUT); break; }
+      if (lane == 0) {
+        // all MMAs issued by this thread complete before TMEM is released
+        asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(
+                         su32(&bars->mma_done))
+                     : "memory");
+        drain_wait(&bars->mma_done, 0, p.status);
       }
     }
   } else if (warp < 4) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
   } else if (warp < 8) {
-    // ---------------------------------------------------------------- converters
+    // ---------------------------------------------------------------- converters (each CTA)
     asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n");
     const int ct = threadIdx.x - 128;  // 0..127
     uint32_t it = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
+    for (int t = pair; t < tiles && ok; t += npairs) {
       for (int kb = 0; kb < nkb; ++kb, ++it) {
         const uint32_t s8 = it % S8, ph8 = (it / S8) & 1;
         const uint32_t s16 = it % S16, ph16 = (it / S16) & 1;
-        if (!wait_bar(&bars->full8[s8], ph8, bars, p.status)) { ok = false; break; }
-        if (!wait_bar(&bars->empty16[s16], ph16 ^ 1, bars, p.status)) { ok = false; break; }
-        const uint8_t* src = ring8 + s8 * STAGE8;
-        uint8_t* dst = ring16 + s16 * STAGE16;
-        // 1536 units of 16 int8: units 0..511 are A rows (128 x 4), 512..1535 B rows (256 x 4)
-#pragma unroll 4
-        for (int i = 0; i < 12; ++i) {
+        // every lane waits; the outcome is made warp-uniform so the warp stays converged
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->full8[s8], ph8, bars, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->empty16[s16], ph16 ^ 1, bars, p.status))) { ok = false; break; }
+        const uint8_t* src = ring8 + s8 * B8;
+        uint8_t* dst = ring16 + s16 * STAGE16 + A16;
+        // 512 units of 16 int8 (128 rows x 4): 4 per thread
+        uint4 v[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
           const int u = ct + 128 * i;
-          const int isB = u >= 512;
-          const int uu = isB ? u - 512 : u;
-          const int r = uu >> 2, sgm = uu & 3;
-          const uint4 v = *reinterpret_cast<const uint4*>(src + (isB ? A8 : 0) + r * 64 + sgm * 16);
+          v[i] = *reinterpret_cast<const uint4*>(src + (u >> 2) * 64 + (u & 3) * 16);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int u = ct + 128 * i;
+          const int r = u >> 2, sgm = u & 3;
           uint32_t o[8];
-          i8x4_to_f16x4(v.x, o[0], o[1]);
-          i8x4_to_f16x4(v.y, o[2], o[3]);
-          i8x4_to_f16x4(v.z, o[4], o[5]);
-          i8x4_to_f16x4(v.w, o[6], o[7]);
-          uint8_t* rowp = dst + (isB ? A16 : 0) + r * 128;
-          const int c0 = (2 * sgm) ^ (r & 7), c1 = (2 * sgm + 1) ^ (r & 7);
-          *reinterpret_cast<uint4*>(rowp + c0 * 16) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(rowp + c1 * 16) = make_uint4(o[4], o[5], o[6], o[7]);
+          i8x4_to_f16x4(v[i].x, o[0], o[1]);
+          i8x4_to_f16x4(v[i].y, o[2], o[3]);
+          i8x4_to_f16x4(v[i].z, o[4], o[5]);
+          i8x4_to_f16x4(v[i].w, o[6], o[7]);
+          uint8_t* rowp = dst + r * 128;
+          *reinterpret_cast<uint4*>(rowp + (((2 * sgm) ^ (r & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+          *reinterpret_cast<uint4*>(rowp + (((2 * sgm + 1) ^ (r & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
         }
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive(&bars->empty8[s8]);
-          mbar_arrive(&bars->full16[s16]);
+          mbar_arrive_local(&bars->empty8[s8]);
+          // the activation tile of this stage must have landed before the pair's MMA reads it
+          if (!wait_bar(&bars->full_a[s16], ph16, bars, p.status)) ok = false;
+          else mbar_arrive_cluster(map_to(su32(&bars->full16[s16]), 0));
         }
+        ok = __shfl_sync(0xffffffffu, ok, 0);
+        if (!ok) break;
       }
     }
   } else {
-    // ---------------------------------------------------------------- epilogue (8 warps)
+    // ---------------------------------------------------------------- epilogue (8 warps, each CTA)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n");
     const int q = warp & 3;            // TMEM lane quadrant this warp may access
     const int h = (warp - 8) >> 2;     // column half
+    const uint32_t accempty0 = map_to(su32(&bars->accempty[0]), 0);
+    const uint32_t accempty1 = map_to(su32(&bars->accempty[1]), 0);
     uint32_t ch = 0;
     bool ok = true;
-    for (int t = blockIdx.x; t < tiles && ok; t += gridDim.x) {
-      const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows, p.N, nt_n);
-      const int nch = (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
+    for (int t = pair; t < tiles && ok; t += npairs) {
+      const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
+      const bool single = tile_single_pass(p, tl, lane);
+      const int nch = single ? 1 : (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
       int32_t acc[128];
       for (int c = 0; c < nch; ++c, ++ch) {
         const uint32_t b = ch & 1;
-        if (!wait_bar(&bars->accfull[b], (ch >> 1) & 1, bars, p.status)) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->accfull[b], (ch >> 1) & 1, bars, p.status))) {
+          ok = false;
+          break;
+        }
         tc_fence_after();
         const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * BN + h * 128;
 #pragma unroll
@@ -403,10 +495,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         tc_fence_before();
         __syncwarp();
-        if (lane == 0) mbar_arrive(&bars->accempty[b]);
+        if (lane == 0) mbar_arrive_cluster(b ? accempty1 : accempty0);
       }
       if (!ok) break;
-      const int64_t m = tl.row0 + q * 32 + lane;
+      const int64_t m = tl.row0 + BM_CTA * rank + q * 32 + lane;
       if (m < tl.row_end) {
         EpiParams ep = p.ep;
         if (ep.w_mode == W8A8_W_CHANNEL) ep.s_w = p.ep.s_w + (int64_t)tl.e * p.N;
@@ -440,9 +532,41 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no remote arrive or MMA can target a CTA that has left
   if (warp == 2) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TMEM_COLS));
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(TMEM_COLS));
+  }
+}
+
+// int8 -> fp16 integer codes and row L1 norms (the GEMM-ready activation format)
+__global__ void __launch_bounds__(256)
+to_gemm_ready_kernel(const int8_t* __restrict__ a, int64_t K, __half* __restrict__ a16, int32_t* __restrict__ norms) {
+  __shared__ int sh[8];
+  const int64_t row = blockIdx.x;
+  int s = 0;
+  const int8_t* ar = a + row * K;
+  __half* hr = a16 + row * K;
+  for (int64_t i = threadIdx.x; i < K / 16; i += 256) {
+    const uint4 v = reinterpret_cast<const uint4*>(ar)[i];
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    uint32_t o[8];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      i8x4_to_f16x4(w[j], o[2 * j], o[2 * j + 1]);
+#pragma unroll
+      for (int b = 0; b < 4; ++b) s += abs((int)(int8_t)(w[j] >> (8 * b)));
+    }
+    reinterpret_cast<uint4*>(hr)[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
+    reinterpret_cast<uint4*>(hr)[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
+  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    int t = 0;
+    for (int i = 0; i < 8; ++i) t += sh[i];
+    norms[row] = t;
   }
 }
 
@@ -464,24 +588,31 @@ static PFN_cuTensorMapEncodeTiled_v12000 get_encode() {
   return g_encode;
 }
 
-static bool make_map_i8(CUtensorMap* m, const void* base, int64_t rows, int64_t K, uint32_t box_rows) {
+static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const void* base, int64_t rows, int64_t K,
+                     uint32_t box_rows, CUtensorMapSwizzle sw) {
   auto enc = get_encode();
   if (!enc) return false;
   cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)K};
+  cuuint64_t strides[1] = {(cuuint64_t)K * (cuuint64_t)esize};
   cuuint32_t box[2] = {(cuuint32_t)tc::BK, box_rows};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, sw,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
 int gemm_tc_max_segments() { return tc::MAX_SEG; }
 
+cudaError_t to_gemm_ready(const int8_t* a, int64_t rows, int64_t K, void* a16, int32_t* norms, cudaStream_t st) {
+  if (rows == 0) return cudaSuccess;
+  tc::to_gemm_ready_kernel<<<(unsigned)rows, 256, 0, st>>>(a, K, static_cast<__half*>(a16), norms);
+  return cudaGetLastError();
+}
+
 cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   if (g.E > tc::MAX_SEG) return cudaErrorNotSupported;
   if (g.rows == 0 || g.N == 0) return cudaSuccess;
+  if (!g.a16 || !g.norms) return cudaErrorInvalidValue;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -495,14 +626,19 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
     s_attr_dev = dev;
   }
   CUtensorMap ma, mb;
-  if (!make_map_i8(&ma, g.a, g.rows, g.K, tc::BM)) return cudaErrorInvalidValue;
-  if (!make_map_i8(&mb, g.w, (int64_t)g.E * g.N, g.K, tc::BN)) return cudaErrorInvalidValue;
+  if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.a16, g.rows, g.K, tc::BM_CTA,
+                CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if (!make_map(&mb, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, g.w, (int64_t)g.E * g.N, g.K, tc::BN_CTA,
+                CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   tc::KParams p;
   p.rows = g.rows;
   p.N = g.N;
   p.K = g.K;
   p.E = g.E;
   p.seg = g.seg;
+  p.norms = g.norms;
   p.ep.act_mode = g.act_mode;
   p.ep.w_mode = g.w_mode;
   p.ep.s_x = g.s_x;
@@ -512,11 +648,11 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   p.ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
   p.y = static_cast<__nv_bfloat16*>(g.y);
   p.status = g.status;
-  // upper bound on work items (exact for a dense launch)
   const int64_t nt_n = (g.N + tc::BN - 1) / tc::BN;
   const int64_t tiles_ub = g.seg ? ((g.rows + tc::BM - 1) / tc::BM + g.E) * nt_n : ((g.rows + tc::BM - 1) / tc::BM) * nt_n;
-  const int grid = (int)(tiles_ub < s_sms ? tiles_ub : s_sms);
-  tc::gemm_tc_kernel<<<grid, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
+  const int64_t max_pairs = s_sms / 2;
+  const int pairs = (int)(tiles_ub < max_pairs ? tiles_ub : max_pairs);
+  tc::gemm_tc_kernel<<<2 * pairs, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
   return cudaGetLastError();
 }
 

@@ -11,12 +11,16 @@ namespace w8a8 {
 struct EpiParams;
 
 // quant.cu
+// q_i8: int8 codes [rows, K] or nullptr; q_f16: the same codes as fp16 [rows, K] (the GEMM-ready
+// activation format) or nullptr; norm_out: sum_k |q| per row (with q_f16); sum_out: sum_k q.
 cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t ldx,
-                       const int64_t* row_index, int8_t* q, float* scale, int32_t* zp,
-                       int32_t* sum_out, cudaStream_t st);
+                       const int64_t* row_index, int8_t* q_i8, void* q_f16, float* scale, int32_t* zp,
+                       int32_t* sum_out, int32_t* norm_out, cudaStream_t st);
 cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, int32_t* out,
                      cudaStream_t st);
-cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, float* sg, cudaStream_t st);
+// gq: int8 codes, or g16 + norms: the packed (fp16 codes + row L1 norms) format
+cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, void* g16, int32_t* norms, float* sg,
+                           cudaStream_t st);
 cudaError_t moe_combine(const void* out, const int64_t* row_of, const float* tw, int64_t T, int topk,
                         int64_t H, void* y, cudaStream_t st);
 
@@ -46,7 +50,9 @@ bool requant_vec_ok(const uint8_t* w, const int8_t* q, int64_t K);
 // GEMM problem description shared by both GEMM engines.  Rows of A are grouped into
 // segments; segment e multiplies weight rows [e*N, (e+1)*N).  A dense GEMM is one segment.
 struct GemmArgs {
-  const int8_t* a;      // [rows, K]
+  const int8_t* a;      // [rows, K] int8 codes (warp-MMA engine)
+  const void* a16;      // [rows, K] the same codes as fp16 (tcgen05 engine)
+  const int32_t* norms; // [rows] sum_k |a[r, k]| (tcgen05 engine)
   const int8_t* w;      // [E*N, K]
   int64_t rows;         // rows of A (dense M, or an upper bound for grouped)
   int64_t N, K;
@@ -66,6 +72,8 @@ struct GemmArgs {
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st);
 // gemm_tc.cu: tcgen05 kernel; returns cudaErrorNotSupported when it cannot run
 cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st);
+// int8 codes -> fp16 codes + row L1 norms (K % 16 == 0, 16-byte aligned rows)
+cudaError_t to_gemm_ready(const int8_t* a, int64_t rows, int64_t K, void* a16, int32_t* norms, cudaStream_t st);
 int gemm_tc_max_segments();
 
 }  // namespace w8a8

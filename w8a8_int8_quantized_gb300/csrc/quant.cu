@@ -114,11 +114,12 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
 // MODE: w8a8_act_mode.  row_index: optional gather (MoE), sum_out: optional per-row sum
 // of q (weight azp_adj).
 // ---------------------------------------------------------------------------
-template <int MODE, int THREADS>
+template <int MODE, int THREADS, bool F16>
 __global__ void __launch_bounds__(THREADS)
 quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
-               const int64_t* __restrict__ row_index, int8_t* __restrict__ q,
-               float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out) {
+               const int64_t* __restrict__ row_index, int8_t* __restrict__ q, __half* __restrict__ q16,
+               float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out,
+               int32_t* __restrict__ norm_out) {
   __shared__ float sh[THREADS / 32];
   __shared__ int shi[THREADS / 32];
   const int64_t row = blockIdx.x;
@@ -156,8 +157,7 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
     rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
     rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
   }
-  int qsum = 0;
-  uint2* qr = reinterpret_cast<uint2*>(q + row * K);
+  int qsum = 0, qabs = 0;
 #pragma unroll
   for (int i = 0; i < kMaxVec; ++i) {
     const int idx = threadIdx.x + i * THREADS;
@@ -169,11 +169,21 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
       for (int j = 0; j < 8; ++j) {
         c[j] = apply_rq(rq, f[j]);
         qsum += c[j];
+        qabs += abs(c[j]);
       }
-      uint2 o;
-      o.x = pack4_i8(c[0], c[1], c[2], c[3]);
-      o.y = pack4_i8(c[4], c[5], c[6], c[7]);
-      qr[idx] = o;
+      if (F16) {
+        uint4 o;
+        o.x = pack_f16x2(c[0], c[1]);
+        o.y = pack_f16x2(c[2], c[3]);
+        o.z = pack_f16x2(c[4], c[5]);
+        o.w = pack_f16x2(c[6], c[7]);
+        reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
+      } else {
+        uint2 o;
+        o.x = pack4_i8(c[0], c[1], c[2], c[3]);
+        o.y = pack4_i8(c[4], c[5], c[6], c[7]);
+        reinterpret_cast<uint2*>(q + row * K)[idx] = o;
+      }
     }
   }
   if (threadIdx.x == 0) {
@@ -184,6 +194,10 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
     const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
     if (threadIdx.x == 0) sum_out[row] = tot;
   }
+  if (F16) {
+    const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
+    if (threadIdx.x == 0) norm_out[row] = tot;
+  }
 }
 
 // ---------------------------------------------------------------------------
@@ -192,9 +206,9 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
 template <int MODE, int THREADS>
 __global__ void __launch_bounds__(THREADS)
 quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
-                   const int64_t* __restrict__ row_index, int8_t* __restrict__ q,
+                   const int64_t* __restrict__ row_index, int8_t* __restrict__ q, __half* __restrict__ q16,
                    float* __restrict__ scale, int32_t* __restrict__ zp,
-                   int32_t* __restrict__ sum_out) {
+                   int32_t* __restrict__ sum_out, int32_t* __restrict__ norm_out) {
   __shared__ float sh[THREADS / 32];
   __shared__ int shi[THREADS / 32];
   const int64_t row = blockIdx.x;
@@ -220,11 +234,13 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
     rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
     rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
   }
-  int qsum = 0;
+  int qsum = 0, qabs = 0;
   for (int64_t k = threadIdx.x; k < K; k += THREADS) {
     const int c = apply_rq(rq, __bfloat162float(xr[k]));
-    q[row * K + k] = (int8_t)c;
+    if (q16) q16[row * K + k] = __int2half_rn(c);
+    else q[row * K + k] = (int8_t)c;
     qsum += c;
+    qabs += abs(c);
   }
   if (threadIdx.x == 0) {
     if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
@@ -234,38 +250,59 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
     const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
     if (threadIdx.x == 0) sum_out[row] = tot;
   }
+  if (norm_out) {
+    const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
+    if (threadIdx.x == 0) norm_out[row] = tot;
+  }
 }
 
 template <int MODE>
 static cudaError_t launch_quant_rows(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx,
-                                     const int64_t* row_index, int8_t* q, float* scale, int32_t* zp,
-                                     int32_t* sum_out, cudaStream_t st) {
+                                     const int64_t* row_index, int8_t* q, __half* q16, float* scale,
+                                     int32_t* zp, int32_t* sum_out, int32_t* norm_out, cudaStream_t st) {
   const bool aligned = (K % 8 == 0) && (ldx % 8 == 0) && ((reinterpret_cast<uintptr_t>(x) & 15) == 0) &&
-                       ((reinterpret_cast<uintptr_t>(q) & 7) == 0);
+                       (q16 ? ((reinterpret_cast<uintptr_t>(q16) & 15) == 0)
+                            : ((reinterpret_cast<uintptr_t>(q) & 7) == 0));
   const int64_t nvec = K / 8;
   if (aligned && nvec <= (int64_t)kMaxVec * 128) {
-    quant_rows_vec<MODE, 128><<<(unsigned)rows, 128, 0, st>>>(x, K, ldx, row_index, q, scale, zp, sum_out);
+    if (q16)
+      quant_rows_vec<MODE, 128, true><<<(unsigned)rows, 128, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
+                                                                       sum_out, norm_out);
+    else
+      quant_rows_vec<MODE, 128, false><<<(unsigned)rows, 128, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
+                                                                        sum_out, norm_out);
   } else if (aligned && nvec <= (int64_t)kMaxVec * 256) {
-    quant_rows_vec<MODE, 256><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, scale, zp, sum_out);
+    if (q16)
+      quant_rows_vec<MODE, 256, true><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
+                                                                       sum_out, norm_out);
+    else
+      quant_rows_vec<MODE, 256, false><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
+                                                                        sum_out, norm_out);
   } else {
-    quant_rows_generic<MODE, 256><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, scale, zp, sum_out);
+    quant_rows_generic<MODE, 256><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
+                                                                   sum_out, norm_out);
   }
   return cudaGetLastError();
 }
 
 cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t ldx,
-                       const int64_t* row_index, int8_t* q, float* scale, int32_t* zp,
-                       int32_t* sum_out, cudaStream_t st) {
+                       const int64_t* row_index, int8_t* q, void* q_f16, float* scale, int32_t* zp,
+                       int32_t* sum_out, int32_t* norm_out, cudaStream_t st) {
   const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  __half* qh = static_cast<__half*>(q_f16);
   switch (mode) {
     case W8A8_ACT_DYN_TOKEN_SYM:
-      return launch_quant_rows<W8A8_ACT_DYN_TOKEN_SYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+      return launch_quant_rows<W8A8_ACT_DYN_TOKEN_SYM>(xb, rows, K, ldx, row_index, q, qh, scale, zp, sum_out,
+                                                       norm_out, st);
     case W8A8_ACT_DYN_TOKEN_ASYM:
-      return launch_quant_rows<W8A8_ACT_DYN_TOKEN_ASYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+      return launch_quant_rows<W8A8_ACT_DYN_TOKEN_ASYM>(xb, rows, K, ldx, row_index, q, qh, scale, zp, sum_out,
+                                                        norm_out, st);
     case W8A8_ACT_STATIC_TENSOR_SYM:
-      return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_SYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+      return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_SYM>(xb, rows, K, ldx, row_index, q, qh, scale, zp,
+                                                           sum_out, norm_out, st);
     default:
-      return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_ASYM>(xb, rows, K, ldx, row_index, q, scale, zp, sum_out, st);
+      return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_ASYM>(xb, rows, K, ldx, row_index, q, qh, scale, zp,
+                                                            sum_out, norm_out, st);
   }
 }
 
@@ -305,11 +342,12 @@ cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, i
 // MoE glue: g = bf16(silu(gate) * up) then per-row symmetric quantization.
 // h row = [gate (I) | up (I)], I % 8 == 0.
 // ---------------------------------------------------------------------------
-template <int THREADS>
+template <int THREADS, bool F16>
 __global__ void __launch_bounds__(THREADS)
 silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t I, int8_t* __restrict__ gq,
-                      float* __restrict__ sg) {
+                      __half* __restrict__ g16, int32_t* __restrict__ norm_out, float* __restrict__ sg) {
   __shared__ float sh[THREADS / 32];
+  __shared__ int shi[THREADS / 32];
   const int64_t row = blockIdx.x;
   const uint4* gate = reinterpret_cast<const uint4*>(h + row * 2 * I);
   const uint4* up = reinterpret_cast<const uint4*>(h + row * 2 * I + I);
@@ -335,29 +373,50 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t I, int8_t* __
     }
   }
   const RowQuant rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
-  uint2* qr = reinterpret_cast<uint2*>(gq + row * I);
+  int qabs = 0;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
     const int idx = threadIdx.x + i * THREADS;
     if (idx < nvec) {
       int c[8];
 #pragma unroll
-      for (int j = 0; j < 8; ++j) c[j] = quant_sym(g[i][j], rq.s);
-      uint2 o;
-      o.x = pack4_i8(c[0], c[1], c[2], c[3]);
-      o.y = pack4_i8(c[4], c[5], c[6], c[7]);
-      qr[idx] = o;
+      for (int j = 0; j < 8; ++j) {
+        c[j] = quant_sym(g[i][j], rq.s);
+        qabs += abs(c[j]);
+      }
+      if (F16) {
+        uint4 o;
+        o.x = pack_f16x2(c[0], c[1]);
+        o.y = pack_f16x2(c[2], c[3]);
+        o.z = pack_f16x2(c[4], c[5]);
+        o.w = pack_f16x2(c[6], c[7]);
+        reinterpret_cast<uint4*>(g16 + row * I)[idx] = o;
+      } else {
+        uint2 o;
+        o.x = pack4_i8(c[0], c[1], c[2], c[3]);
+        o.y = pack4_i8(c[4], c[5], c[6], c[7]);
+        reinterpret_cast<uint2*>(gq + row * I)[idx] = o;
+      }
     }
   }
   if (threadIdx.x == 0) sg[row] = rq.s;
+  if (F16) {
+    const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
+    if (threadIdx.x == 0) norm_out[row] = tot;
+  }
 }
 
-cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, float* sg, cudaStream_t st) {
+cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, void* g16, int32_t* norms, float* sg,
+                           cudaStream_t st) {
   const int64_t nvec = I / 8;
+  const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
+  __half* gh = static_cast<__half*>(g16);
   if (nvec <= 4 * 128) {
-    silu_mul_quant_kernel<128><<<(unsigned)R, 128, 0, st>>>(static_cast<const __nv_bfloat16*>(h), I, gq, sg);
+    if (g16) silu_mul_quant_kernel<128, true><<<(unsigned)R, 128, 0, st>>>(hb, I, gq, gh, norms, sg);
+    else silu_mul_quant_kernel<128, false><<<(unsigned)R, 128, 0, st>>>(hb, I, gq, gh, norms, sg);
   } else if (nvec <= 4 * 512) {
-    silu_mul_quant_kernel<512><<<(unsigned)R, 512, 0, st>>>(static_cast<const __nv_bfloat16*>(h), I, gq, sg);
+    if (g16) silu_mul_quant_kernel<512, true><<<(unsigned)R, 512, 0, st>>>(hb, I, gq, gh, norms, sg);
+    else silu_mul_quant_kernel<512, false><<<(unsigned)R, 512, 0, st>>>(hb, I, gq, gh, norms, sg);
   } else {
     return cudaErrorInvalidValue;
   }
