@@ -11,8 +11,8 @@
 //     |any partial sum| <= 2^17 * 128 = 2^24 and the fp32 accumulator over the whole K is
 //     exact (the activation producer writes these row L1 norms next to the fp16 codes);
 //   - chunked: otherwise the K loop is cut into chunks of 1024 (1024 * 128 * 128 = 2^24),
-//     each chunk goes to a fresh TMEM accumulator, and the epilogue adds the chunks'
-//     exact fp32 results into int32 registers.
+//     each chunk goes to TMEM buffer 0, and the epilogue adds the chunk's exact fp32 result
+//     into an int32 running sum kept in TMEM buffer 1 (tcgen05.ld / tcgen05.st).
 // Either way the result equals the int32 GEMM exactly, for any int8 data.
 //
 // Shape.  CTA pairs (cluster of 2, `cta_group::2`) compute 256 x 256 output tiles with
@@ -20,11 +20,11 @@
 // own 128 activation rows and its 128-row half of the weight tile, so a CTA converts only
 // 128 x 64 weight bytes per K step.
 //   activations: fp16 integer codes [rows, K] -> TMA, 128-byte swizzle, straight into the
-//                MMA operand ring (5 stages x 32 KB)
-//   weights:     int8 [E*N, K] -> TMA -> int8 staging ring (6 stages x 8 KB) -> 4 converter
-//                warps: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152) into the swizzled
-//                operand layout
-//   accumulator: two 256-column fp32 TMEM buffers per CTA, alternating per chunk/tile
+//                MMA operand ring (7 stages x 16 KB)
+//   weights:     int8 [E*N, K] -> TMA -> int8 staging ring (4 x 8 KB) -> 4 converter warps,
+//                each owning every 4th K step: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152)
+//                into the swizzled operand layout (4 x 16 KB)
+//   accumulator: two 256-column TMEM buffers per CTA, alternating per single-pass tile
 //   epilogue:    8 warps per CTA read TMEM, apply y = bf16((s_x*s_w) * f32(acc - zp*azp_adj)
 //                + bias), store.
 // The pair is persistent and walks a static list of (segment, row tile, column tile) work
@@ -50,27 +50,30 @@ constexpr int BM_CTA = 128;    // activation rows per CTA
 constexpr int BN = 256;        // weight rows (output columns) per pair tile
 constexpr int BN_CTA = 128;    // weight rows converted and held per CTA
 constexpr int BK = 64;
-constexpr int S16 = 5;
-constexpr int S8 = 6;
+constexpr int SA = 7;          // activation ring (fp16 tiles straight from TMA)
+constexpr int CONV_WARPS = 4;  // converter warp w owns the K steps it with it % 4 == w
+constexpr int SB = CONV_WARPS; // converted weight ring: slot w belongs to converter warp w
+constexpr int S8 = CONV_WARPS; // int8 weight staging ring: slot w belongs to converter warp w
 constexpr int CHUNK_STEPS = 16;   // 16 * 64 = 1024 K per exact fp32 chunk
 constexpr int32_t kNormSingle = 131072;  // row L1 norm below 2^17 -> single pass is exact
 constexpr int A16 = BM_CTA * BK * 2;     // 16 KB
 constexpr int B16 = BN_CTA * BK * 2;     // 16 KB
-constexpr int STAGE16 = A16 + B16;
 constexpr int B8 = BN_CTA * BK;          // 8 KB
-constexpr int DATA_BYTES = S16 * STAGE16 + S8 * B8;
+constexpr int OFF_B16 = SA * A16;
+constexpr int OFF_B8 = OFF_B16 + SB * B16;
+constexpr int DATA_BYTES = OFF_B8 + S8 * B8;
 constexpr int MAX_SEG = 1024;
 constexpr int NUM_THREADS = 512;
 constexpr int TMEM_COLS = 512;
 constexpr int EPI_WARPS = 8;
-constexpr int CONV_WARPS = 4;
 
 struct __align__(8) Bars {
-  uint64_t full_a[S16];    // activation tile landed (TMA tx)
-  uint64_t full16[S16];    // both CTAs' operands ready (leader only; 2 x CONV_WARPS arrivals)
-  uint64_t empty16[S16];   // MMAs reading the stage finished (multicast commit)
+  uint64_t full_a[SA];     // activation tile landed (TMA tx)
+  uint64_t empty_a[SA];    // MMAs reading the activation slot finished (multicast commit)
+  uint64_t full16[SB];     // both CTAs' operands of the step ready (leader only; 2 arrivals)
+  uint64_t empty16[SB];    // MMAs reading the converted weight slot finished (multicast commit)
   uint64_t full8[S8];      // int8 weight tile landed (TMA tx)
-  uint64_t empty8[S8];     // converters done reading the int8 tile
+  uint64_t empty8[S8];     // converter done reading the int8 tile
   uint64_t accfull[2];     // accumulator buffer ready (multicast commit)
   uint64_t accempty[2];    // both CTAs drained the buffer (leader only; 2 x EPI_WARPS arrivals)
   uint64_t mma_done;
@@ -226,6 +229,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&r)[32]) {
 }
 __device__ __forceinline__ void tmem_ld_wait() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const int32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};\n" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+      "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]), "r"(v[17]),
+      "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]), "r"(v[25]), "r"(v[26]),
+      "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+
 // int8 x 4 -> fp16 x 4, exact: (v ^ 0x80) is v + 128 as an unsigned byte; placing it in the
 // mantissa of 1024.0 (0x6400) gives 1024 + 128 + v, and subtracting 1152 leaves v.
 __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
@@ -288,8 +304,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* ring16 = smem;
-  uint8_t* ring8 = smem + S16 * STAGE16;
+  uint8_t* ringA = smem;
+  uint8_t* ringB16 = smem + OFF_B16;
+  uint8_t* ring8 = smem + OFF_B8;
   Bars* bars = reinterpret_cast<Bars*>(smem + DATA_BYTES);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -300,14 +317,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   const int nkb = (int)((p.K + BK - 1) / BK);
 
   if (threadIdx.x == 0) {
-    for (int i = 0; i < S16; ++i) {
+    for (int i = 0; i < SA; ++i) {
       mbar_init(&bars->full_a[i], 1);
-      mbar_init(&bars->full16[i], 2 * CONV_WARPS);
+      mbar_init(&bars->empty_a[i], 1);
+    }
+    for (int i = 0; i < SB; ++i) {
+      mbar_init(&bars->full16[i], 2);
       mbar_init(&bars->empty16[i], 1);
     }
     for (int i = 0; i < S8; ++i) {
       mbar_init(&bars->full8[i], 1);
-      mbar_init(&bars->empty8[i], CONV_WARPS);
+      mbar_init(&bars->empty8[i], 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&bars->accfull[i], 1);
@@ -341,7 +361,6 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (each CTA)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
     if (lane == 0) {
       uint32_t nb = 0, na = 0;  // weight / activation copies issued
       bool ok = true;
@@ -350,55 +369,67 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int32_t arow = (int32_t)(tl.row0 + BM_CTA * rank);
         const int32_t brow = (int32_t)((int64_t)tl.e * p.N + tl.n0 + BN_CTA * rank);
         for (int kb = 0; kb < nkb; ++kb) {
+          const uint32_t sa = na % SA, pha = (na / SA) & 1;
+          if (!wait_bar(&bars->empty_a[sa], pha ^ 1, bars, p.status)) { ok = false; break; }
+          mbar_expect_tx(&bars->full_a[sa], A16);
+          tma_load_2d(ringA + sa * A16, &tmA, kb * BK, arow, &bars->full_a[sa]);
+          ++na;
           const uint32_t s8 = nb % S8, ph8 = (nb / S8) & 1;
           if (!wait_bar(&bars->empty8[s8], ph8 ^ 1, bars, p.status)) { ok = false; break; }
           mbar_expect_tx(&bars->full8[s8], B8);
           tma_load_2d(ring8 + s8 * B8, &tmB, kb * BK, brow, &bars->full8[s8]);
           ++nb;
-          const uint32_t s16 = na % S16, ph16 = (na / S16) & 1;
-          if (!wait_bar(&bars->empty16[s16], ph16 ^ 1, bars, p.status)) { ok = false; break; }
-          mbar_expect_tx(&bars->full_a[s16], A16);
-          tma_load_2d(ring16 + s16 * STAGE16, &tmA, kb * BK, arow, &bars->full_a[s16]);
-          ++na;
         }
       }
       // every issued copy must land before the CTA may exit
       for (uint32_t j = (nb > (uint32_t)S8 ? nb - S8 : 0); j < nb; ++j)
         drain_wait(&bars->full8[j % S8], (j / S8) & 1, p.status);
-      for (uint32_t j = (na > (uint32_t)S16 ? na - S16 : 0); j < na; ++j)
-        drain_wait(&bars->full_a[j % S16], (j / S16) & 1, p.status);
+      for (uint32_t j = (na > (uint32_t)SA ? na - SA : 0); j < na; ++j)
+        drain_wait(&bars->full_a[j % SA], (j / SA) & 1, p.status);
     }
   } else if (warp == 1) {
     // ---------------------------------------------------------------- MMA issuer (even CTA)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
+    // Accumulator buffers: a single-pass tile takes the next buffer (alternating, so its
+    // epilogue overlaps the following tile's MMAs).  A chunked tile takes both: buffer 0
+    // receives each 1024-K chunk, buffer 1 is the epilogue's int32 running sum.  Every
+    // acquisition of a buffer waits for the epilogue's release of the previous one.
     if (rank == 0) {
-      uint32_t it = 0, ch = 0;
+      uint32_t it = 0, nbuf = 0;
+      uint32_t acq0 = 0u, acq1 = 0u;  // acquisitions of buffer 0 / 1 so far
       bool ok = true;
       for (int t = pair; t < tiles && ok; t += npairs) {
         const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
-        const int spc = tile_single_pass(p, tl, lane) ? nkb : CHUNK_STEPS;
+        const bool single = tile_single_pass(p, tl, lane);
         if (lane == 0) {
+          const int spc = single ? nkb : CHUNK_STEPS;
           uint32_t b = 0;
-          for (int kb = 0; kb < nkb; ++kb, ++it) {
+          if (single) {
+            b = nbuf;
+            nbuf ^= 1u;
+          } else {
+            if (!wait_bar(&bars->accempty[1], (acq1 & 1) ^ 1, bars, p.status)) ok = false;
+            ++acq1;
+          }
+          for (int kb = 0; kb < nkb && ok; ++kb, ++it) {
             if (kb % spc == 0) {
-              b = ch & 1;
-              if (!wait_bar(&bars->accempty[b], ((ch >> 1) & 1) ^ 1, bars, p.status)) { ok = false; break; }
+              const uint32_t a = b ? acq1 : acq0;
+              if (!wait_bar(&bars->accempty[b], (a & 1) ^ 1, bars, p.status)) { ok = false; break; }
+              if (b) ++acq1; else ++acq0;
               tc_fence_after();
             }
-            const uint32_t s = it % S16, ph = (it / S16) & 1;
-            if (!wait_bar(&bars->full16[s], ph, bars, p.status)) { ok = false; break; }
+            const uint32_t sb = it % SB, phb = (it / SB) & 1;
+            if (!wait_bar(&bars->full16[sb], phb, bars, p.status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t abase = su32(ring16 + s * STAGE16);
-            const uint32_t bbase = abase + A16;
+            const uint32_t sa = it % SA;
+            const uint32_t abase = su32(ringA + sa * A16);
+            const uint32_t bbase = su32(ringB16 + sb * B16);
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               mma_f16_pair(tmem + b * BN, desc_sw128(abase + kk * 32), desc_sw128(bbase + kk * 32),
                            (kb % spc != 0 || kk != 0) ? 1u : 0u);
-            mma_commit_pair(&bars->empty16[s]);
-            if (kb % spc == spc - 1 || kb == nkb - 1) {
-              mma_commit_pair(&bars->accfull[b]);
-              ++ch;
-            }
+            mma_commit_pair(&bars->empty_a[sa]);
+            mma_commit_pair(&bars->empty16[sb]);
+            if (kb % spc == spc - 1 || kb == nkb - 1) mma_commit_pair(&bars->accfull[b]);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -412,49 +443,56 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       }
     }
   } else if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 40;\n");
   } else if (warp < 8) {
     // ---------------------------------------------------------------- converters (each CTA)
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 72;\n");
-    const int ct = threadIdx.x - 128;  // 0..127
-    uint32_t it = 0;
+    // Warp w converts whole K steps it = w, w + 4, ...: the 128 x 64 int8 weight tile of the
+    // step (int8 slot w) into the fp16 operand layout (fp16 slot w), so four steps are in
+    // flight at once and the per-step synchronisation latency overlaps.
+    const int cw = warp - 4;
+    const uint32_t full16_leader = map_to(su32(&bars->full16[cw]), 0);
+    const uint8_t* src = ring8 + cw * B8;
+    uint8_t* dst = ringB16 + cw * B16;
+    uint32_t it = 0;  // global step counter (same sequence as the producer and the MMA)
+    uint32_t use = 0; // how many steps this warp has converted
     bool ok = true;
     for (int t = pair; t < tiles && ok; t += npairs) {
       for (int kb = 0; kb < nkb; ++kb, ++it) {
-        const uint32_t s8 = it % S8, ph8 = (it / S8) & 1;
-        const uint32_t s16 = it % S16, ph16 = (it / S16) & 1;
+        if ((int)(it % CONV_WARPS) != cw) continue;
+        const uint32_t ph = use & 1;
+        ++use;
         // every lane waits; the outcome is made warp-uniform so the warp stays converged
-        if (!__all_sync(0xffffffffu, wait_bar(&bars->full8[s8], ph8, bars, p.status))) { ok = false; break; }
-        if (!__all_sync(0xffffffffu, wait_bar(&bars->empty16[s16], ph16 ^ 1, bars, p.status))) { ok = false; break; }
-        const uint8_t* src = ring8 + s8 * B8;
-        uint8_t* dst = ring16 + s16 * STAGE16 + A16;
-        // 512 units of 16 int8 (128 rows x 4): 4 per thread
-        uint4 v[4];
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->full8[cw], ph, bars, p.status))) { ok = false; break; }
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->empty16[cw], ph ^ 1, bars, p.status))) { ok = false; break; }
+        // 512 units of 16 int8 (128 rows x 4): 16 per lane, in 4 batches
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = ct + 128 * i;
-          v[i] = *reinterpret_cast<const uint4*>(src + (u >> 2) * 64 + (u & 3) * 16);
-        }
+        for (int bt = 0; bt < 4; ++bt) {
+          uint4 v[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int u = ct + 128 * i;
-          const int r = u >> 2, sgm = u & 3;
-          uint32_t o[8];
-          i8x4_to_f16x4(v[i].x, o[0], o[1]);
-          i8x4_to_f16x4(v[i].y, o[2], o[3]);
-          i8x4_to_f16x4(v[i].z, o[4], o[5]);
-          i8x4_to_f16x4(v[i].w, o[6], o[7]);
-          uint8_t* rowp = dst + r * 128;
-          *reinterpret_cast<uint4*>(rowp + (((2 * sgm) ^ (r & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
-          *reinterpret_cast<uint4*>(rowp + (((2 * sgm + 1) ^ (r & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+          for (int i = 0; i < 4; ++i) {
+            const int u = lane + 32 * (4 * bt + i);
+            v[i] = *reinterpret_cast<const uint4*>(src + (u >> 2) * 64 + (u & 3) * 16);
+          }
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const int u = lane + 32 * (4 * bt + i);
+            const int r = u >> 2, sgm = u & 3;
+            uint32_t o[8];
+            i8x4_to_f16x4(v[i].x, o[0], o[1]);
+            i8x4_to_f16x4(v[i].y, o[2], o[3]);
+            i8x4_to_f16x4(v[i].z, o[4], o[5]);
+            i8x4_to_f16x4(v[i].w, o[6], o[7]);
+            uint8_t* rowp = dst + r * 128;
+            *reinterpret_cast<uint4*>(rowp + (((2 * sgm) ^ (r & 7)) * 16)) = make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(rowp + (((2 * sgm + 1) ^ (r & 7)) * 16)) = make_uint4(o[4], o[5], o[6], o[7]);
+          }
         }
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         __syncwarp();
         if (lane == 0) {
-          mbar_arrive_local(&bars->empty8[s8]);
-          // the activation tile of this stage must have landed before the pair's MMA reads it
-          if (!wait_bar(&bars->full_a[s16], ph16, bars, p.status)) ok = false;
-          else mbar_arrive_cluster(map_to(su32(&bars->full16[s16]), 0));
+          mbar_arrive_local(&bars->empty8[cw]);
+          // the activation tile of this step must have landed before the pair's MMA reads it
+          if (!wait_bar(&bars->full_a[it % SA], (it / SA) & 1, bars, p.status)) ok = false;
+          else mbar_arrive_cluster(full16_leader);
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
         if (!ok) break;
@@ -462,70 +500,90 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
   } else {
     // ---------------------------------------------------------------- epilogue (8 warps, each CTA)
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 200;\n");
-    const int q = warp & 3;            // TMEM lane quadrant this warp may access
-    const int h = (warp - 8) >> 2;     // column half
+    // Warp (q, h) owns TMEM lanes 32q..32q+31 (its CTA's rows) and columns 128h..128h+127,
+    // processed in groups of 32 columns.
+    const int q = warp & 3;
+    const int h = (warp - 8) >> 2;
     const uint32_t accempty0 = map_to(su32(&bars->accempty[0]), 0);
     const uint32_t accempty1 = map_to(su32(&bars->accempty[1]), 0);
-    uint32_t ch = 0;
+    const uint32_t lanebase = tmem + ((uint32_t)(q * 32) << 16) + h * 128;
+    uint32_t nbuf = 0;
+    uint32_t filled0 = 0u, filled1 = 0u;  // fills of buffer 0 / 1 consumed so far
     bool ok = true;
     for (int t = pair; t < tiles && ok; t += npairs) {
       const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
       const bool single = tile_single_pass(p, tl, lane);
+      const int64_t m = tl.row0 + BM_CTA * rank + q * 32 + lane;
+      const bool row_ok = m < tl.row_end;
+      EpiParams ep = p.ep;
+      if (ep.w_mode == W8A8_W_CHANNEL) ep.s_w = p.ep.s_w + (int64_t)tl.e * p.N;
+      const float sx = row_ok ? epi_row_scale(ep, m) : 0.f;
+      const int zpm = row_ok ? epi_row_zp(ep, m) : 0;
+      const int64_t nb = tl.n0 + h * 128;
+      __nv_bfloat16* yrow = p.y + (row_ok ? m : 0) * p.N;
       const int nch = single ? 1 : (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
-      int32_t acc[128];
-      for (int c = 0; c < nch; ++c, ++ch) {
-        const uint32_t b = ch & 1;
-        if (!__all_sync(0xffffffffu, wait_bar(&bars->accfull[b], (ch >> 1) & 1, bars, p.status))) {
+      const uint32_t b = single ? nbuf : 0u;
+      if (single) nbuf ^= 1u;
+      for (int c = 0; c < nch; ++c) {
+        const uint32_t fcount = b ? filled1 : filled0;
+        if (!__all_sync(0xffffffffu, wait_bar(&bars->accfull[b], fcount & 1, bars, p.status))) {
           ok = false;
           break;
         }
+        if (b) ++filled1; else ++filled0;
         tc_fence_after();
-        const uint32_t tbase = tmem + ((uint32_t)(q * 32) << 16) + b * BN + h * 128;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
+        const bool last = (c == nch - 1);
+#pragma unroll 1
+        for (int g = 0; g < 4; ++g) {
           uint32_t r[32];
-          tmem_ld32(tbase + j * 32, r);
-          tmem_ld_wait();
+          tmem_ld32(lanebase + b * BN + g * 32, r);
+          int32_t v[32];
+          if (c > 0) {
+            uint32_t pr[32];
+            tmem_ld32(lanebase + BN + g * 32, pr);  // running int32 sum (buffer 1)
+            tmem_ld_wait();
 #pragma unroll
-          for (int i = 0; i < 32; ++i) {
-            const int32_t v = __float2int_rn(__uint_as_float(r[i]));
-            acc[j * 32 + i] = (c == 0) ? v : acc[j * 32 + i] + v;
+            for (int i = 0; i < 32; ++i) v[i] = (int32_t)pr[i] + __float2int_rn(__uint_as_float(r[i]));
+          } else {
+            tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) v[i] = __float2int_rn(__uint_as_float(r[i]));
+          }
+          if (!last) {
+            tmem_st32(lanebase + BN + g * 32, v);
+          } else if (row_ok) {
+            const int64_t n0 = nb + g * 32;
+            if (((p.N & 7) == 0) && n0 + 32 <= p.N) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) f[i] = epi_apply(ep, v[8 * j + i], sx, zpm, n0 + 8 * j + i);
+                uint4 o;
+                o.x = pack_bf16x2(f[0], f[1]);
+                o.y = pack_bf16x2(f[2], f[3]);
+                o.z = pack_bf16x2(f[4], f[5]);
+                o.w = pack_bf16x2(f[6], f[7]);
+                *reinterpret_cast<uint4*>(yrow + n0 + 8 * j) = o;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (n0 + i < p.N) yrow[n0 + i] = __float2bfloat16_rn(epi_apply(ep, v[i], sx, zpm, n0 + i));
+            }
           }
         }
+        if (!last) tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive_cluster(b ? accempty1 : accempty0);
       }
       if (!ok) break;
-      const int64_t m = tl.row0 + BM_CTA * rank + q * 32 + lane;
-      if (m < tl.row_end) {
-        EpiParams ep = p.ep;
-        if (ep.w_mode == W8A8_W_CHANNEL) ep.s_w = p.ep.s_w + (int64_t)tl.e * p.N;
-        const float sx = epi_row_scale(ep, m);
-        const int zpm = epi_row_zp(ep, m);
-        const int64_t nb = tl.n0 + h * 128;
-        __nv_bfloat16* yrow = p.y + m * p.N;
-        const bool vec = ((p.N & 7) == 0);
-#pragma unroll
-        for (int gI = 0; gI < 16; ++gI) {
-          const int64_t n = nb + gI * 8;
-          if (vec && n + 8 <= p.N) {
-            float f[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) f[i] = epi_apply(ep, acc[gI * 8 + i], sx, zpm, n + i);
-            uint4 o;
-            o.x = pack_bf16x2(f[0], f[1]);
-            o.y = pack_bf16x2(f[2], f[3]);
-            o.z = pack_bf16x2(f[4], f[5]);
-            o.w = pack_bf16x2(f[6], f[7]);
-            *reinterpret_cast<uint4*>(yrow + n) = o;
-          } else {
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-              if (n + i < p.N) yrow[n + i] = __float2bfloat16_rn(epi_apply(ep, acc[gI * 8 + i], sx, zpm, n + i));
-          }
-        }
+      if (!single) {
+        // the running-sum buffer is free again
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive_cluster(accempty1);
       }
     }
   }
