@@ -121,9 +121,14 @@ __device__ __forceinline__ void mbar_init(uint64_t* b, uint32_t count) {
 __device__ __forceinline__ void mbar_arrive_local(uint64_t* b) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];\n" ::"r"(su32(b)) : "memory");
 }
-// arrive on a barrier given by its shared::cluster address (own CTA or the peer)
+// Arrive on a barrier given by its shared::cluster address (own CTA or the peer).
+// CTA-scope release: everything a CTA publishes to its peer this way lives in the
+// publishing CTA's own shared memory (converted weight tiles, landed activation tiles) or
+// TMEM, and is handed to the tensor-core (async) proxy by fence.proxy.async /
+// tcgen05.fence before the arrive.  A cluster-scope release would add a fence costing
+// ~1.6k cycles per arrive on this part without ordering anything more that the MMA needs.
 __device__ __forceinline__ void mbar_arrive_cluster(uint32_t caddr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(caddr) : "memory");
+  asm volatile("mbarrier.arrive.release.cta.shared::cluster.b64 _, [%0];\n" ::"r"(caddr) : "memory");
 }
 __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;\n" ::"r"(su32(b)), "r"(bytes)
@@ -132,7 +137,7 @@ __device__ __forceinline__ void mbar_expect_tx(uint64_t* b, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try(uint64_t* b, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      "{\n.reg .pred p;\nmbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n"
       "selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
       : "r"(su32(b)), "r"(parity)
