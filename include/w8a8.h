@@ -271,6 +271,30 @@ w8a8_status w8a8_moe_quantize_gather_packed(const void* x, int64_t T, int64_t K,
 w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void* packed,
                                        float* s_g, cudaStream_t stream);
 
+/*
+ * w8a8_scaled_mm_noalloc -- w8a8_scaled_mm without a workspace, for callers that cannot
+ * allocate device memory (a host runtime that owns only the tensors it passes in and has no
+ * allocator to lend, or a latency-critical path where cudaMalloc's possible device-wide
+ * synchronization is not allowed).  The pages describe no counterpart: it exists only for
+ * such callers.
+ *   Arguments, results and requirements are those of w8a8_scaled_mm, except that there is
+ *   no workspace: the activations are staged in a 36 MiB buffer owned by the library (a
+ *   device array placed in GPU memory when the library's module is loaded on a device and
+ *   kept until the process exits).  It always runs the tensor-core engine.
+ *   Limit: roundup(M*K*2, 256) + roundup(M*4, 256) <= 36 MiB (e.g. M*K up to 4096 x 4096);
+ *   larger problems return W8A8_ERR_WORKSPACE before any launch.
+ *   The first call on each device looks up the buffer's device address (no allocation) and
+ *   caches it; make that first call before any stream capture.
+ *   All calls on a device share the one buffer, which keeps the last call's contents; every
+ *   call rewrites all of it that it reads, so nothing needs clearing.  Calls whose work
+ *   overlaps on the same GPU (e.g. issued to two streams at once) race on the buffer.
+ */
+w8a8_status w8a8_scaled_mm_noalloc(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N,
+                                   int64_t K, int act_mode, const float* s_x, const int32_t* zp,
+                                   const int32_t* azp_adj, int w_mode, const float* s_w,
+                                   const void* bias, void* y, int32_t* dev_status,
+                                   cudaStream_t stream);
+
 #ifdef __cplusplus
 }
 #endif

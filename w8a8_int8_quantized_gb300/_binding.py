@@ -53,6 +53,7 @@ SIGNATURES = {
     "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_gather_packed": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     "w8a8_silu_mul_quant_packed": (_I, [_P, _I64, _I64, _P, _P, _P]),
+    "w8a8_scaled_mm_noalloc": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
 }
 
 _lib = None
