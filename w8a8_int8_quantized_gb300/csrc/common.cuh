@@ -19,6 +19,22 @@ namespace w8a8 {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
+// rint(RN(x / s)) -- the IEEE float32 quotient rounded half to even -- without a division
+// in the common case.  r = RN(1/s) is computed once per row.  t = RN(x*r) differs from the
+// exact x/s by at most |x/s|*(2^-23 + 2^-48), and RN(x/s) by at most |x/s|*2^-24, so when t
+// is more than |t|*2^-20 away from every half-integer both lie strictly inside the same
+// interval between half-integers and round to the same integer.  Otherwise (rare: about
+// |t|*2^-19 of the values near each half-integer, and always for |t| >= 2^19, or a
+// non-finite t) the exact IEEE division decides.  Every subtraction below is exact, so the
+// test itself is exact.  Returns the integer as a float.
+__device__ __forceinline__ float rint_div(float x, float s, float r) {
+  const float t = __fmul_rn(x, r);
+  const float n = rintf(t);
+  const float d = fabsf(__fsub_rn(fabsf(__fsub_rn(t, n)), 0.5f));
+  if (d > __fmul_rn(fabsf(t), 0x1p-20f)) return n;
+  return rintf(__fdiv_rn(x, s));
+}
+
 // rint(x / s) clamped to [-127, 127]
 __device__ __forceinline__ int quant_sym(float x, float s) {
   int v = __float2int_rn(__fdiv_rn(x, s));
@@ -32,6 +48,165 @@ __device__ __forceinline__ int quant_asym(float x, float s, int zp) {
   return (int)min(127ll, max(-128ll, v));
 }
 
+// The same integer as rint_div, returned as an int and computed without conversion-pipe
+// instructions on the fast path: for |t| < 2^22, t + 1.5*2^23 lands in [2^23, 2^24) where
+// float32 spacing is exactly 1, so the addition itself rounds t to the nearest integer
+// (ties to even), subtracting 1.5*2^23 back is exact, and the integer is the low mantissa
+// bits of the sum minus 2^22.  The fast path is only taken for |t| < 2^19.  The slow path
+// clamps to +-2^30 so that adding a zero point cannot overflow.
+__device__ __forceinline__ int rint_div_i(float x, float s, float r) {
+  const float t = __fmul_rn(x, r);
+  const float m = __fadd_rn(t, 12582912.0f);
+  const float n = __fsub_rn(m, 12582912.0f);
+  const float d = fabsf(__fsub_rn(fabsf(__fsub_rn(t, n)), 0.5f));
+  if (d > __fmul_rn(fabsf(t), 0x1p-20f)) return __float_as_int(m) - 0x4B400000;
+  const float e = rintf(__fdiv_rn(x, s));
+  return __float2int_rn(fminf(fmaxf(e, -1073741824.0f), 1073741824.0f));
+}
+
+// rint_div_i for quotients known to satisfy |x/s| <= 256 (a row divided by its own
+// absmax/127, or anything clamped to int8 range afterwards when it is that small): the
+// margin |t|*2^-20 is then at most 2^-12, used as a constant, and the slow path needs no
+// clamp.
+__device__ __forceinline__ int rint_div_small(float x, float s, float r) {
+  const float t = __fmul_rn(x, r);
+  const float m = __fadd_rn(t, 12582912.0f);
+  const float e = __fsub_rn(t, __fsub_rn(m, 12582912.0f));
+  if (fabsf(e) < 0.499755859375f) return __float_as_int(m) - 0x4B400000;  // 0.5 - 2^-12, exact
+  return __float2int_rn(rintf(__fdiv_rn(x, s)));
+}
+
+// ---- packed float32 pairs (sm_100+ f32x2 arithmetic): element 0 in the low 32 bits
+__device__ __forceinline__ uint64_t f2pack(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void f2unpack(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t f2mul(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2add(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
+  uint64_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+
+// Two values of a row quantized with the row's own absmax scale (|x / s| <= 256), the
+// rint_div_small rule applied to both lanes of a pair at once.  On return w0 / w1 hold
+// 0x4B400000 + q (the float bits of q + 1.5*2^23), so their low bytes are the int8 codes,
+// and n holds q0, q1 as exact floats.
+__device__ __forceinline__ void quant_pair_row(float x0, float x1, float s, float r, uint64_t r2,
+                                               uint32_t& w0, uint32_t& w1, uint64_t& n) {
+  const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
+  const uint64_t t = f2mul(f2pack(x0, x1), r2);
+  const uint64_t m = f2add(t, kMagic);
+  n = f2sub(m, kMagic);
+  float e0, e1, m0, m1;
+  f2unpack(f2sub(t, n), e0, e1);
+  f2unpack(m, m0, m1);
+  w0 = __float_as_uint(m0);
+  w1 = __float_as_uint(m1);
+  if (!(fmaxf(fabsf(e0), fabsf(e1)) < 0.499755859375f)) {  // 0.5 - 2^-12: decide by division
+    const float n0 = rintf(__fdiv_rn(x0, s)), n1 = rintf(__fdiv_rn(x1, s));
+    w0 = 0x4B400000u + (uint32_t)__float2int_rn(n0);
+    w1 = 0x4B400000u + (uint32_t)__float2int_rn(n1);
+    n = f2pack(n0, n1);
+  }
+}
+
+// N values of a row quantized with the row's own absmax scale (|x / s| <= 256): the
+// rint_div_small rule for a whole group, with the rare exact-division fallback hoisted out
+// of the common path.  On return b[j] = 0x4B400000 + q_j (its low byte is the int8 code).
+template <int N>
+__device__ __forceinline__ void quant_row_group(const float* x, float s, float r, uint32_t* b) {
+  float emax = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; ++j) {
+    const float t = __fmul_rn(x[j], r);
+    const float m = __fadd_rn(t, 12582912.0f);
+    const float e = __fsub_rn(t, __fsub_rn(m, 12582912.0f));
+    emax = fmaxf(emax, fabsf(e));
+    b[j] = __float_as_uint(m);
+  }
+  if (!(emax < 0.499755859375f)) {  // some value lies within 2^-12 of a tie: decide those exactly
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const float t = __fmul_rn(x[j], r);
+      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f));
+      if (!(fabsf(e) < 0.499755859375f)) b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(x[j], s)));
+    }
+  }
+}
+
+// quant_row_group on packed float32 pairs (N even): half the float instructions.
+template <int N>
+__device__ __forceinline__ void quant_row_group_x2(const float* x, float s, float r, uint32_t* b) {
+  const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
+  const uint64_t r2 = f2pack(r, r);
+  float emax = 0.f;
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const uint64_t t = f2mul(f2pack(x[j], x[j + 1]), r2);
+    const uint64_t m = f2add(t, kMagic);
+    float e0, e1, m0, m1;
+    f2unpack(f2sub(t, f2sub(m, kMagic)), e0, e1);
+    f2unpack(m, m0, m1);
+    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+    b[j] = __float_as_uint(m0);
+    b[j + 1] = __float_as_uint(m1);
+  }
+  if (!(emax < 0.499755859375f)) {  // some value lies within 2^-12 of a tie: decide those exactly
+#pragma unroll
+    for (int j = 0; j < N; ++j) {
+      const float t = __fmul_rn(x[j], r);
+      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f));
+      if (!(fabsf(e) < 0.499755859375f)) b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(x[j], s)));
+    }
+  }
+}
+
+// four int8 values (low bytes of a, b, c, d) packed into one word, byte 0 = a
+__device__ __forceinline__ uint32_t pack4_i8_prmt(int a, int b, int c, int d) {
+  const uint32_t lo = __byte_perm((uint32_t)a, (uint32_t)b, 0x0040);
+  const uint32_t hi = __byte_perm((uint32_t)c, (uint32_t)d, 0x0040);
+  return __byte_perm(lo, hi, 0x5410);
+}
+
+// int8 x 4 -> fp16 x 4, exact: (v ^ 0x80) is v + 128 as an unsigned byte; placing it in the
+// mantissa of 1024.0 (0x6400) gives 1024 + 128 + v, and subtracting 1152 leaves v.
+__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  const uint32_t x = w ^ 0x80808080u;
+  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
+  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
+  const uint32_t bias = 0x64806480u;  // 1152.0 in both halves
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(a), "r"(bias));
+  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(b), "r"(bias));
+}
+
+// Symmetric and affine quantization from a precomputed reciprocal (same results as
+// quant_sym / quant_asym).
+__device__ __forceinline__ int quant_sym_r(float x, float s, float r) {
+  return min(127, max(-127, rint_div_i(x, s, r)));
+}
+// a value of a row quantized with that row's own absmax scale: |x / s| <= 127 (+ rounding)
+__device__ __forceinline__ int quant_row_sym(float x, float s, float r) { return rint_div_small(x, s, r); }
+__device__ __forceinline__ int quant_asym_r(float x, float s, float r, int zp) {
+  // |rint| + |zp| stays far below 2^24 whenever the result is not clamped, so the float sum
+  // is exact there; larger magnitudes clamp either way
+  const float v = __fadd_rn(rint_div(x, s, r), (float)zp);
+  return __float2int_rn(fminf(fmaxf(v, -128.f), 127.f));
+}
+
 __device__ __forceinline__ uint32_t pack4_i8(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
          ((uint32_t)(d & 0xFF) << 24);
@@ -40,6 +215,12 @@ __device__ __forceinline__ uint32_t pack4_i8(int a, int b, int c, int d) {
 // two small integers (|v| <= 2048, exact in fp16) packed as fp16x2
 __device__ __forceinline__ uint32_t pack_f16x2(int lo, int hi) {
   __half2 v = __halves2half2(__int2half_rn(lo), __int2half_rn(hi));
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// two small integral floats (exact in fp16) packed as fp16x2
+__device__ __forceinline__ uint32_t pack_f16x2_f(float lo, float hi) {
+  __half2 v = __floats2half2_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
 }
 

@@ -247,17 +247,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const int32_t (&v)[32]
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 
-// int8 x 4 -> fp16 x 4, exact: (v ^ 0x80) is v + 128 as an unsigned byte; placing it in the
-// mantissa of 1024.0 (0x6400) gives 1024 + 128 + v, and subtracting 1152 leaves v.
-__device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  const uint32_t x = w ^ 0x80808080u;
-  const uint32_t a = __byte_perm(x, 0x64646464u, 0x4140);
-  const uint32_t b = __byte_perm(x, 0x64646464u, 0x4342);
-  const uint32_t bias = 0x64806480u;  // 1152.0 in both halves
-  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(lo) : "r"(a), "r"(bias));
-  asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(b), "r"(bias));
-}
-
 // ------------------------------------------------------------------ work list
 struct Tile {
   int e;

@@ -16,7 +16,6 @@
 
 namespace w8a8 {
 
-constexpr int kMaxVec = 8;  // 16-byte vectors cached per thread
 
 struct RowStats {
   float a, b;  // sym: a = absmax; asym: a = min, b = max
@@ -110,94 +109,147 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
 }
 
 // ---------------------------------------------------------------------------
-// Vector path: K % 8 == 0, ldx % 8 == 0, 16-byte aligned rows, K <= 8*kMaxVec*THREADS.
+// Vector path: K % 8 == 0, ldx % 8 == 0, 16-byte aligned rows, K <= 8*NV*THREADS.
 // MODE: w8a8_act_mode.  row_index: optional gather (MoE), sum_out: optional per-row sum
 // of q (weight azp_adj).
 // ---------------------------------------------------------------------------
-template <int MODE, int THREADS, bool F16>
+template <int MODE, int THREADS, int NV, bool F16, bool SUM>
 __global__ void __launch_bounds__(THREADS)
-quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
+quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int64_t ldx,
                const int64_t* __restrict__ row_index, int8_t* __restrict__ q, __half* __restrict__ q16,
                float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out,
                int32_t* __restrict__ norm_out) {
   __shared__ float sh[THREADS / 32];
   __shared__ int shi[THREADS / 32];
-  const int64_t row = blockIdx.x;
-  const int64_t src = row_index ? row_index[row] : row;
-  const uint4* xr = reinterpret_cast<const uint4*>(x + src * ldx);
   const int nvec = (int)(K / 8);
-  uint4 v[kMaxVec];
-  float r0 = (MODE == W8A8_ACT_DYN_TOKEN_ASYM) ? __int_as_float(0x7f800000) : 0.f;  // min or absmax
-  float r1 = __int_as_float(0xff800000);                                              // max
+  // Persistent: this CTA quantizes rows blockIdx.x, + gridDim.x, ...; the next row's loads
+  // are issued before the current row is processed so that HBM traffic overlaps the math.
+  uint4 nxt[NV];
+  int64_t row = blockIdx.x;
+  auto load_row = [&](int64_t r, uint4 (&dst)[NV]) {
+    const int64_t src = row_index ? row_index[r] : r;
+    const uint4* xr = reinterpret_cast<const uint4*>(x + src * ldx);
 #pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (idx < nvec) {
-      v[i] = ldg_stream(xr + idx);
-      if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
-        float f[8];
-        unpack8(v[i], f);
+    for (int i = 0; i < NV; ++i) {
+      const int idx = threadIdx.x + i * THREADS;
+      if (idx < nvec) dst[i] = ldg_stream(xr + idx);
+    }
+  };
+  if (row < rows) load_row(row, nxt);
+  for (; row < rows; row += gridDim.x) {
+    uint4 v[NV];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) {
-          if (MODE == W8A8_ACT_DYN_TOKEN_SYM) r0 = fmaxf(r0, fabsf(f[j]));
-          else { r0 = fminf(r0, f[j]); r1 = fmaxf(r1, f[j]); }
+    for (int i = 0; i < NV; ++i) v[i] = nxt[i];
+    if (row + gridDim.x < rows) load_row(row + gridDim.x, nxt);
+    // row statistics on packed bf16 pairs (max/min are exact): |x| max for the symmetric
+    // rule, min and max for the affine rule
+    __nv_bfloat162 m0 = __floats2bfloat162_rn(MODE == W8A8_ACT_DYN_TOKEN_ASYM ? __int_as_float(0x7f800000) : 0.f,
+                                              MODE == W8A8_ACT_DYN_TOKEN_ASYM ? __int_as_float(0x7f800000) : 0.f);
+    __nv_bfloat162 m1 = __floats2bfloat162_rn(__int_as_float(0xff800000), __int_as_float(0xff800000));
+    if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+#pragma unroll
+      for (int i = 0; i < NV; ++i) {
+        const int idx = threadIdx.x + i * THREADS;
+        if (idx < nvec) {
+          const uint32_t wd[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
+              const uint32_t a = wd[j] & 0x7FFF7FFFu;
+              m0 = __hmax2(m0, *reinterpret_cast<const __nv_bfloat162*>(&a));
+            } else {
+              m0 = __hmin2(m0, *reinterpret_cast<const __nv_bfloat162*>(&wd[j]));
+              m1 = __hmax2(m1, *reinterpret_cast<const __nv_bfloat162*>(&wd[j]));
+            }
+          }
         }
       }
     }
-  }
-  RowQuant rq;
-  if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
-    rq = row_quant_sym(block_reduce_max<THREADS>(r0, sh));
-  } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
-    const float lo = block_reduce_min<THREADS>(r0, sh);
-    const float hi = block_reduce_max<THREADS>(r1, sh);
-    rq = row_quant_asym(lo, hi);
-  } else {
-    rq.s = scale[0];
-    rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
-    rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
-  }
-  int qsum = 0, qabs = 0;
+    RowQuant rq;
+    if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
+      const float a = fmaxf(__low2float(m0), __high2float(m0));
+      rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
+    } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+      const float lo = block_reduce_min<THREADS>(fminf(__low2float(m0), __high2float(m0)), sh);
+      const float hi = block_reduce_max<THREADS>(fmaxf(__low2float(m1), __high2float(m1)), sh);
+      rq = row_quant_asym(lo, hi);
+    } else {
+      rq.s = scale[0];
+      rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
+      rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
+    }
+    const float r = __frcp_rn(rq.s);
+    const int qlo = rq.affine ? -128 : -127;
+    int qsum = 0, qabs = 0;
 #pragma unroll
-  for (int i = 0; i < kMaxVec; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (idx < nvec) {
-      float f[8];
-      unpack8(v[i], f);
-      int c[8];
+    for (int i = 0; i < NV; ++i) {
+      const int idx = threadIdx.x + i * THREADS;
+      if (idx < nvec) {
+        float f[8];
+        unpack8(v[i], f);
+        int c[8];
+        uint32_t w0, w1;
+        if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
+          // |x| <= absmax: codes never exceed +-127
+          uint32_t b[8];
+          quant_row_group_x2<8>(f, rq.s, r, b);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = apply_rq(rq, f[j]);
-        qsum += c[j];
-        qabs += abs(c[j]);
-      }
-      if (F16) {
-        uint4 o;
-        o.x = pack_f16x2(c[0], c[1]);
-        o.y = pack_f16x2(c[2], c[3]);
-        o.z = pack_f16x2(c[4], c[5]);
-        o.w = pack_f16x2(c[6], c[7]);
-        reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
-      } else {
-        uint2 o;
-        o.x = pack4_i8(c[0], c[1], c[2], c[3]);
-        o.y = pack4_i8(c[4], c[5], c[6], c[7]);
-        reinterpret_cast<uint2*>(q + row * K)[idx] = o;
+          for (int j = 0; j < 8; ++j) {
+            const int n = (int)(b[j] - 0x4B400000u);
+            if (SUM) qsum += n;
+            if (F16) qabs += abs(n);
+          }
+          w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
+          w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+        } else {
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            int n = rint_div_i(f[j], rq.s, r);
+            if (rq.affine) n += rq.zp;
+            n = min(127, max(qlo, n));
+            c[j] = n;
+            if (SUM) qsum += n;
+            if (F16) qabs += abs(n);
+          }
+          w0 = pack4_i8_prmt(c[0], c[1], c[2], c[3]);
+          w1 = pack4_i8_prmt(c[4], c[5], c[6], c[7]);
+        }
+        if (F16) {
+          uint4 o;
+          i8x4_to_f16x4(w0, o.x, o.y);
+          i8x4_to_f16x4(w1, o.z, o.w);
+          reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
+        } else {
+          reinterpret_cast<uint2*>(q + row * K)[idx] = make_uint2(w0, w1);
+        }
       }
     }
+    if (threadIdx.x == 0) {
+      if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
+      if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
+    }
+    if (SUM) {
+      const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
+      if (threadIdx.x == 0) sum_out[row] = tot;
+    }
+    if (F16) {
+      const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
+      if (threadIdx.x == 0) norm_out[row] = tot;
+    }
   }
-  if (threadIdx.x == 0) {
-    if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
-    if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
-  }
-  if (sum_out) {
-    const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
-    if (threadIdx.x == 0) sum_out[row] = tot;
-  }
-  if (F16) {
-    const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
-    if (threadIdx.x == 0) norm_out[row] = tot;
-  }
+}
+
+// Persistent grid for a row kernel: enough CTAs to fill every SM once, never more than rows.
+template <typename Kern>
+static unsigned persistent_grid(Kern kern, int threads, int64_t rows) {
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, threads, 0) != cudaSuccess || per_sm < 1)
+    per_sm = 1;
+  if (sms < 1) sms = 1;
+  const int64_t g = (int64_t)sms * per_sm;
+  return (unsigned)(rows < g ? rows : g);
 }
 
 // ---------------------------------------------------------------------------
@@ -256,6 +308,33 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
   }
 }
 
+template <int MODE, int THREADS, int NV, bool F16, bool SUM>
+static void launch_vec(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* row_index,
+                       int8_t* q, __half* q16, float* scale, int32_t* zp, int32_t* sum_out, int32_t* norm_out,
+                       cudaStream_t st) {
+  auto kern = quant_rows_vec<MODE, THREADS, NV, F16, SUM>;
+  static unsigned cached = 0;  // per instantiation: CTAs that fill the GPU once
+  if (cached == 0) cached = persistent_grid(kern, THREADS, (int64_t)1 << 40);
+  const unsigned grid = (unsigned)(rows < (int64_t)cached ? rows : (int64_t)cached);
+  kern<<<grid, THREADS, 0, st>>>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out);
+}
+
+template <int MODE, bool F16, bool SUM>
+static void launch_vec_k(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* row_index,
+                         int8_t* q, __half* q16, float* scale, int32_t* zp, int32_t* sum_out, int32_t* norm_out,
+                         cudaStream_t st) {
+  // about 16 values per thread; 256-thread CTAs keep registers low and occupancy high
+  const int64_t nvec = K / 8;
+  if (nvec <= 256 * 1)
+    launch_vec<MODE, 256, 1, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+  else if (nvec <= 256 * 2)
+    launch_vec<MODE, 256, 2, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+  else if (nvec <= 512 * 2)
+    launch_vec<MODE, 512, 2, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+  else
+    launch_vec<MODE, 512, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+}
+
 template <int MODE>
 static cudaError_t launch_quant_rows(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx,
                                      const int64_t* row_index, int8_t* q, __half* q16, float* scale,
@@ -264,20 +343,10 @@ static cudaError_t launch_quant_rows(const __nv_bfloat16* x, int64_t rows, int64
                        (q16 ? ((reinterpret_cast<uintptr_t>(q16) & 15) == 0)
                             : ((reinterpret_cast<uintptr_t>(q) & 7) == 0));
   const int64_t nvec = K / 8;
-  if (aligned && nvec <= (int64_t)kMaxVec * 128) {
-    if (q16)
-      quant_rows_vec<MODE, 128, true><<<(unsigned)rows, 128, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
-                                                                       sum_out, norm_out);
-    else
-      quant_rows_vec<MODE, 128, false><<<(unsigned)rows, 128, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
-                                                                        sum_out, norm_out);
-  } else if (aligned && nvec <= (int64_t)kMaxVec * 256) {
-    if (q16)
-      quant_rows_vec<MODE, 256, true><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
-                                                                       sum_out, norm_out);
-    else
-      quant_rows_vec<MODE, 256, false><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
-                                                                        sum_out, norm_out);
+  if (aligned && nvec <= 512 * 4) {
+    if (q16) launch_vec_k<MODE, true, false>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+    else if (sum_out) launch_vec_k<MODE, false, true>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+    else launch_vec_k<MODE, false, false>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
   } else {
     quant_rows_generic<MODE, 256><<<(unsigned)rows, 256, 0, st>>>(x, K, ldx, row_index, q, q16, scale, zp,
                                                                    sum_out, norm_out);
@@ -373,6 +442,7 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t I, int8_t* __
     }
   }
   const RowQuant rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
+  const float rcp = __frcp_rn(rq.s);
   int qabs = 0;
 #pragma unroll
   for (int i = 0; i < NV; ++i) {
@@ -381,7 +451,7 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t I, int8_t* __
       int c[8];
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
-        c[j] = quant_sym(g[i][j], rq.s);
+        c[j] = quant_row_sym(g[i][j], rq.s, rcp);
         qabs += abs(c[j]);
       }
       if (F16) {

@@ -1,0 +1,106 @@
+"""Run one kernel of the library repeatedly on a fixed, seeded case, for profilers.
+
+    python -m w8a8_int8_quantized_gb300.profile_cases CASE [--reps R]
+
+Cases (inputs drawn on the device with a seeded generator; nothing is checked here):
+  quant          w8a8_quantize_act, dynamic symmetric, M=8192, K=4096
+  quant_packed   w8a8_quantize_act_packed, dynamic symmetric, M=8192, K=4096
+  quant_asym     w8a8_quantize_act, dynamic asymmetric, M=8192, K=4096
+  wquant         w8a8_quantize_weight (+ azp_adj), N=28672, K=4096
+  requant        fp8block_to_int8_rowwise_batched over 8 x [6144, 4096]
+  gemm           w8a8_scaled_mm_packed, M=4096, N=28672, K=4096
+  gemm_o         w8a8_scaled_mm_packed, M=4096, N=4096, K=4096
+  small          w8a8_linear at M=16 (warp-MMA engine), N=28672, K=4096
+  moe            the MoE layer: 4096 tokens, 32 experts, top-4
+
+Every case uses a few GB of device memory at most, so a profiler capture of one launch
+stays small.
+"""
+
+import argparse
+import math
+
+import torch
+
+import w8a8_int8_quantized_gb300 as w8
+
+
+def _gen(seed):
+    return torch.Generator(device="cuda").manual_seed(seed)
+
+
+def _bf16(shape, std, seed):
+    return torch.randn(*shape, device="cuda", generator=_gen(seed)).mul_(std).to(torch.bfloat16)
+
+
+def case_fn(name):
+    dev = "cuda"
+    if name in ("quant", "quant_packed", "quant_asym"):
+        x = _bf16((8192, 4096), 1.0, 1)
+        if name == "quant":
+            return lambda: w8.quantize_act(x, "dyn_sym")
+        if name == "quant_asym":
+            return lambda: w8.quantize_act(x, "dyn_asym")
+        buf = torch.empty(w8.act_packed_size(8192, 4096), dtype=torch.uint8, device=dev)
+        return lambda: w8.quantize_act_packed(x, "dyn_sym", buf=buf)
+    if name == "wquant":
+        w = _bf16((28672, 4096), 0.02, 2)
+        return lambda: w8.quantize_weight(w, with_azp_adj=True)
+    if name == "requant":
+        g = _gen(3)
+        mats = []
+        for _ in range(8):
+            c = torch.randn(6144, 4096, device=dev, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
+            s = torch.exp(torch.empty(48, 32, device=dev).uniform_(math.log(1e-4), math.log(1e-2), generator=g))
+            mats.append((c, s))
+        outs = [(torch.empty(c.shape, dtype=torch.int8, device=dev), torch.empty(c.shape[0], device=dev))
+                for c, _ in mats]
+        return lambda: w8.fp8block_to_int8_rowwise_batched(mats, outs)
+    if name in ("gemm", "gemm_o"):
+        N = 28672 if name == "gemm" else 4096
+        x = _bf16((4096, 4096), 1.0, 4)
+        wq = torch.randint(-127, 128, (N, 4096), dtype=torch.int8, device=dev, generator=_gen(5))
+        sw = torch.rand(N, device=dev, generator=_gen(6)).mul_(1e-3)
+        pa = w8.quantize_act_packed(x)
+        y = torch.empty(4096, N, dtype=torch.bfloat16, device=dev)
+        return lambda: w8.scaled_mm_packed(pa, wq, sw, out=y)
+    if name == "small":
+        x = _bf16((16, 4096), 1.0, 7)
+        wq = torch.randint(-127, 128, (28672, 4096), dtype=torch.int8, device=dev, generator=_gen(8))
+        sw = torch.rand(28672, device=dev, generator=_gen(9)).mul_(1e-3)
+        ws = torch.empty(w8.linear_workspace_size(16, 4096), dtype=torch.uint8, device=dev)
+        y = torch.empty(16, 28672, dtype=torch.bfloat16, device=dev)
+        return lambda: w8.linear(x, wq, sw, workspace=ws, out=y)
+    if name == "moe":
+        T, H, E, k, inter = 4096, 4096, 32, 4, 1408
+        g = _gen(10)
+        ids = torch.stack([torch.randperm(E, device=dev, generator=g)[:k] for _ in range(T)]).reshape(-1)
+        order = torch.argsort(ids, stable=True)
+        seg = torch.zeros(E + 1, dtype=torch.int64, device=dev)
+        seg[1:] = torch.cumsum(torch.bincount(ids, minlength=E), 0)
+        row_of = torch.empty(T * k, dtype=torch.int64, device=dev)
+        row_of[order] = torch.arange(T * k, device=dev)
+        x = _bf16((T, H), 1.0, 11)
+        w13q, s13 = w8.quantize_weight(_bf16((E * 2 * inter, H), 0.02, 12))
+        w2q, s2 = w8.quantize_weight(_bf16((E * H, inter), 0.02, 13))
+        tw = torch.rand(T, k, device=dev, generator=g)
+        args = (x, order // k, seg, row_of.view(T, k), tw, w13q.view(E, 2 * inter, H), s13.view(E, 2 * inter),
+                w2q.view(E, H, inter), s2.view(E, H))
+        return lambda: w8.moe_forward(*args)
+    raise SystemExit(f"unknown case {name}")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("case")
+    ap.add_argument("--reps", type=int, default=5)
+    a = ap.parse_args()
+    fn = case_fn(a.case)
+    for _ in range(a.reps):
+        fn()
+    torch.cuda.synchronize()
+    print(f"{a.case}: ran {a.reps} times")
+
+
+if __name__ == "__main__":
+    main()
