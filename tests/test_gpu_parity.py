@@ -324,6 +324,35 @@ def test_fp8_requant_illegal_scale(bad_val):
     assert int(st.item()) == 4
 
 
+@pytest.mark.parametrize("N,K", [(9, 8192), (9, 20480), (5, 65536), (140, 4112)])
+def test_fp8_requant_long_rows(N, K):
+    """Row lengths that take the 8- and 4-warp shared-memory rings, the streaming kernel
+    (rows longer than a ring slot) and a partial last column block."""
+    codes, sinv, _ = wl.fp8_block_matrix(N, K, seed=5, stream=K, zero_frac=0.0)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, s = w8.fp8block_to_int8_rowwise(codes.to(DEV), sinv.to(DEV), status=st)
+    rq, rs, bad = oracle.fp8_block_to_int8_rowwise(codes.numpy(), sinv.numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    assert int(st.item()) == 0 and not bad.any()
+
+
+@pytest.mark.parametrize("K,col,code", [(4112, 4100, 0x7F), (4096, 0, 0xFF), (65536, 65535, 0xFF)])
+def test_fp8_requant_nan_code(K, col, code):
+    """An E4M3 NaN code (either sign) anywhere in a row, including a partial last block and
+    a streamed row, zeroes that row and reports a bad scale."""
+    codes, sinv, _ = wl.fp8_block_matrix(3, K, seed=6, stream=col, zero_frac=0.0)
+    c = codes.clone()
+    c[1, col] = code
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    q, s = w8.fp8block_to_int8_rowwise(c.to(DEV), sinv.to(DEV), status=st)
+    rq, rs, bad = oracle.fp8_block_to_int8_rowwise(c.numpy(), sinv.numpy())
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    assert bad[1] and not bad[0] and not bad[2]
+    assert int(st.item()) == 4
+
+
 def test_fp8_requant_batched_mixed():
     mats = [wl.fp8_block_matrix(*shape, seed=4, stream=i) for i, shape in
             enumerate([(512, 4096), (300, 1500), (64, 4096), (3000, 1500), (130, 4112)])]

@@ -4,10 +4,10 @@
 //   W[i,j] = W_fp8[i,j] * weight_scale_inv[i//128, j//128]   (the _inv scale multiplies)
 //   s[i]   = max_j |W[i,j]| / 127 ;  q = clamp(round(W / s), -127, 127) ;  zero row -> q=0, s=1.
 // Rows are independent (the README's tool also works matrix by matrix, row chunk by row
-// chunk), so one CTA owns one row: it reads the row's codes once with 16-byte loads,
-// decodes them once into registers, reduces the absmax across the CTA and writes q from
-// the cached values.  One launch covers a whole batch of matrices through a by-value
-// descriptor table; ragged or unaligned matrices take a warp-per-row byte-load path.
+// chunk), so one warp owns one row at a time.  Aligned rows (K % 16 == 0) are brought into
+// shared memory by one bulk copy each and read twice on chip (absmax, then quantize); the
+// others take a warp-per-row byte-load path.  One launch per path covers a whole batch of
+// matrices through a by-value descriptor table.
 #include "common.cuh"
 #include "internal.h"
 
@@ -25,98 +25,255 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
 __device__ __forceinline__ bool e4m3_is_nan(uint32_t c) { return (c & 0x7Fu) == 0x7Fu; }
 __device__ __forceinline__ bool scale_ok(float s) { return (s > 0.f) && (s <= 3.402823466e38f); }
 
-// Vector path (K % 16 == 0, 16-byte aligned rows, any length): one warp per row, many
-// warps per SM.  Pass 1 reads the row (16-byte groups) and finds its absmax; pass 2 reads it
-// again, from L1/L2, and quantizes it.
+// ---------------------------------------------------------------- vector path
+// Matrices with K % 16 == 0 and 16-byte aligned rows.  One warp per row; the row is read
+// twice on chip (pass 1: absmax, pass 2: quantize) but from HBM once.
 //
-// Row absmax without decoding every code: the codes of one 16-byte group share one block
-// scale sc > 0, E4M3 magnitude grows with the 7-bit code (exponent bits above mantissa
-// bits), and rounding is monotone, so max_j RN(|v_j| * sc) = RN(v(max_j code_j) * sc).
-// The largest 7-bit code of a group is a byte-wise max; 0x7F, the largest, is the NaN
-// code, so a group holds a NaN exactly when that max is 0x7F.
-constexpr int kReqWarpsPerCta = 8;
+// Decoding.  The hardware E4M3 -> fp16x2 conversion is exact (every E4M3 value is an fp16
+// value) and costs one instruction per two codes; fp16 -> fp32 is exact too.
+//
+// Pass 1, absmax without the block scale per code: the codes of one 128-column block share
+// one scale sc > 0, so max_j RN(|v_j| * sc) = RN(max_j |v_j| * sc) (rounding is monotone).
+// max_j |v_j| is taken on the fp16 values with the NaN-propagating absolute maximum, so an
+// E4M3 NaN code (S.1111.111) anywhere in the block leaves a NaN there.
+//
+// Pass 2, q = rint(RN(Wf / s)) with Wf = RN(v * sc), from one multiply per code: with
+// r = RN(1/s) and the block factor c = RN(sc * r), t = RN(v * c) differs from Wf / s by at
+// most |Wf / s| * 4.0001 * 2^-24 < 2^-15 (|Wf / s| <= 127 * (1 + 2^-24) because |Wf| is at
+// most the row absmax), and RN(Wf / s) differs from Wf / s by less than 2^-17.  So when t is
+// more than 2^-14 away from every half-integer, rint(t) = rint(RN(Wf / s)).  t + 1.5 * 2^23
+// rounds t to an integer (ties to even) and its low byte is the int8 code; the distance to
+// that integer is exact.  Groups with a value within 2^-14 of a tie (about 1 code in 8000),
+// and blocks whose scale or factor lies outside [2^-100, 2^100] (where the products above
+// could leave the normal range), are decided by the IEEE division itself.
 
-// value of a non-negative 7-bit E4M3 code times 2^-120, exactly (as a float32 bit pattern)
-__device__ __forceinline__ float e4m3_mag_scaled(uint32_t code7) { return __uint_as_float(code7 << 20); }
-
-// any byte of w equal to 0x7F or 0xFF (the E4M3 NaN codes)
-__device__ __forceinline__ bool has_nan_code(uint32_t w) {
-  return (((w & 0x7F7F7F7Fu) + 0x01010101u) & 0x80808080u) != 0u;
+// largest |value| of n16 groups of 16 codes as fp16 bits (> 0x7C00: a NaN code)
+__device__ __forceinline__ uint32_t habsmax_nan(uint32_t acc, uint32_t h) {
+  asm("max.NaN.xorsign.abs.f16x2 %0, %0, %1;" : "+r"(acc) : "r"(h));
+  return acc;
+}
+__device__ __forceinline__ void e4m3x4_to_f16x4(uint32_t w, uint32_t& h01, uint32_t& h23) {
+  asm("{ .reg .b16 lo, hi; mov.b32 {lo, hi}, %2; cvt.rn.f16x2.e4m3x2 %0, lo; cvt.rn.f16x2.e4m3x2 %1, hi; }"
+      : "=r"(h01), "=r"(h23)
+      : "r"(w));
+}
+__device__ __forceinline__ uint32_t group_absmax(uint32_t acc, const uint4& c) {
+  uint32_t h0, h1, h2, h3, h4, h5, h6, h7;
+  e4m3x4_to_f16x4(c.x, h0, h1);
+  e4m3x4_to_f16x4(c.y, h2, h3);
+  e4m3x4_to_f16x4(c.z, h4, h5);
+  e4m3x4_to_f16x4(c.w, h6, h7);
+  return habsmax_nan(habsmax_nan(habsmax_nan(habsmax_nan(acc, h0), h1), habsmax_nan(h2, h3)),
+                     habsmax_nan(habsmax_nan(h4, h5), habsmax_nan(h6, h7)));
+}
+// the block absmax times the block scale, RN(max|v| * sc); NaN codes and illegal scales flag bad
+__device__ __forceinline__ float block_amax(uint32_t acc, float sc, bool& bad) {
+  const uint32_t hm = max(acc & 0x7FFFu, (acc >> 16) & 0x7FFFu);  // non-negative fp16 bits order like values
+  bad |= (hm > 0x7C00u) || !scale_ok(sc);
+  return __fmul_rn(__half2float(__ushort_as_half((unsigned short)hm)), sc);
+}
+// block factor c = RN(sc * r), or -1 when the fast path's range conditions do not hold
+__device__ __forceinline__ float block_factor(float sc, float r) {
+  const float c = __fmul_rn(sc, r);
+  return (sc >= 0x1p-100f && c >= 0x1p-100f && c <= 0x1p100f) ? c : -1.f;
 }
 
-// The largest 7-bit code among 16 codes.
-__device__ __forceinline__ uint32_t max_code7(const uint4& c) {
-  uint32_t m = __vmaxu4(__vmaxu4(c.x & 0x7F7F7F7Fu, c.y & 0x7F7F7F7Fu), __vmaxu4(c.z & 0x7F7F7F7Fu, c.w & 0x7F7F7F7Fu));
-  m = __vmaxu4(m, m >> 16);
-  m = __vmaxu4(m, m >> 8);
-  return m & 0xFFu;
-}
-
-// 16 codes of one group -> 16 int8 codes: Wf = RN(value * sc) (as (value*2^-120)*(sc*2^120),
-// one rounding, or decoded exactly first when sc*2^120 would overflow), then q = rint(Wf/s)
-// by the rint_div_small rule (|Wf| <= absmax, so |Wf / s| stays within 128).
-__device__ __forceinline__ uint4 requant_group(const uint4& c, float sc, float s, float r) {
-  const bool fast = fabsf(sc) < 256.f;
-  const float sc2 = fast ? __fmul_rn(sc, 0x1p120f) : sc;
-  const uint32_t wd[4] = {c.x, c.y, c.z, c.w};
-  float wf[16];
+// 16 codes -> 16 int8 codes (see the note above); c < 0 takes the exact path for all 16.
+__device__ __forceinline__ uint4 requant_group(const uint4& cd, float c, const float* sc_ptr, float s) {
+  const uint32_t wd[4] = {cd.x, cd.y, cd.z, cd.w};
+  float f[16];
 #pragma unroll
-  for (int j = 0; j < 16; ++j) {
-    const uint32_t top = __byte_perm(wd[j >> 2], 0u, 0x0444u | (uint32_t)((j & 3) << 12));  // byte -> bits 31:24
-    float a = __uint_as_float((uint32_t)((int32_t)top >> 4) & 0x87F00000u);
-    if (!fast) a = __fmul_rn(a, 0x1p120f);
-    wf[j] = __fmul_rn(a, sc2);
+  for (int g = 0; g < 4; ++g) {
+    uint32_t h01, h23;
+    e4m3x4_to_f16x4(wd[g], h01, h23);
+    const __half2 a = *reinterpret_cast<const __half2*>(&h01), b = *reinterpret_cast<const __half2*>(&h23);
+    f[4 * g] = __low2float(a);
+    f[4 * g + 1] = __high2float(a);
+    f[4 * g + 2] = __low2float(b);
+    f[4 * g + 3] = __high2float(b);
   }
-  uint32_t b[16];
-  quant_row_group_x2<16>(wf, s, r, b);
+  const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
+  const uint64_t c2 = f2pack(c, c);
+  uint32_t bq[16];
+  float emax = 0.f;
+#pragma unroll
+  for (int j = 0; j < 16; j += 2) {
+    const uint64_t t = f2mul(f2pack(f[j], f[j + 1]), c2);
+    const uint64_t m = f2add(t, kMagic);
+    float e0, e1, m0, m1;
+    f2unpack(f2sub(t, f2sub(m, kMagic)), e0, e1);
+    f2unpack(m, m0, m1);
+    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+    bq[j] = __float_as_uint(m0);
+    bq[j + 1] = __float_as_uint(m1);
+  }
+  if (!(emax < 0.49993896484375f) || c < 0.f) {  // 0.5 - 2^-14
+    const float sc = *sc_ptr;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) {
+      const float t = __fmul_rn(f[j], c);
+      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f));
+      if (c < 0.f || !(fabsf(e) < 0.49993896484375f))
+        bq[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(__fmul_rn(f[j], sc), s)));
+    }
+  }
   uint32_t out[4];
 #pragma unroll
-  for (int g = 0; g < 4; ++g)
-    out[g] = __byte_perm(__byte_perm(b[4 * g], b[4 * g + 1], 0x0040), __byte_perm(b[4 * g + 2], b[4 * g + 3], 0x0040),
-                         0x5410);
+  for (int g = 0; g < 4; ++g) out[g] = pack4_i8_prmt(bq[4 * g], bq[4 * g + 1], bq[4 * g + 2], bq[4 * g + 3]);
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-__global__ void __launch_bounds__(kReqWarpsPerCta * 32)
-requant_warp_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
-  const int lane = threadIdx.x & 31;
-  const int64_t stride = (int64_t)gridDim.x * kReqWarpsPerCta;
-  for (int64_t grow = (int64_t)blockIdx.x * kReqWarpsPerCta + (threadIdx.x >> 5); grow < b.total_rows;
-       grow += stride) {
-    int lo = 0, hi = b.count - 1;
-    while (lo < hi) {
-      const int mid = (lo + hi + 1) >> 1;
-      if (b.m[mid].row0 <= grow) lo = mid; else hi = mid - 1;
+__device__ __forceinline__ const ReqMat& find_mat(const ReqBatch& b, int64_t grow) {
+  int lo = 0, hi = b.count - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (b.m[mid].row0 <= grow) lo = mid; else hi = mid - 1;
+  }
+  return b.m[lo];
+}
+
+// Pass 1 over a row held in shared memory: lane l owns the 128-column blocks l, l + 32, ...
+// A full block is read in a lane-rotated order so that the eight lanes of each quarter-warp
+// touch eight different 16-byte bank groups.
+__device__ __forceinline__ void row_absmax_smem(const uint4* rowv, const float* srow, int nv, int nbc, int lane,
+                                                float& amax, bool& bad) {
+  for (int b = lane; b < nbc; b += 32) {
+    const int n16 = min(8, nv - 8 * b);
+    uint32_t acc = 0u;
+    if (n16 == 8) {
+#pragma unroll
+      for (int j = 0; j < 8; ++j) acc = group_absmax(acc, rowv[8 * b + ((j + lane) & 7)]);
+    } else {
+      for (int j = 0; j < n16; ++j) acc = group_absmax(acc, rowv[8 * b + j]);
     }
-    const ReqMat& mt = b.m[lo];
+    amax = fmaxf(amax, block_amax(acc, srow[b], bad));
+  }
+}
+
+__device__ __forceinline__ float row_scale(float amax, bool& bad) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
+  bad = __any_sync(0xffffffffu, bad) || !(amax <= 3.402823466e38f);
+  return (!bad && amax != 0.f) ? __fdiv_rn(amax, 127.f) : 1.f;
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes) : "memory");
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(dst),
+               "l"(src), "r"(bytes), "r"(bar)
+               : "memory");
+}
+// waits for the phase with the given parity; false after 2 s
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+  uint64_t t0;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
+  for (;;) {
+    uint32_t ok;
+    asm volatile("{\n.reg .pred p;\nmbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\nselp.u32 %0, 1, 0, p;\n}\n"
+                 : "=r"(ok)
+                 : "r"(bar), "r"(parity)
+                 : "memory");
+    if (ok) return true;
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    if (t - t0 > 2000000000ull) return false;
+  }
+}
+
+// Row-ring kernel: every warp owns one shared-memory slot of `slot` bytes and walks the
+// batch's rows gw, gw + warps, ...; a row is brought in by one bulk copy (issued right after
+// the warp has finished the previous row), so many rows per SM are in flight while other
+// warps compute.  slot >= the largest K of the batch, a multiple of 128.
+template <int WARPS>
+__global__ void __launch_bounds__(WARPS * 32, 1024 / (WARPS * 32))
+requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  uint8_t* ring = smem + (size_t)warp * slot;
+  float* cb = reinterpret_cast<float*>(smem + (size_t)WARPS * slot) + (size_t)warp * (slot / 128);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(smem + (size_t)WARPS * slot + (size_t)WARPS * (slot / 128) * 4) + warp;
+  const uint32_t sbar = (uint32_t)__cvta_generic_to_shared(bar);
+  const uint32_t sring = (uint32_t)__cvta_generic_to_shared(ring);
+  const int64_t gw = (int64_t)blockIdx.x * WARPS + warp, tw = (int64_t)gridDim.x * WARPS;
+  if (gw >= b.total_rows) return;
+  if (lane == 0) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(sbar));
+    asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+    const ReqMat& m0 = find_mat(b, gw);
+    bulk_load(sring, m0.w + (gw - m0.row0) * (int64_t)m0.K, (uint32_t)m0.K, sbar);
+  }
+  __syncwarp();
+  uint32_t phase = 0;
+  for (int64_t grow = gw; grow < b.total_rows; grow += tw, phase ^= 1u) {
+    const ReqMat& mt = find_mat(b, grow);
     const int64_t i = grow - mt.row0;
-    const int K = mt.K;
-    const int nv = K / 16;
-    const int nbc = (K + 127) / 128;
-    const uint4* wr = reinterpret_cast<const uint4*>(mt.w + i * (int64_t)K);
+    const int K = mt.K, nv = K / 16, nbc = (K + 127) / 128;
+    if (!__all_sync(0xffffffffu, bar_wait(sbar, phase))) {
+      if (lane == 0) report_status(st, W8A8_ERR_TIMEOUT);
+      return;
+    }
+    const uint4* rowv = reinterpret_cast<const uint4*>(ring);
     const float* srow = mt.sinv + (i / 128) * nbc;
-    // pass 1: absmax from the per-group largest code (reads the row from HBM into L1)
     float amax = 0.f;
     bool bad = false;
-#pragma unroll 2
-    for (int idx = lane; idx < nv; idx += 32) {
-      const uint4 c = wr[idx];
-      const float sc = srow[idx >> 3];  // 16 codes per group, 8 groups per 128-column block
-      const uint32_t mc = max_code7(c);
-      bad |= (mc == 0x7Fu) || !scale_ok(sc);
-      amax = fmaxf(amax, __fmul_rn(__fmul_rn(__uint_as_float(mc << 20), 0x1p120f), sc));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, o));
-    bad = __any_sync(0xffffffffu, bad) || !(amax <= 3.402823466e38f);
-    float s = 1.f;
-    if (!bad && amax != 0.f) s = __fdiv_rn(amax, 127.f);
-    const float r = __frcp_rn(s);
-    // pass 2: decode, quantize, store (the row is read again, now from L1/L2)
+    row_absmax_smem(rowv, srow, nv, nbc, lane, amax, bad);
+    const float s = row_scale(amax, bad);
     uint4* qr = reinterpret_cast<uint4*>(mt.q + i * (int64_t)K);
+    if (!bad) {
+      const float r = __frcp_rn(s);
+      for (int bb = lane; bb < nbc; bb += 32) cb[bb] = block_factor(srow[bb], r);
+      __syncwarp();
 #pragma unroll 2
-    for (int idx = lane; idx < nv; idx += 32)
-      qr[idx] = bad ? make_uint4(0u, 0u, 0u, 0u) : requant_group(wr[idx], srow[idx >> 3], s, r);
+      for (int idx = lane; idx < nv; idx += 32)
+        qr[idx] = requant_group(rowv[idx], cb[idx >> 3], srow + (idx >> 3), s);
+    } else {
+      for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    if (lane == 0) {
+      mt.s[i] = s;
+      if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
+    }
+    __syncwarp();  // every lane is done with the slot (and with cb)
+    if (lane == 0 && grow + tw < b.total_rows) {
+      const ReqMat& mn = find_mat(b, grow + tw);
+      asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+      bulk_load(sring, mn.w + (grow + tw - mn.row0) * (int64_t)mn.K, (uint32_t)mn.K, sbar);
+    }
+  }
+}
+
+// Rows too long for a shared-memory slot: a warp streams its row from global memory twice
+// (the second pass mostly from L1/L2).
+constexpr int kReqStreamWarps = 8;
+__global__ void __launch_bounds__(kReqStreamWarps * 32)
+requant_stream_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tw = (int64_t)gridDim.x * kReqStreamWarps;
+  for (int64_t grow = (int64_t)blockIdx.x * kReqStreamWarps + (threadIdx.x >> 5); grow < b.total_rows; grow += tw) {
+    const ReqMat& mt = find_mat(b, grow);
+    const int64_t i = grow - mt.row0;
+    const int K = mt.K, nv = K / 16, nbc = (K + 127) / 128;
+    const uint4* wr = reinterpret_cast<const uint4*>(mt.w + i * (int64_t)K);
+    const float* srow = mt.sinv + (i / 128) * nbc;
+    float amax = 0.f;
+    bool bad = false;
+    for (int bb = lane; bb < nbc; bb += 32) {
+      const int n16 = min(8, nv - 8 * bb);
+      uint32_t acc = 0u;
+      for (int j = 0; j < n16; ++j) acc = group_absmax(acc, wr[8 * bb + j]);
+      amax = fmaxf(amax, block_amax(acc, srow[bb], bad));
+    }
+    const float s = row_scale(amax, bad);
+    uint4* qr = reinterpret_cast<uint4*>(mt.q + i * (int64_t)K);
+    if (!bad) {
+      const float r = __frcp_rn(s);
+#pragma unroll 2
+      for (int idx = lane; idx < nv; idx += 32)
+        qr[idx] = requant_group(wr[idx], block_factor(srow[idx >> 3], r), srow + (idx >> 3), s);
+    } else {
+      for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
+    }
     if (lane == 0) {
       mt.s[i] = s;
       if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
@@ -124,20 +281,64 @@ requant_warp_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
   }
 }
 
-static void launch_requant_warps(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
+// ring slot bytes for a largest row of kmax bytes; warps per CTA so that two CTAs fit an SM
+static int ring_slot(int64_t kmax) { return (int)((kmax + 127) / 128 * 128); }
+static size_t ring_smem(int warps, int slot) {
+  return (size_t)warps * slot + (size_t)warps * (slot / 128) * 4 + (size_t)warps * 8;
+}
+
+template <int WARPS>
+static cudaError_t launch_ring(const ReqBatch& b, int slot, int32_t* st, cudaStream_t stream) {
+  static int s_dev = -1, s_sms = 0;
+  static size_t s_attr = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const size_t smem = ring_smem(WARPS, slot);
+  if (s_dev != dev) {
+    e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    s_dev = dev;
+    s_attr = 0;
+  }
+  if (smem > s_attr) {
+    e = cudaFuncSetAttribute(requant_ring_kernel<WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    s_attr = smem;
+  }
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_ring_kernel<WARPS>, WARPS * 32, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int64_t need = (b.total_rows + WARPS - 1) / WARPS;
+  const int64_t cap = (int64_t)s_sms * per_sm;
+  requant_ring_kernel<WARPS><<<(unsigned)(need < cap ? need : cap), WARPS * 32, smem, stream>>>(b, slot, st);
+  return cudaGetLastError();
+}
+
+static cudaError_t launch_vec(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
+  int64_t kmax = 0;
+  for (int k = 0; k < b.count; ++k) kmax = b.m[k].K > kmax ? b.m[k].K : kmax;
+  const int slot = ring_slot(kmax);
+  // slots of 16 warps up to 112 KB per CTA, so that two CTAs share an SM
+  if (ring_smem(16, slot) <= (size_t)112 * 1024) return launch_ring<16>(b, slot, st, stream);
+  if (ring_smem(8, slot) <= (size_t)112 * 1024) return launch_ring<8>(b, slot, st, stream);
+  if (ring_smem(4, slot) <= (size_t)200 * 1024) return launch_ring<4>(b, slot, st, stream);
   static unsigned cached = 0;
   if (cached == 0) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_warp_kernel, kReqWarpsPerCta * 32, 0) !=
-            cudaSuccess || per_sm < 1)
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_stream_kernel, kReqStreamWarps * 32, 0) !=
+            cudaSuccess ||
+        per_sm < 1)
       per_sm = 1;
     cached = (unsigned)((sms < 1 ? 1 : sms) * per_sm);
   }
-  const int64_t need = (b.total_rows + kReqWarpsPerCta - 1) / kReqWarpsPerCta;
-  const unsigned grid = (unsigned)(need < (int64_t)cached ? need : (int64_t)cached);
-  requant_warp_kernel<<<grid, kReqWarpsPerCta * 32, 0, stream>>>(b, st);
+  const int64_t need = (b.total_rows + kReqStreamWarps - 1) / kReqStreamWarps;
+  requant_stream_kernel<<<(unsigned)(need < (int64_t)cached ? need : (int64_t)cached), kReqStreamWarps * 32, 0,
+                          stream>>>(b, st);
+  return cudaGetLastError();
 }
 
 // Any K and alignment: byte loads, two passes over the row.
@@ -204,8 +405,7 @@ cudaError_t requant_batch(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
     ++t.count;
   }
   if (vb.total_rows > 0) {
-    launch_requant_warps(vb, st, stream);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_vec(vb, st, stream);
     if (e != cudaSuccess) return e;
   }
   if (gb.total_rows > 0) {
