@@ -70,6 +70,34 @@ def test_quantize_act_dyn_asym(M, K):
     np.testing.assert_array_equal(zp.cpu().numpy(), rz)
 
 
+def _asym_stress_rows(K):
+    """bf16 rows that stress the affine rule's fast path: rows far from zero (|x/s| up to
+    about 2^16), constant rows, rows of two values, tiny magnitudes and rows of exact
+    multiples of a power of two (many exact ties)."""
+    g = torch.Generator().manual_seed(K)
+    rows = [
+        1000.0 + torch.randint(0, 8, (K,), generator=g).float() * 4.0,      # bf16 step 4 at 1000
+        -3.0e4 + torch.rand(K, generator=g) * 300.0,
+        torch.full((K,), -7.5),
+        torch.where(torch.rand(K, generator=g) < 0.5, torch.tensor(1.0), torch.tensor(3.0)),
+        torch.randn(K, generator=g) * 1e-30,
+        torch.randint(-64, 64, (K,), generator=g).float() * 0.125,
+        torch.randn(K, generator=g) * 5.0 + 40.0,
+        torch.linspace(-1.0, 1.0, K),
+    ]
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("K", [512, 4096, 1500])
+def test_quantize_act_dyn_asym_stress(K):
+    x = _asym_stress_rows(K)
+    q, s, zp = w8.quantize_act(x.to(DEV), "dyn_asym")
+    rq, rs, rz = oracle.quantize_act_dynamic_asymmetric(x.float().numpy())
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(zp.cpu().numpy(), rz)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+
+
 @pytest.mark.parametrize("M,K", [(16, 512), (128, 4096), (3, 1500)])
 def test_quantize_act_static(M, K):
     x = wl.asym_activations(M, K, seed=K + 1)

@@ -19,22 +19,6 @@ namespace w8a8 {
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-// rint(RN(x / s)) -- the IEEE float32 quotient rounded half to even -- without a division
-// in the common case.  r = RN(1/s) is computed once per row.  t = RN(x*r) differs from the
-// exact x/s by at most |x/s|*(2^-23 + 2^-48), and RN(x/s) by at most |x/s|*2^-24, so when t
-// is more than |t|*2^-20 away from every half-integer both lie strictly inside the same
-// interval between half-integers and round to the same integer.  Otherwise (rare: about
-// |t|*2^-19 of the values near each half-integer, and always for |t| >= 2^19, or a
-// non-finite t) the exact IEEE division decides.  Every subtraction below is exact, so the
-// test itself is exact.  Returns the integer as a float.
-__device__ __forceinline__ float rint_div(float x, float s, float r) {
-  const float t = __fmul_rn(x, r);
-  const float n = rintf(t);
-  const float d = fabsf(__fsub_rn(fabsf(__fsub_rn(t, n)), 0.5f));
-  if (d > __fmul_rn(fabsf(t), 0x1p-20f)) return n;
-  return rintf(__fdiv_rn(x, s));
-}
-
 // rint(x / s) clamped to [-127, 127]
 __device__ __forceinline__ int quant_sym(float x, float s) {
   int v = __float2int_rn(__fdiv_rn(x, s));
@@ -62,6 +46,27 @@ __device__ __forceinline__ int rint_div_i(float x, float s, float r) {
   if (d > __fmul_rn(fabsf(t), 0x1p-20f)) return __float_as_int(m) - 0x4B400000;
   const float e = rintf(__fdiv_rn(x, s));
   return __float2int_rn(fminf(fmaxf(e, -1073741824.0f), 1073741824.0f));
+}
+
+// rint(RN(x / s)) for a value whose approximate quotient t lies near the half-integer
+// h = k + 0.5, without a division in the common case.  The residual x - h*s is formed by one
+// fma, whose sign is exact.  RN(x / s) lands on h itself exactly when |x / s - h| <=
+// ulp(h)/2, i.e. |x - h*s| <= s*ulp(h)/2 =: tau (tau is s scaled by a power of two, so exact;
+// ties at ulp(h)/2 go to h because h = k + 0.5 has a zero last mantissa bit for |h| >= 1.5):
+// then the result is the even one of k, k + 1.  Otherwise RN(x / s) lies strictly on the
+// residual's side of h and less than 1/2 from it, so the result is k or k + 1 by that side.
+// The rounded residual decides both tests unless it equals tau; that case, |h| < 1.5 (where
+// the neighbours of h are not symmetric), and s outside [2^-100, 2^100] use the division.
+// Requires |t - x/s| < 2^-13 and |t| < 2^22.
+__device__ __forceinline__ float rint_quot_near_tie(float x, float s, float t) {
+  const float h = __fadd_rn(rintf(__fsub_rn(t, 0.5f)), 0.5f);
+  if (fabsf(h) >= 1.5f && s >= 0x1p-100f && s <= 0x1p100f) {
+    const float rho = fabsf(__fmaf_rn(-h, s, x));
+    const float tau = __fmul_rn(__fmul_rn(s, __uint_as_float(__float_as_uint(h) & 0x7F800000u)), 0x1p-24f);
+    if (rho < tau) return rintf(h);
+    if (rho > tau) return __fmaf_rn(-h, s, x) > 0.f ? __fadd_rn(h, 0.5f) : __fsub_rn(h, 0.5f);
+  }
+  return rintf(__fdiv_rn(x, s));
 }
 
 // rint_div_i for quotients known to satisfy |x/s| <= 256 (a row divided by its own
@@ -101,78 +106,88 @@ __device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
   return r;
 }
 
-// Two values of a row quantized with the row's own absmax scale (|x / s| <= 256), the
-// rint_div_small rule applied to both lanes of a pair at once.  On return w0 / w1 hold
-// 0x4B400000 + q (the float bits of q + 1.5*2^23), so their low bytes are the int8 codes,
-// and n holds q0, q1 as exact floats.
-__device__ __forceinline__ void quant_pair_row(float x0, float x1, float s, float r, uint64_t r2,
-                                               uint32_t& w0, uint32_t& w1, uint64_t& n) {
-  const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
-  const uint64_t t = f2mul(f2pack(x0, x1), r2);
-  const uint64_t m = f2add(t, kMagic);
-  n = f2sub(m, kMagic);
-  float e0, e1, m0, m1;
-  f2unpack(f2sub(t, n), e0, e1);
-  f2unpack(m, m0, m1);
-  w0 = __float_as_uint(m0);
-  w1 = __float_as_uint(m1);
-  if (!(fmaxf(fabsf(e0), fabsf(e1)) < 0.499755859375f)) {  // 0.5 - 2^-12: decide by division
-    const float n0 = rintf(__fdiv_rn(x0, s)), n1 = rintf(__fdiv_rn(x1, s));
-    w0 = 0x4B400000u + (uint32_t)__float2int_rn(n0);
-    w1 = 0x4B400000u + (uint32_t)__float2int_rn(n1);
-    n = f2pack(n0, n1);
-  }
-}
-
-// N values of a row quantized with the row's own absmax scale (|x / s| <= 256): the
-// rint_div_small rule for a whole group, with the rare exact-division fallback hoisted out
-// of the common path.  On return b[j] = 0x4B400000 + q_j (its low byte is the int8 code).
-template <int N>
-__device__ __forceinline__ void quant_row_group(const float* x, float s, float r, uint32_t* b) {
-  float emax = 0.f;
-#pragma unroll
-  for (int j = 0; j < N; ++j) {
-    const float t = __fmul_rn(x[j], r);
-    const float m = __fadd_rn(t, 12582912.0f);
-    const float e = __fsub_rn(t, __fsub_rn(m, 12582912.0f));
-    emax = fmaxf(emax, fabsf(e));
-    b[j] = __float_as_uint(m);
-  }
-  if (!(emax < 0.499755859375f)) {  // some value lies within 2^-12 of a tie: decide those exactly
-#pragma unroll
-    for (int j = 0; j < N; ++j) {
-      const float t = __fmul_rn(x[j], r);
-      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f));
-      if (!(fabsf(e) < 0.499755859375f)) b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(x[j], s)));
-    }
-  }
-}
-
 // quant_row_group on packed float32 pairs (N even): half the float instructions.
 template <int N>
 __device__ __forceinline__ void quant_row_group_x2(const float* x, float s, float r, uint32_t* b) {
+  // |x / s| <= 128 here, so t = RN(x * r) is within 2^-16 of x / s and RN(x / s) within 2^-17:
+  // a t more than 2^-14 from every half-integer rounds like the IEEE quotient
   const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
   const uint64_t r2 = f2pack(r, r);
   float emax = 0.f;
+  float e[N];
 #pragma unroll
   for (int j = 0; j < N; j += 2) {
     const uint64_t t = f2mul(f2pack(x[j], x[j + 1]), r2);
     const uint64_t m = f2add(t, kMagic);
-    float e0, e1, m0, m1;
-    f2unpack(f2sub(t, f2sub(m, kMagic)), e0, e1);
+    float m0, m1;
+    f2unpack(f2sub(t, f2sub(m, kMagic)), e[j], e[j + 1]);
     f2unpack(m, m0, m1);
-    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+    emax = fmaxf(emax, fmaxf(fabsf(e[j]), fabsf(e[j + 1])));
     b[j] = __float_as_uint(m0);
     b[j + 1] = __float_as_uint(m1);
   }
-  if (!(emax < 0.499755859375f)) {  // some value lies within 2^-12 of a tie: decide those exactly
+  if (!(emax < 0.49993896484375f)) {  // 0.5 - 2^-14: decide the values near a tie exactly
+#pragma unroll
+    for (int j = 0; j < N; ++j)
+      if (!(fabsf(e[j]) < 0.49993896484375f))
+        b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rint_quot_near_tie(x[j], s, __fmul_rn(x[j], r)));
+  }
+}
+
+// four int32 values saturated to [-128, 127] and packed into one word, byte 0 = a
+__device__ __forceinline__ uint32_t pack4_i8_sat(int a, int b, int c, int d) {
+  uint32_t hi, w;
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, 0;" : "=r"(hi) : "r"(d), "r"(c));
+  asm("cvt.pack.sat.s8.s32.b32 %0, %1, %2, %3;" : "=r"(w) : "r"(b), "r"(a), "r"(hi));
+  return w;
+}
+
+// Per-byte +1 / -1 for the signs of four int8 values (prmt with sign replication gives
+// 0xFF for a negative byte, 0x00 otherwise; or-ing 0x01 makes those -1 and +1).
+__device__ __forceinline__ int sign_bytes(uint32_t w) {
+  uint32_t s;
+  asm("prmt.b32 %0, %1, 0, 0xBA98;" : "=r"(s) : "r"(w));
+  return (int)(s | 0x01010101u);
+}
+// sum and sum of absolute values of the four int8 values of w, added to acc
+__device__ __forceinline__ int sum4_i8(uint32_t w, int acc) { return __dp4a((int)w, 0x01010101, acc); }
+__device__ __forceinline__ int abssum4_i8(uint32_t w, int acc) { return __dp4a((int)w, sign_bytes(w), acc); }
+
+// N values (N % 4 == 0) of a row under the affine rule q = clamp(rint(x / s) + zp, -128, 127),
+// written as N/4 packed words.  t = RN(x * r) with r = RN(1/s) and the zero point folded into
+// the rounding constant (1.5*2^23 + zp, exact for |zp| < 2^22): the low mantissa bits of
+// t + 1.5*2^23 + zp are rint(t) + zp.  thr = 0.5 - (margin of the row): a value whose t lies
+// at least that far inside an integer interval rounds as the IEEE quotient does; the others
+// (and every value when thr <= 0) are decided by the division.
+template <int N>
+__device__ __forceinline__ void quant_row_group_affine_x2(const float* x, float s, float r, int zp, float thr,
+                                                          uint32_t* out) {
+  const float mg = __fadd_rn(12582912.0f, (float)zp);
+  const uint64_t mg2 = f2pack(mg, mg);
+  const uint64_t r2 = f2pack(r, r);
+  float emax = 0.f;
+  int qv[N];
+#pragma unroll
+  for (int j = 0; j < N; j += 2) {
+    const uint64_t t = f2mul(f2pack(x[j], x[j + 1]), r2);
+    const uint64_t m = f2add(t, mg2);
+    float e0, e1, m0, m1;
+    f2unpack(f2sub(t, f2sub(m, mg2)), e0, e1);
+    f2unpack(m, m0, m1);
+    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+    qv[j] = __float_as_int(m0) - 0x4B400000;
+    qv[j + 1] = __float_as_int(m1) - 0x4B400000;
+  }
+  if (!(emax < thr)) {
 #pragma unroll
     for (int j = 0; j < N; ++j) {
       const float t = __fmul_rn(x[j], r);
-      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f));
-      if (!(fabsf(e) < 0.499755859375f)) b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(x[j], s)));
+      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, mg), mg));
+      if (!(fabsf(e) < thr)) qv[j] = quant_asym(x[j], s, zp);
     }
   }
+#pragma unroll
+  for (int g = 0; g < N / 4; ++g) out[g] = pack4_i8_sat(qv[4 * g], qv[4 * g + 1], qv[4 * g + 2], qv[4 * g + 3]);
 }
 
 // four int8 values (low bytes of a, b, c, d) packed into one word, byte 0 = a
@@ -193,19 +208,8 @@ __device__ __forceinline__ void i8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
   asm("sub.rn.f16x2 %0, %1, %2;\n" : "=r"(hi) : "r"(b), "r"(bias));
 }
 
-// Symmetric and affine quantization from a precomputed reciprocal (same results as
-// quant_sym / quant_asym).
-__device__ __forceinline__ int quant_sym_r(float x, float s, float r) {
-  return min(127, max(-127, rint_div_i(x, s, r)));
-}
 // a value of a row quantized with that row's own absmax scale: |x / s| <= 127 (+ rounding)
 __device__ __forceinline__ int quant_row_sym(float x, float s, float r) { return rint_div_small(x, s, r); }
-__device__ __forceinline__ int quant_asym_r(float x, float s, float r, int zp) {
-  // |rint| + |zp| stays far below 2^24 whenever the result is not clamped, so the float sum
-  // is exact there; larger magnitudes clamp either way
-  const float v = __fadd_rn(rint_div(x, s, r), (float)zp);
-  return __float2int_rn(fminf(fmaxf(v, -128.f), 127.f));
-}
 
 __device__ __forceinline__ uint32_t pack4_i8(int a, int b, int c, int d) {
   return (uint32_t)(a & 0xFF) | ((uint32_t)(b & 0xFF) << 8) | ((uint32_t)(c & 0xFF) << 16) |
@@ -219,10 +223,6 @@ __device__ __forceinline__ uint32_t pack_f16x2(int lo, int hi) {
 }
 
 // two small integral floats (exact in fp16) packed as fp16x2
-__device__ __forceinline__ uint32_t pack_f16x2_f(float lo, float hi) {
-  __half2 v = __floats2half2_rn(lo, hi);
-  return *reinterpret_cast<uint32_t*>(&v);
-}
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

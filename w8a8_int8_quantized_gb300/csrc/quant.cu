@@ -119,13 +119,20 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
                const int64_t* __restrict__ row_index, int8_t* __restrict__ q, __half* __restrict__ q16,
                float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out,
                int32_t* __restrict__ norm_out) {
-  __shared__ float sh[THREADS / 32];
-  __shared__ int shi[THREADS / 32];
+  constexpr int W = THREADS / 32;
+  constexpr bool DYN = (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM);
+  // One CTA barrier per row: per-warp partials go to a double-buffered shared array, so a
+  // warp may start writing row k+1's partials while slower warps still read row k's; the
+  // row sums of row k (SUM / F16) are completed behind row k+1's barrier.
+  __shared__ float sh_lo[2][W], sh_hi[2][W];
+  __shared__ int sh_sum[2][W], sh_abs[2][W];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = (int)(K / 8);
   // Persistent: this CTA quantizes rows blockIdx.x, + gridDim.x, ...; the next row's loads
   // are issued before the current row is processed so that HBM traffic overlaps the math.
   uint4 nxt[NV];
-  int64_t row = blockIdx.x;
+  int64_t row = blockIdx.x, prev = -1;
+  int buf = 0;
   auto load_row = [&](int64_t r, uint4 (&dst)[NV]) {
     const int64_t src = row_index ? row_index[r] : r;
     const uint4* xr = reinterpret_cast<const uint4*>(x + src * ldx);
@@ -135,18 +142,28 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       if (idx < nvec) dst[i] = ldg_stream(xr + idx);
     }
   };
+  auto finish_sums = [&](int b, int64_t r) {
+    int s = 0, a = 0;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      if (SUM) s += sh_sum[b][i];
+      if (F16) a += sh_abs[b][i];
+    }
+    if (SUM) sum_out[r] = s;
+    if (F16) norm_out[r] = a;
+  };
   if (row < rows) load_row(row, nxt);
-  for (; row < rows; row += gridDim.x) {
+  for (; row < rows; row += gridDim.x, buf ^= 1) {
     uint4 v[NV];
 #pragma unroll
     for (int i = 0; i < NV; ++i) v[i] = nxt[i];
     if (row + gridDim.x < rows) load_row(row + gridDim.x, nxt);
     // row statistics on packed bf16 pairs (max/min are exact): |x| max for the symmetric
     // rule, min and max for the affine rule
-    __nv_bfloat162 m0 = __floats2bfloat162_rn(MODE == W8A8_ACT_DYN_TOKEN_ASYM ? __int_as_float(0x7f800000) : 0.f,
-                                              MODE == W8A8_ACT_DYN_TOKEN_ASYM ? __int_as_float(0x7f800000) : 0.f);
-    __nv_bfloat162 m1 = __floats2bfloat162_rn(__int_as_float(0xff800000), __int_as_float(0xff800000));
-    if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+    if (DYN) {
+      __nv_bfloat162 m0 = __floats2bfloat162_rn(MODE == W8A8_ACT_DYN_TOKEN_ASYM ? __int_as_float(0x7f800000) : 0.f,
+                                                MODE == W8A8_ACT_DYN_TOKEN_ASYM ? __int_as_float(0x7f800000) : 0.f);
+      __nv_bfloat162 m1 = __floats2bfloat162_rn(__int_as_float(0xff800000), __int_as_float(0xff800000));
 #pragma unroll
       for (int i = 0; i < NV; ++i) {
         const int idx = threadIdx.x + i * THREADS;
@@ -164,15 +181,41 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
           }
         }
       }
+      float lo = MODE == W8A8_ACT_DYN_TOKEN_SYM ? fmaxf(__low2float(m0), __high2float(m0))
+                                                : fminf(__low2float(m0), __high2float(m0));
+      float hi = fmaxf(__low2float(m1), __high2float(m1));
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
+          lo = fmaxf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        } else {
+          lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+          hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+        }
+      }
+      if (lane == 0) {
+        sh_lo[buf][warp] = lo;
+        sh_hi[buf][warp] = hi;
+      }
     }
+    __syncthreads();
+    if ((SUM || F16) && threadIdx.x == 0 && prev >= 0) finish_sums(buf ^ 1, prev);
     RowQuant rq;
+    float rq_lo = 0.f, rq_hi = 0.f;
     if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
-      const float a = fmaxf(__low2float(m0), __high2float(m0));
-      rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
+      float a = sh_lo[buf][0];
+#pragma unroll
+      for (int i = 1; i < W; ++i) a = fmaxf(a, sh_lo[buf][i]);
+      rq = row_quant_sym(a);
     } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
-      const float lo = block_reduce_min<THREADS>(fminf(__low2float(m0), __high2float(m0)), sh);
-      const float hi = block_reduce_max<THREADS>(fmaxf(__low2float(m1), __high2float(m1)), sh);
-      rq = row_quant_asym(lo, hi);
+      rq_lo = sh_lo[buf][0];
+      rq_hi = sh_hi[buf][0];
+#pragma unroll
+      for (int i = 1; i < W; ++i) {
+        rq_lo = fminf(rq_lo, sh_lo[buf][i]);
+        rq_hi = fmaxf(rq_hi, sh_hi[buf][i]);
+      }
+      rq = row_quant_asym(rq_lo, rq_hi);
     } else {
       rq.s = scale[0];
       rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
@@ -180,6 +223,14 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
     }
     const float r = __frcp_rn(rq.s);
     const int qlo = rq.affine ? -128 : -127;
+    // dynamic affine rows: the margin of the packed fast path grows with max|x / s| (t = x * r
+    // is within 3 * 2^-24 * |x / s| of the IEEE quotient; 2^-21 leaves room for tmax's own
+    // rounding).  For bf16 rows |x / s| < 2^17; beyond 2^20 thr <= 0 and every value divides.
+    float thr = 0.f;
+    if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+      const float tmax = __fmul_rn(fmaxf(fabsf(rq_lo), fabsf(rq_hi)), r);
+      thr = __fsub_rd(0.5f, __fmul_rn(tmax, 0x1p-21f));
+    }
     int qsum = 0, qabs = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
@@ -187,33 +238,33 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       if (idx < nvec) {
         float f[8];
         unpack8(v[i], f);
-        int c[8];
         uint32_t w0, w1;
         if (MODE == W8A8_ACT_DYN_TOKEN_SYM) {
           // |x| <= absmax: codes never exceed +-127
           uint32_t b[8];
           quant_row_group_x2<8>(f, rq.s, r, b);
-#pragma unroll
-          for (int j = 0; j < 8; ++j) {
-            const int n = (int)(b[j] - 0x4B400000u);
-            if (SUM) qsum += n;
-            if (F16) qabs += abs(n);
-          }
-          w0 = __byte_perm(__byte_perm(b[0], b[1], 0x0040), __byte_perm(b[2], b[3], 0x0040), 0x5410);
-          w1 = __byte_perm(__byte_perm(b[4], b[5], 0x0040), __byte_perm(b[6], b[7], 0x0040), 0x5410);
+          w0 = pack4_i8_prmt(b[0], b[1], b[2], b[3]);
+          w1 = pack4_i8_prmt(b[4], b[5], b[6], b[7]);
+        } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+          // |x / s| <= 127 in a degenerate (symmetric-rule) row, so the [-128, 127] saturation
+          // of the packing never differs from the symmetric clamp there
+          uint32_t o2[2];
+          quant_row_group_affine_x2<8>(f, rq.s, r, rq.zp, thr, o2);
+          w0 = o2[0];
+          w1 = o2[1];
         } else {
+          int c[8];
 #pragma unroll
           for (int j = 0; j < 8; ++j) {
             int n = rint_div_i(f[j], rq.s, r);
             if (rq.affine) n += rq.zp;
-            n = min(127, max(qlo, n));
-            c[j] = n;
-            if (SUM) qsum += n;
-            if (F16) qabs += abs(n);
+            c[j] = min(127, max(qlo, n));
           }
           w0 = pack4_i8_prmt(c[0], c[1], c[2], c[3]);
           w1 = pack4_i8_prmt(c[4], c[5], c[6], c[7]);
         }
+        if (SUM) qsum = sum4_i8(w1, sum4_i8(w0, qsum));
+        if (F16) qabs = abssum4_i8(w1, abssum4_i8(w0, qabs));
         if (F16) {
           uint4 o;
           i8x4_to_f16x4(w0, o.x, o.y);
@@ -225,17 +276,25 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       }
     }
     if (threadIdx.x == 0) {
-      if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
+      if (DYN) scale[row] = rq.s;
       if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
     }
-    if (SUM) {
-      const int tot = block_reduce_sum_i<THREADS>(qsum, shi);
-      if (threadIdx.x == 0) sum_out[row] = tot;
+    if (SUM || F16) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        if (SUM) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
+        if (F16) qabs += __shfl_xor_sync(0xffffffffu, qabs, o);
+      }
+      if (lane == 0) {
+        sh_sum[buf][warp] = qsum;
+        sh_abs[buf][warp] = qabs;
+      }
+      prev = row;
     }
-    if (F16) {
-      const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
-      if (threadIdx.x == 0) norm_out[row] = tot;
-    }
+  }
+  if (SUM || F16) {
+    __syncthreads();
+    if (threadIdx.x == 0 && prev >= 0) finish_sums(buf ^ 1, prev);
   }
 }
 
@@ -323,14 +382,15 @@ template <int MODE, bool F16, bool SUM>
 static void launch_vec_k(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* row_index,
                          int8_t* q, __half* q16, float* scale, int32_t* zp, int32_t* sum_out, int32_t* norm_out,
                          cudaStream_t st) {
-  // about 16 values per thread; 256-thread CTAs keep registers low and occupancy high
+  // Rows are latency-bound at these sizes (one CTA-wide reduction per row), so short rows get
+  // small CTAs and many rows in flight per SM; about 16-32 values per thread.
   const int64_t nvec = K / 8;
-  if (nvec <= 256 * 1)
-    launch_vec<MODE, 256, 1, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
-  else if (nvec <= 256 * 2)
-    launch_vec<MODE, 256, 2, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
-  else if (nvec <= 512 * 2)
-    launch_vec<MODE, 512, 2, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+  if (nvec <= 128 * 2)
+    launch_vec<MODE, 128, 2, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+  else if (nvec <= 128 * 4)
+    launch_vec<MODE, 128, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+  else if (nvec <= 256 * 4)
+    launch_vec<MODE, 256, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
   else
     launch_vec<MODE, 512, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
 }
