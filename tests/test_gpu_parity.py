@@ -88,6 +88,49 @@ def _asym_stress_rows(K):
     return torch.stack(rows).to(torch.bfloat16)
 
 
+def _sym_tie_rows(K):
+    """bf16 rows whose quotients x/s sit on or next to half-integers: s = 1 and s = 2 with
+    x = (k + 1/2) s (exact ties), absmax 100 (s not a power of two) with x the bf16 values
+    nearest (k + 1/2) s and their neighbours, and values around +-s/2 and +-3s/2."""
+    g = torch.Generator().manual_seed(K)
+    k = torch.randint(-127, 127, (K,), generator=g).float()
+    rows = []
+    r = k + 0.5
+    r[0] = 127.0
+    rows.append(r)                                   # s = 1: every value an exact tie
+    r = 2.0 * k + 1.0
+    r[0] = 254.0
+    rows.append(r)                                   # s = 2
+    s100 = np.float32(100.0) / np.float32(127.0)
+    base = torch.from_numpy(((k.numpy() + 0.5) * s100).astype(np.float32))
+    b16 = base.to(torch.bfloat16).float()
+    step = torch.randint(-2, 3, (K,), generator=g).float()
+    near = (b16.view(torch.int32) + (step.to(torch.int32) << 16)).view(torch.float32)
+    near[0] = 100.0
+    rows.append(near)                                # near-ties, s = RN(100/127)
+    small = torch.tensor([0.5, -0.5, 1.5, -1.5, 0.49, 0.51, 1.49, 1.51], dtype=torch.float32)
+    r = small[torch.randint(0, 8, (K,), generator=g)] * s100
+    r[0] = 100.0
+    rows.append(r)                                   # |h| < 1.5 and its edges
+    return torch.stack(rows).to(torch.bfloat16)
+
+
+@pytest.mark.parametrize("K", [512, 4096])
+def test_quantize_sym_near_ties(K):
+    """The exact near-tie decision (residual sign and size against s*ulp(h)/2) against the
+    oracle's IEEE division, through the activation and the weight quantizers."""
+    x = _sym_tie_rows(K)
+    rq, rs = oracle.quantize_act_dynamic_symmetric(x.float().numpy())
+    q, s, _ = w8.quantize_act(x.to(DEV), "dyn_sym")
+    np.testing.assert_array_equal(s.cpu().numpy(), rs)
+    np.testing.assert_array_equal(q.cpu().numpy(), rq)
+    wq, sw, adj = w8.quantize_weight(x.to(DEV), with_azp_adj=True)
+    wr, wsr = oracle.quantize_weight_per_channel(x.float().numpy())
+    np.testing.assert_array_equal(sw.cpu().numpy(), wsr)
+    np.testing.assert_array_equal(wq.cpu().numpy(), wr)
+    np.testing.assert_array_equal(adj.cpu().numpy(), wr.astype(np.int64).sum(1))
+
+
 @pytest.mark.parametrize("K", [512, 4096, 1500])
 def test_quantize_act_dyn_asym_stress(K):
     x = _asym_stress_rows(K)
