@@ -8,8 +8,11 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
   quant_asym     w8a8_quantize_act, dynamic asymmetric, M=8192, K=4096
   wquant         w8a8_quantize_weight (+ azp_adj), N=28672, K=4096
   requant        fp8block_to_int8_rowwise_batched over 8 x [6144, 4096]
-  gemm           w8a8_scaled_mm_packed, M=4096, N=28672, K=4096
-  gemm_o         w8a8_scaled_mm_packed, M=4096, N=4096, K=4096
+  gemm           w8a8_scaled_mm_packed, M=4096, N=28672, K=4096 (Llama-like activations, as the
+                 bench: 1% outlier channels, so every tile runs the single fp32 pass)
+  gemm_o         the same with N=4096
+  gemm_chunked   M=4096, N=28672, K=4096 with N(0,1) activations: many rows' L1 norms exceed
+                 2^17, so their tiles run the 1024-K chunked mode
   small          w8a8_linear at M=16 (warp-MMA engine), N=28672, K=4096
   moe            the MoE layer: 4096 tokens, 32 experts, top-4
 
@@ -23,6 +26,7 @@ import math
 import torch
 
 import w8a8_int8_quantized_gb300 as w8
+from w8a8_int8_quantized_gb300 import workloads as wl
 
 
 def _gen(seed):
@@ -56,9 +60,9 @@ def case_fn(name):
         outs = [(torch.empty(c.shape, dtype=torch.int8, device=dev), torch.empty(c.shape[0], device=dev))
                 for c, _ in mats]
         return lambda: w8.fp8block_to_int8_rowwise_batched(mats, outs)
-    if name in ("gemm", "gemm_o"):
-        N = 28672 if name == "gemm" else 4096
-        x = _bf16((4096, 4096), 1.0, 4)
+    if name in ("gemm", "gemm_o", "gemm_chunked"):
+        N = 4096 if name == "gemm_o" else 28672
+        x = _bf16((4096, 4096), 1.0, 4) if name == "gemm_chunked" else wl.llama_activations(4096, 4096, seed=4).to(dev)
         wq = torch.randint(-127, 128, (N, 4096), dtype=torch.int8, device=dev, generator=_gen(5))
         sw = torch.rand(N, device=dev, generator=_gen(6)).mul_(1e-3)
         pa = w8.quantize_act_packed(x)
