@@ -32,6 +32,30 @@ M_TOKENS = 4096
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
 
+def gemm_traffic():
+    """DRAM bytes per GEMM launch from the committed ncu summary, if it was taken with the
+    kernel source as it is now (else None: the counters are stale)."""
+    import hashlib
+    prof = os.path.join(HERE, "profiles", "gemm_tc_kernel_llama3_8b_m4096.md")
+    src = os.path.join(HERE, "w8a8_int8_quantized_gb300", "csrc", "gemm_tc.cu")
+    if not (os.path.exists(prof) and os.path.exists(src)):
+        return None
+    text = open(prof).read()
+    sha, per = None, {}
+    for line in text.splitlines():
+        line = line.strip()
+        if line.startswith("source_sha256:"):
+            sha = line.split(":", 1)[1].strip()
+        elif line.startswith("traffic_bytes_per_launch:"):
+            for kv in line.split(":", 1)[1].split():
+                k, v = kv.split("=")
+                per[k] = int(v)
+    with open(src, "rb") as f:
+        if sha is None or hashlib.sha256(f.read()).hexdigest() != sha or not per:
+            return None
+    return per
+
+
 def load_peaks():
     p = os.path.join(HERE, "MEASURED_PEAKS.json")
     if os.path.exists(p):
@@ -232,10 +256,15 @@ def run_ours(args, world, rank, pg):
         }
     achieved = gemm_flops / (gemm_ms * 1e-3) / 1e12
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    tr = gemm_traffic()
     roofline = {
         "bound": "tensor", "kernel": "gemm_tc_kernel (tcgen05 kind::f16, int8 operands exact in fp16)",
         "achieved": round(achieved, 1), "peak": peak, "unit": "TFLOP/s", "frac": round(achieved / peak, 4),
-        "traffic": None,
+        # mean DRAM bytes per GEMM launch over the four layer launches of a step (ncu, committed
+        # under profiles/), null when the kernel source changed since the capture
+        "traffic": (round(sum(tr[L["name"]] for L in layers) / len(layers)) if tr and all(
+            L["name"] in tr for L in layers) else None),
+        "traffic_per_layer": tr,
         "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)",
         "per_launch_flops": "2*M*N*K of each GEMM launch (M=4096)",
     }
