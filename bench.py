@@ -522,11 +522,14 @@ def main():
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
-    world, rank, local, pg = dist_setup(args)
     if args.impl == "reference":
+        # the CPU oracle on rank 0 only; the other ranks exit at once (no collective needed)
+        world = int(os.environ.get("WORLD_SIZE", "1"))
+        rank = int(os.environ.get("RANK", "0"))
         if rank == 0:
             print(json.dumps(run_reference(args, world, rank)), flush=True)
         return
+    world, rank, local, pg = dist_setup(args)
     line = run_ours(args, world, rank, pg)
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
