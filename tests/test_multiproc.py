@@ -24,10 +24,10 @@ def _torchrun(args, timeout=240):
     return subprocess.run(cmd, cwd=ROOT, env=env, capture_output=True, text=True, timeout=timeout)
 
 
-def test_barrier_and_max_over_ranks_gloo():
-    r = _torchrun([os.path.join("tests", "dist_bench_worker.py")])
+def test_barrier_and_max_over_ranks_gloo(tmp_path):
+    r = _torchrun([os.path.join("tests", "dist_bench_worker.py"), str(tmp_path)])
     assert r.returncode == 0, r.stderr[-2000:]
-    res = [json.loads(l.split("RESULT ", 1)[1]) for l in r.stdout.splitlines() if "RESULT " in l]
+    res = [json.loads((tmp_path / f"rank{i}.json").read_text()) for i in range(2)]
     assert sorted(x["rank"] for x in res) == [0, 1]
     for x in res:
         assert x["world"] == 2
