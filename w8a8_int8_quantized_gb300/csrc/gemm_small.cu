@@ -82,6 +82,7 @@ gemm_small_m_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__ wq
   const int8_t* px1 = xq + (m0 + g + 8) * K;
 
   int acc0[4] = {0, 0, 0, 0}, acc1[4] = {0, 0, 0, 0};
+  const bool two = (m0 + 8) < mend;  // second group of 8 token rows present (CTA-uniform)
   const int64_t nchunks = (K + 63) / 64;
   for (int64_t c0 = warp; c0 < nchunks; c0 += (int64_t)kSmWarps * kSmUnroll) {
     uint4 wa[kSmUnroll][2], xb[kSmUnroll][2];
@@ -93,7 +94,7 @@ gemm_small_m_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__ wq
       wa[u][0] = ld16_stream_or_zero(pw0 + kb, kin && wr0);
       wa[u][1] = ld16_stream_or_zero(pw1 + kb, kin && wr1);
       xb[u][0] = ld16_or_zero(px0 + kb, kin && xr0);
-      xb[u][1] = ld16_or_zero(px1 + kb, kin && xr1);
+      xb[u][1] = ld16_or_zero(px1 + kb, kin && xr1 && two);
     }
 #pragma unroll
     for (int u = 0; u < kSmUnroll; ++u) {
@@ -102,9 +103,12 @@ gemm_small_m_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__ wq
       const uint32_t B0[4] = {xb[u][0].x, xb[u][0].y, xb[u][0].z, xb[u][0].w};
       const uint32_t B1[4] = {xb[u][1].x, xb[u][1].y, xb[u][1].z, xb[u][1].w};
 #pragma unroll
-      for (int j = 0; j < 2; ++j) {
+      for (int j = 0; j < 2; ++j)
         mma_s8_16832(acc0, A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B0[2 * j], B0[2 * j + 1]);
-        mma_s8_16832(acc1, A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B1[2 * j], B1[2 * j + 1]);
+      if (two) {  // blocks of at most 8 token rows (decode) skip the all-zero second group
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          mma_s8_16832(acc1, A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B1[2 * j], B1[2 * j + 1]);
       }
     }
   }
