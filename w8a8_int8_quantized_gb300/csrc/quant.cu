@@ -469,88 +469,139 @@ cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, i
 
 // ---------------------------------------------------------------------------
 // MoE glue: g = bf16(silu(gate) * up) then per-row symmetric quantization.
-// h row = [gate (I) | up (I)], I % 8 == 0.
+// h row = [gate (I) | up (I)], I % 8 == 0.  Persistent like quant_rows_vec: the next row's
+// loads are issued before the current row is processed, one CTA barrier per row.  The SiLU
+// uses the fast exponential and division (g is compared with the oracle's float64 SiLU within
+// the bf16 tolerance); the quantization of g is the exact row rule.
 // ---------------------------------------------------------------------------
-template <int THREADS, bool F16>
+template <int THREADS, int NV, bool F16>
 __global__ void __launch_bounds__(THREADS)
-silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t I, int8_t* __restrict__ gq,
+silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t rows, int64_t I, int8_t* __restrict__ gq,
                       __half* __restrict__ g16, int32_t* __restrict__ norm_out, float* __restrict__ sg) {
-  __shared__ float sh[THREADS / 32];
-  __shared__ int shi[THREADS / 32];
-  const int64_t row = blockIdx.x;
-  const uint4* gate = reinterpret_cast<const uint4*>(h + row * 2 * I);
-  const uint4* up = reinterpret_cast<const uint4*>(h + row * 2 * I + I);
+  constexpr int W = THREADS / 32;
+  __shared__ float sh_a[2][W];
+  __shared__ int sh_abs[2][W];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = (int)(I / 8);
-  constexpr int NV = 4;
-  float g[NV][8];
-  float a = 0.f;
+  uint4 ng[NV], nu[NV];
+  auto load_row = [&](int64_t r) {
+    const uint4* gate = reinterpret_cast<const uint4*>(h + r * 2 * I);
+    const uint4* up = reinterpret_cast<const uint4*>(h + r * 2 * I + I);
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (idx < nvec) {
-      float fa[8], fb[8];
-      unpack8(gate[idx], fa);
-      unpack8(up[idx], fb);
-#pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        const float e = expf(-fa[j]);
-        const float sl = __fdiv_rn(fa[j], __fadd_rn(1.f, e));
-        const float v = __bfloat162float(__float2bfloat16_rn(__fmul_rn(sl, fb[j])));
-        g[i][j] = v;
-        a = fmaxf(a, fabsf(v));
+    for (int i = 0; i < NV; ++i) {
+      const int idx = threadIdx.x + i * THREADS;
+      if (idx < nvec) {
+        ng[i] = ldg_stream(gate + idx);
+        nu[i] = ldg_stream(up + idx);
       }
     }
-  }
-  const RowQuant rq = row_quant_sym(block_reduce_max<THREADS>(a, sh));
-  const float rcp = __frcp_rn(rq.s);
-  int qabs = 0;
+  };
+  int64_t row = blockIdx.x, prev = -1;
+  int buf = 0;
+  if (row < rows) load_row(row);
+  for (; row < rows; row += gridDim.x, buf ^= 1) {
+    float g[NV][8];
+    float a = 0.f;
 #pragma unroll
-  for (int i = 0; i < NV; ++i) {
-    const int idx = threadIdx.x + i * THREADS;
-    if (idx < nvec) {
-      int c[8];
+    for (int i = 0; i < NV; ++i) {
+      const int idx = threadIdx.x + i * THREADS;
+      if (idx < nvec) {
+        float fa[8], fb[8];
+        unpack8(ng[i], fa);
+        unpack8(nu[i], fb);
 #pragma unroll
-      for (int j = 0; j < 8; ++j) {
-        c[j] = quant_row_sym(g[i][j], rq.s, rcp);
-        qabs += abs(c[j]);
-      }
-      if (F16) {
-        uint4 o;
-        o.x = pack_f16x2(c[0], c[1]);
-        o.y = pack_f16x2(c[2], c[3]);
-        o.z = pack_f16x2(c[4], c[5]);
-        o.w = pack_f16x2(c[6], c[7]);
-        reinterpret_cast<uint4*>(g16 + row * I)[idx] = o;
-      } else {
-        uint2 o;
-        o.x = pack4_i8(c[0], c[1], c[2], c[3]);
-        o.y = pack4_i8(c[4], c[5], c[6], c[7]);
-        reinterpret_cast<uint2*>(gq + row * I)[idx] = o;
+        for (int j = 0; j < 8; ++j) {
+          const float sl = __fdividef(fa[j], 1.f + __expf(-fa[j]));
+          const float v = __bfloat162float(__float2bfloat16_rn(__fmul_rn(sl, fb[j])));
+          g[i][j] = v;
+          a = fmaxf(a, fabsf(v));
+        }
       }
     }
+    if (row + gridDim.x < rows) load_row(row + gridDim.x);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+    if (lane == 0) sh_a[buf][warp] = a;
+    __syncthreads();
+    if (F16 && threadIdx.x == 0 && prev >= 0) {
+      int t = 0;
+#pragma unroll
+      for (int i = 0; i < W; ++i) t += sh_abs[buf ^ 1][i];
+      norm_out[prev] = t;
+    }
+    a = sh_a[buf][0];
+#pragma unroll
+    for (int i = 1; i < W; ++i) a = fmaxf(a, sh_a[buf][i]);
+    const RowQuant rq = row_quant_sym(a);
+    const float rcp = __frcp_rn(rq.s);
+    int qabs = 0;
+#pragma unroll
+    for (int i = 0; i < NV; ++i) {
+      const int idx = threadIdx.x + i * THREADS;
+      if (idx < nvec) {
+        uint32_t b[8];
+        quant_row_group_x2<8>(g[i], rq.s, rcp, b);  // |g| <= absmax: codes within +-127
+        const uint32_t w0 = pack4_i8_prmt(b[0], b[1], b[2], b[3]);
+        const uint32_t w1 = pack4_i8_prmt(b[4], b[5], b[6], b[7]);
+        if (F16) {
+          qabs = abssum4_i8(w1, abssum4_i8(w0, qabs));
+          uint4 o;
+          i8x4_to_f16x4(w0, o.x, o.y);
+          i8x4_to_f16x4(w1, o.z, o.w);
+          reinterpret_cast<uint4*>(g16 + row * I)[idx] = o;
+        } else {
+          reinterpret_cast<uint2*>(gq + row * I)[idx] = make_uint2(w0, w1);
+        }
+      }
+    }
+    if (threadIdx.x == 0) sg[row] = rq.s;
+    if (F16) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) qabs += __shfl_xor_sync(0xffffffffu, qabs, o);
+      if (lane == 0) sh_abs[buf][warp] = qabs;
+      prev = row;
+    }
   }
-  if (threadIdx.x == 0) sg[row] = rq.s;
   if (F16) {
-    const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
-    if (threadIdx.x == 0) norm_out[row] = tot;
+    __syncthreads();
+    if (threadIdx.x == 0 && prev >= 0) {
+      int t = 0;
+#pragma unroll
+      for (int i = 0; i < W; ++i) t += sh_abs[buf ^ 1][i];
+      norm_out[prev] = t;
+    }
   }
+}
+
+template <int THREADS, int NV, bool F16>
+static void launch_silu(const __nv_bfloat16* h, int64_t R, int64_t I, int8_t* gq, __half* g16, int32_t* norms,
+                        float* sg, cudaStream_t st) {
+  auto kern = silu_mul_quant_kernel<THREADS, NV, F16>;
+  static unsigned cached = 0;
+  if (cached == 0) cached = persistent_grid(kern, THREADS, (int64_t)1 << 40);
+  const unsigned grid = (unsigned)(R < (int64_t)cached ? R : (int64_t)cached);
+  kern<<<grid, THREADS, 0, st>>>(h, R, I, gq, g16, norms, sg);
+}
+
+template <bool F16>
+static cudaError_t launch_silu_k(const __nv_bfloat16* h, int64_t R, int64_t I, int8_t* gq, __half* g16,
+                                 int32_t* norms, float* sg, cudaStream_t st) {
+  const int64_t nvec = I / 8;
+  if (nvec <= 128 * 2) launch_silu<128, 2, F16>(h, R, I, gq, g16, norms, sg, st);
+  else if (nvec <= 128 * 4) launch_silu<128, 4, F16>(h, R, I, gq, g16, norms, sg, st);
+  else if (nvec <= 256 * 4) launch_silu<256, 4, F16>(h, R, I, gq, g16, norms, sg, st);
+  else if (nvec <= 512 * 4) launch_silu<512, 4, F16>(h, R, I, gq, g16, norms, sg, st);
+  else return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, void* g16, int32_t* norms, float* sg,
                            cudaStream_t st) {
-  const int64_t nvec = I / 8;
+  if (R == 0) return cudaSuccess;
   const __nv_bfloat16* hb = static_cast<const __nv_bfloat16*>(h);
   __half* gh = static_cast<__half*>(g16);
-  if (nvec <= 4 * 128) {
-    if (g16) silu_mul_quant_kernel<128, true><<<(unsigned)R, 128, 0, st>>>(hb, I, gq, gh, norms, sg);
-    else silu_mul_quant_kernel<128, false><<<(unsigned)R, 128, 0, st>>>(hb, I, gq, gh, norms, sg);
-  } else if (nvec <= 4 * 512) {
-    if (g16) silu_mul_quant_kernel<512, true><<<(unsigned)R, 512, 0, st>>>(hb, I, gq, gh, norms, sg);
-    else silu_mul_quant_kernel<512, false><<<(unsigned)R, 512, 0, st>>>(hb, I, gq, gh, norms, sg);
-  } else {
-    return cudaErrorInvalidValue;
-  }
-  return cudaGetLastError();
+  return g16 ? launch_silu_k<true>(hb, R, I, gq, gh, norms, sg, st)
+             : launch_silu_k<false>(hb, R, I, gq, gh, norms, sg, st);
 }
 
 // ---------------------------------------------------------------------------
