@@ -518,6 +518,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int nch = single ? 1 : (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
       const uint32_t b = single ? nbuf : 0u;
       if (single) nbuf ^= 1u;
+      // Single-pass tiles of the symmetric modes: every fp32 accumulator is the exact integer
+      // (|acc| <= 2^24), which is also f32(acc), so y follows from it without the int32/int64
+      // round trip; per-channel scales and bias are read 16 bytes at a time.
+      const bool direct = single && (ep.act_mode == W8A8_ACT_DYN_TOKEN_SYM || ep.act_mode == W8A8_ACT_STATIC_TENSOR_SYM);
+      const bool sw_vec = ep.w_mode == W8A8_W_CHANNEL && (reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0;
+      const bool bias_vec = ep.bias && (reinterpret_cast<uintptr_t>(ep.bias) & 15) == 0;
       for (int c = 0; c < nch; ++c) {
         const uint32_t fcount = b ? filled1 : filled0;
         if (!__all_sync(0xffffffffu, wait_bar(&bars->accfull[b], fcount & 1, bars, p.status))) {
@@ -531,6 +537,54 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         for (int g = 0; g < 4; ++g) {
           uint32_t r[32];
           tmem_ld32(lanebase + b * BN + g * 32, r);
+          if (direct) {
+            tmem_ld_wait();
+            if (!row_ok) continue;
+            const int64_t n0 = nb + g * 32;
+            if (((p.N & 7) == 0) && n0 + 32 <= p.N && (sw_vec || ep.w_mode != W8A8_W_CHANNEL) &&
+                (!ep.bias || bias_vec)) {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) {
+                float sw[8], bb[8];
+                if (ep.w_mode == W8A8_W_CHANNEL) {
+                  const float4 a0 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n0 + 8 * j));
+                  const float4 a1 = __ldg(reinterpret_cast<const float4*>(ep.s_w + n0 + 8 * j + 4));
+                  sw[0] = a0.x; sw[1] = a0.y; sw[2] = a0.z; sw[3] = a0.w;
+                  sw[4] = a1.x; sw[5] = a1.y; sw[6] = a1.z; sw[7] = a1.w;
+                } else {
+#pragma unroll
+                  for (int i = 0; i < 8; ++i) sw[i] = ep.s_w[0];
+                }
+                if (ep.bias) {
+                  const uint4 bv = __ldg(reinterpret_cast<const uint4*>(ep.bias + n0 + 8 * j));
+                  const uint32_t bw[4] = {bv.x, bv.y, bv.z, bv.w};
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    bb[2 * i] = bf16_lo(bw[i]);
+                    bb[2 * i + 1] = bf16_hi(bw[i]);
+                  }
+                }
+                float f[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                  f[i] = __fmul_rn(__fmul_rn(sx, sw[i]), __uint_as_float(r[8 * j + i]));
+                  if (ep.bias) f[i] = __fadd_rn(f[i], bb[i]);
+                }
+                uint4 o;
+                o.x = pack_bf16x2(f[0], f[1]);
+                o.y = pack_bf16x2(f[2], f[3]);
+                o.z = pack_bf16x2(f[4], f[5]);
+                o.w = pack_bf16x2(f[6], f[7]);
+                *reinterpret_cast<uint4*>(yrow + n0 + 8 * j) = o;
+              }
+            } else {
+#pragma unroll
+              for (int i = 0; i < 32; ++i)
+                if (n0 + i < p.N)
+                  yrow[n0 + i] = __float2bfloat16_rn(epi_apply(ep, (int32_t)__uint_as_float(r[i]), sx, zpm, n0 + i));
+            }
+            continue;
+          }
           int32_t v[32];
           if (c > 0) {
             uint32_t pr[32];
