@@ -518,10 +518,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int nch = single ? 1 : (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
       const uint32_t b = single ? nbuf : 0u;
       if (single) nbuf ^= 1u;
-      // Single-pass tiles of the symmetric modes: every fp32 accumulator is the exact integer
-      // (|acc| <= 2^24), which is also f32(acc), so y follows from it without the int32/int64
-      // round trip; per-channel scales and bias are read 16 bytes at a time.
-      const bool direct = single && (ep.act_mode == W8A8_ACT_DYN_TOKEN_SYM || ep.act_mode == W8A8_ACT_STATIC_TENSOR_SYM);
+      // Single-pass tiles: every fp32 accumulator is the exact integer (|acc| <= 2^24), which is
+      // also f32(acc), so y follows from it without the int32/int64 round trip; per-channel
+      // scales and bias are read 16 bytes at a time.  Dynamic asymmetric rows need
+      // f32(acc - zp*azp_adj): acc, zp and azp_adj (|azp_adj| <= 127*K < 2^24) are exact floats,
+      // so one fma rounds the exact difference once, as the integer path does (rows with
+      // |zp| >= 2^24, which bf16 inputs never produce, take the integer form).
+      const bool dyn_asym = ep.act_mode == W8A8_ACT_DYN_TOKEN_ASYM;
+      const bool direct = single && (ep.act_mode == W8A8_ACT_DYN_TOKEN_SYM ||
+                                     ep.act_mode == W8A8_ACT_STATIC_TENSOR_SYM || dyn_asym);
+      const bool zp_exact = zpm > -16777216 && zpm < 16777216;
+      const float zpf = (float)zpm;
+      const bool azp_vec = dyn_asym && (reinterpret_cast<uintptr_t>(ep.azp) & 15) == 0;
       const bool sw_vec = ep.w_mode == W8A8_W_CHANNEL && (reinterpret_cast<uintptr_t>(ep.s_w) & 15) == 0;
       const bool bias_vec = ep.bias && (reinterpret_cast<uintptr_t>(ep.bias) & 15) == 0;
       for (int c = 0; c < nch; ++c) {
@@ -542,7 +550,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!row_ok) continue;
             const int64_t n0 = nb + g * 32;
             if (((p.N & 7) == 0) && n0 + 32 <= p.N && (sw_vec || ep.w_mode != W8A8_W_CHANNEL) &&
-                (!ep.bias || bias_vec)) {
+                (!ep.bias || bias_vec) && (!dyn_asym || azp_vec)) {
 #pragma unroll
               for (int j = 0; j < 4; ++j) {
                 float sw[8], bb[8];
@@ -564,10 +572,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     bb[2 * i + 1] = bf16_hi(bw[i]);
                   }
                 }
+                float cf[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) cf[i] = __uint_as_float(r[8 * j + i]);
+                if (dyn_asym) {
+                  const int4 z0 = __ldg(reinterpret_cast<const int4*>(ep.azp + n0 + 8 * j));
+                  const int4 z1 = __ldg(reinterpret_cast<const int4*>(ep.azp + n0 + 8 * j + 4));
+                  const int az[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+#pragma unroll
+                  for (int i = 0; i < 8; ++i)
+                    cf[i] = zp_exact ? __fmaf_rn(-zpf, __int2float_rn(az[i]), cf[i])
+                                     : __ll2float_rn((long long)cf[i] - (long long)zpm * (long long)az[i]);
+                }
                 float f[8];
 #pragma unroll
                 for (int i = 0; i < 8; ++i) {
-                  f[i] = __fmul_rn(__fmul_rn(sx, sw[i]), __uint_as_float(r[8 * j + i]));
+                  f[i] = __fmul_rn(__fmul_rn(sx, sw[i]), cf[i]);
                   if (ep.bias) f[i] = __fadd_rn(f[i], bb[i]);
                 }
                 uint4 o;
