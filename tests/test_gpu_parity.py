@@ -231,6 +231,20 @@ def test_scaled_mm_dyn_sym(engine, M, N, K):
     check_bf16(y, r["y_bits"], r["y32"])
 
 
+@pytest.mark.parametrize("M,K", [(1, 4112), (2, 14336), (1, 30016), (2, 30016)])
+def test_decode_rows_staged(M, K):
+    """Decode-sized launches (1-2 token rows) stage the rows in shared memory (more than
+    48 KB at K = 30016); bit-exact against the oracle with a ragged channel block."""
+    N = 520
+    d = _gemm_case(M, N, K, seed=M + K)
+    xq, sx, _ = w8.quantize_act(d["x"].to(DEV), "dyn_sym")
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    y = w8.scaled_mm(xq, wq, sx, sw, "dyn_sym", bias=d["b"].to(DEV))
+    r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]))
+    check_bf16(y, r["y_bits"], r["y32"])
+
+
 @pytest.mark.parametrize("engine", [1, 2])
 @pytest.mark.parametrize("act", ["dyn_asym", "static_sym", "static_asym"])
 @pytest.mark.parametrize("w_mode", [w8.W_CHANNEL, w8.W_TENSOR])
