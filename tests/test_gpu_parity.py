@@ -231,11 +231,13 @@ def test_scaled_mm_dyn_sym(engine, M, N, K):
     check_bf16(y, r["y_bits"], r["y32"])
 
 
-@pytest.mark.parametrize("M,K", [(1, 4112), (2, 14336), (1, 30016), (2, 30016)])
-def test_decode_rows_staged(M, K):
-    """Decode-sized launches (1-2 token rows) stage the rows in shared memory (more than
-    48 KB at K = 30016); bit-exact against the oracle with a ragged channel block."""
-    N = 520
+@pytest.mark.parametrize("M,N,K", [(1, 520, 4112), (2, 520, 14336), (1, 520, 30016), (2, 520, 30016),
+                                   (5, 5000, 4096), (8, 5000, 11200), (8, 300, 64)])
+def test_decode_rows_staged(M, N, K):
+    """Launches of at most 8 token rows stage the rows in shared memory (more than 48 KB at
+    K = 30016) and walk 16-channel blocks persistently (N = 5000: more blocks than CTAs, a
+    ragged last block; K = 11200: warps own unequal numbers of K-chunks; K = 64: most warps
+    own none); bit-exact against the oracle."""
     d = _gemm_case(M, N, K, seed=M + K)
     xq, sx, _ = w8.quantize_act(d["x"].to(DEV), "dyn_sym")
     wq = torch.from_numpy(d["rq"]).to(DEV)
@@ -248,8 +250,9 @@ def test_decode_rows_staged(M, K):
 @pytest.mark.parametrize("engine", [1, 2])
 @pytest.mark.parametrize("act", ["dyn_asym", "static_sym", "static_asym"])
 @pytest.mark.parametrize("w_mode", [w8.W_CHANNEL, w8.W_TENSOR])
-def test_linear_modes(engine, act, w_mode):
-    M, N, K = 130, 384, 1088
+@pytest.mark.parametrize("M,N", [(130, 384), (6, 5000)])
+def test_linear_modes(engine, act, w_mode, M, N):
+    K = 1088
     d = _gemm_case(M, N, K, seed=11, act=act, w_mode=w_mode)
     w8.set_gemm_engine(engine)
     xs = d["x"].float().numpy()

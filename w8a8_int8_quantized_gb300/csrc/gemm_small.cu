@@ -135,11 +135,23 @@ gemm_small_m_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__ wq
   }
 }
 
-// Dense decode blocks (at most 2 token rows): the rows are staged in shared memory once (row
-// stride K + 16 bytes so rows read by one quarter-warp fall in different banks), then every
-// thread issues its weight loads for kXsUnroll chunks before the first MMA, so a K = 4096
-// block needs a single dependent round trip to HBM instead of two.
+// Dense launches of at most 8 token rows whose rows fit in shared memory (<= 96 KB): a
+// persistent CTA stages the rows once and then walks 16-channel blocks, issuing all its weight
+// loads for kXsUnroll chunks per warp before the first MMA, so a K = 4096 block needs one
+// dependent round trip to HBM; two CTAs per SM overlap one's loads with the other's reduction
+// and epilogue.  Warp w only ever reads the 64-byte K-chunks c = w (mod kSmWarps), so it stages
+// exactly those with asynchronous copies, issued before its first weight loads and waited for
+// (this warp's copies only, then a warp barrier) just before its first shared-memory read.  The
+// staged row stride is 64 mod 128 bytes: the two rows one quarter-warp reads, 64 bytes each,
+// cover all 32 banks once.
 constexpr int kXsUnroll = 8;
+__host__ __device__ inline int64_t xs_stride(int64_t K) { return (K + 127) / 128 * 128 + 64; }
+
+__device__ __forceinline__ void cp_async16(void* smem, const void* gmem) {
+  const uint32_t s = static_cast<uint32_t>(__cvta_generic_to_shared(smem));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(s), "l"(gmem) : "memory");
+}
+
 __global__ void __launch_bounds__(kSmWarps * 32)
 gemm_small_m_xs_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__ wq, int64_t rows, int64_t N,
                        int64_t K, EpiParams ep, __nv_bfloat16* __restrict__ y) {
@@ -147,73 +159,88 @@ gemm_small_m_xs_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__
   __shared__ int red[kSmWarps][16][17];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
-  const int64_t n0 = (int64_t)blockIdx.x * 16;
-  const int64_t m0 = (int64_t)blockIdx.y * 16;
-  const int nr = (int)((rows - m0) < 16 ? (rows - m0) : 16);
-  const int64_t ld = K + 16;
-  // stage the token rows (K % 16 == 0, rows 16-byte aligned)
-  for (int64_t i = threadIdx.x; i < (int64_t)nr * (K / 16); i += blockDim.x) {
-    const int64_t r = i / (K / 16), c = i % (K / 16);
-    *reinterpret_cast<uint4*>(xs + r * ld + c * 16) = __ldg(reinterpret_cast<const uint4*>(xq + (m0 + r) * K) + c);
+  const int nr = (int)rows;  // <= 8 (the second token group serves the 9-16 row callers of this form)
+  const int64_t ld = xs_stride(K);
+  const int64_t nchunks = (K + 63) / 64;
+  {
+    const int64_t mine = nchunks > warp ? (nchunks - warp + kSmWarps - 1) / kSmWarps : 0;
+    const int64_t pieces = (int64_t)nr * mine * 4;
+    for (int64_t i = lane; i < pieces; i += 32) {
+      const int64_t r = i / (mine * 4), rem = i % (mine * 4);
+      const int64_t kb = (warp + (rem >> 2) * kSmWarps) * 64 + (rem & 3) * 16;
+      if (kb < K) cp_async16(xs + r * ld + kb, xq + r * K + kb);
+    }
+    asm volatile("cp.async.commit_group;\n" ::: "memory");
   }
-  __syncthreads();
-  const bool wr0 = (n0 + g) < N, wr1 = (n0 + g + 8) < N;
+  bool staged = false;
   const bool xr0 = g < nr, xr1 = (g + 8) < nr;
   const bool two = nr > 8;
-  const int8_t* pw0 = wq + (n0 + g) * K;
-  const int8_t* pw1 = wq + (n0 + g + 8) * K;
   const uint8_t* sx0 = xs + g * ld;
   const uint8_t* sx1 = xs + (g + 8) * ld;
-  int acc0[4] = {0, 0, 0, 0}, acc1[4] = {0, 0, 0, 0};
-  const int64_t nchunks = (K + 63) / 64;
-  for (int64_t c0 = warp; c0 < nchunks; c0 += (int64_t)kSmWarps * kXsUnroll) {
-    uint4 wa[kXsUnroll][2];
+  const int64_t nbn = (N + 15) / 16;
+  for (int64_t nb = blockIdx.x; nb < nbn; nb += gridDim.x) {
+    const int64_t n0 = nb * 16;
+    const bool wr0 = (n0 + g) < N, wr1 = (n0 + g + 8) < N;
+    const int8_t* pw0 = wq + (n0 + g) * K;
+    const int8_t* pw1 = wq + (n0 + g + 8) * K;
+    int acc0[2][4] = {}, acc1[2][4] = {};  // split by k-half: shorter dependent MMA chains
+    for (int64_t c0 = warp; c0 < nchunks; c0 += (int64_t)kSmWarps * kXsUnroll) {
+      uint4 wa[kXsUnroll][2];
 #pragma unroll
-    for (int u = 0; u < kXsUnroll; ++u) {
-      const int64_t c = c0 + (int64_t)u * kSmWarps;
-      const int64_t kb = c * 64 + tq * 16;
-      const bool kin = (c < nchunks) && (kb < K);
-      wa[u][0] = ld16_stream_or_zero(pw0 + kb, kin && wr0);
-      wa[u][1] = ld16_stream_or_zero(pw1 + kb, kin && wr1);
-    }
+      for (int u = 0; u < kXsUnroll; ++u) {
+        const int64_t c = c0 + (int64_t)u * kSmWarps;
+        const int64_t kb = c * 64 + tq * 16;
+        const bool kin = (c < nchunks) && (kb < K);
+        wa[u][0] = ld16_stream_or_zero(pw0 + kb, kin && wr0);
+        wa[u][1] = ld16_stream_or_zero(pw1 + kb, kin && wr1);
+      }
+      if (!staged) {  // warp-uniform
+        asm volatile("cp.async.wait_all;\n" ::: "memory");
+        __syncwarp();
+        staged = true;
+      }
 #pragma unroll
-    for (int u = 0; u < kXsUnroll; ++u) {
-      const int64_t c = c0 + (int64_t)u * kSmWarps;
-      const int64_t kb = c * 64 + tq * 16;
-      const bool kin = (c < nchunks) && (kb < K);
-      const uint4 x0 = (kin && xr0) ? *reinterpret_cast<const uint4*>(sx0 + kb) : make_uint4(0, 0, 0, 0);
-      const uint32_t A0[4] = {wa[u][0].x, wa[u][0].y, wa[u][0].z, wa[u][0].w};
-      const uint32_t A1[4] = {wa[u][1].x, wa[u][1].y, wa[u][1].z, wa[u][1].w};
-      const uint32_t B0[4] = {x0.x, x0.y, x0.z, x0.w};
-#pragma unroll
-      for (int j = 0; j < 2; ++j)
-        mma_s8_16832(acc0, A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B0[2 * j], B0[2 * j + 1]);
-      if (two) {
-        const uint4 x1 = (kin && xr1) ? *reinterpret_cast<const uint4*>(sx1 + kb) : make_uint4(0, 0, 0, 0);
-        const uint32_t B1[4] = {x1.x, x1.y, x1.z, x1.w};
+      for (int u = 0; u < kXsUnroll; ++u) {
+        const int64_t c = c0 + (int64_t)u * kSmWarps;
+        const int64_t kb = c * 64 + tq * 16;
+        const bool kin = (c < nchunks) && (kb < K);
+        const uint4 x0 = (kin && xr0) ? *reinterpret_cast<const uint4*>(sx0 + kb) : make_uint4(0, 0, 0, 0);
+        const uint32_t A0[4] = {wa[u][0].x, wa[u][0].y, wa[u][0].z, wa[u][0].w};
+        const uint32_t A1[4] = {wa[u][1].x, wa[u][1].y, wa[u][1].z, wa[u][1].w};
+        const uint32_t B0[4] = {x0.x, x0.y, x0.z, x0.w};
 #pragma unroll
         for (int j = 0; j < 2; ++j)
-          mma_s8_16832(acc1, A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B1[2 * j], B1[2 * j + 1]);
+          mma_s8_16832(acc0[j], A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B0[2 * j], B0[2 * j + 1]);
+        if (two) {
+          const uint4 x1 = (kin && xr1) ? *reinterpret_cast<const uint4*>(sx1 + kb) : make_uint4(0, 0, 0, 0);
+          const uint32_t B1[4] = {x1.x, x1.y, x1.z, x1.w};
+#pragma unroll
+          for (int j = 0; j < 2; ++j)
+            mma_s8_16832(acc1[j], A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B1[2 * j], B1[2 * j + 1]);
+        }
       }
     }
-  }
-  red[warp][g][2 * tq] = acc0[0];
-  red[warp][g][2 * tq + 1] = acc0[1];
-  red[warp][g + 8][2 * tq] = acc0[2];
-  red[warp][g + 8][2 * tq + 1] = acc0[3];
-  red[warp][g][8 + 2 * tq] = acc1[0];
-  red[warp][g][8 + 2 * tq + 1] = acc1[1];
-  red[warp][g + 8][8 + 2 * tq] = acc1[2];
-  red[warp][g + 8][8 + 2 * tq + 1] = acc1[3];
-  __syncthreads();
-  const int tok = threadIdx.x >> 4, ch = threadIdx.x & 15;
-  const int64_t m = m0 + tok, n = n0 + ch;
-  if (tok < nr && n < N) {
-    int sum = 0;
+    // D fragment: (row g / g+8 = channel, col 2tq / 2tq+1 = token)
+    red[warp][g][2 * tq] = acc0[0][0] + acc0[1][0];
+    red[warp][g][2 * tq + 1] = acc0[0][1] + acc0[1][1];
+    red[warp][g + 8][2 * tq] = acc0[0][2] + acc0[1][2];
+    red[warp][g + 8][2 * tq + 1] = acc0[0][3] + acc0[1][3];
+    red[warp][g][8 + 2 * tq] = acc1[0][0] + acc1[1][0];
+    red[warp][g][8 + 2 * tq + 1] = acc1[0][1] + acc1[1][1];
+    red[warp][g + 8][8 + 2 * tq] = acc1[0][2] + acc1[1][2];
+    red[warp][g + 8][8 + 2 * tq + 1] = acc1[0][3] + acc1[1][3];
+    __syncthreads();
+    const int tok = threadIdx.x >> 4, ch = threadIdx.x & 15;
+    const int64_t n = n0 + ch;
+    if (tok < nr && n < N) {
+      int sum = 0;
 #pragma unroll
-    for (int w = 0; w < kSmWarps; ++w) sum += red[w][ch][tok];
-    y[m * N + n] = __float2bfloat16_rn(epi_apply(ep, sum, epi_row_scale(ep, m), epi_row_zp(ep, m), n));
+      for (int w = 0; w < kSmWarps; ++w) sum += red[w][ch][tok];
+      y[tok * N + n] = __float2bfloat16_rn(epi_apply(ep, sum, epi_row_scale(ep, tok), epi_row_zp(ep, tok), n));
+    }
+    __syncthreads();  // red is rewritten by the next block
   }
+  asm volatile("cp.async.wait_all;\n" ::: "memory");  // warps that read no chunk still own copies
 }
 
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st) {
@@ -227,17 +254,22 @@ cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st) {
   ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
   const int64_t gx = (g.N + 15) / 16;
   {
-    // decode (at most 2 token rows): staging the rows once per CTA removes the second
-    // dependent load round; with more rows the staging traffic outweighs it
-    const int64_t xs_bytes = (g.rows < 16 ? g.rows : 16) * (g.K + 16);
-    if (!g.seg && g.rows > 0 && g.rows <= 2 && xs_bytes <= 96 * 1024) {
-      static int s_attr = 0;
-      if (xs_bytes > 48 * 1024 && !s_attr) {
-        cudaError_t e = cudaFuncSetAttribute(gemm_small_m_xs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    const int64_t xs_bytes = g.rows * xs_stride(g.K);
+    if (!g.seg && g.rows > 0 && g.rows <= 8 && xs_bytes <= 96 * 1024) {
+      static int s_dev = -1, s_grid = 0;
+      int dev = 0;
+      cudaError_t e = cudaGetDevice(&dev);
+      if (e != cudaSuccess) return e;
+      if (dev != s_dev) {
+        e = cudaFuncSetAttribute(gemm_small_m_xs_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
         if (e != cudaSuccess) return e;
-        s_attr = 1;
+        int sms = 0;
+        e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (e != cudaSuccess) return e;
+        s_grid = 2 * sms;  // two CTAs per SM (registers and up to 2 x 96 KB of staged rows)
+        s_dev = dev;
       }
-      dim3 grid((unsigned)gx, (unsigned)((g.rows + 15) / 16));
+      const unsigned grid = (unsigned)(gx < s_grid ? gx : s_grid);
       gemm_small_m_xs_kernel<<<grid, kSmWarps * 32, (size_t)xs_bytes, st>>>(g.a, g.w, g.rows, g.N, g.K, ep,
                                                                          static_cast<__nv_bfloat16*>(g.y));
       return cudaGetLastError();
