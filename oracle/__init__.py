@@ -12,7 +12,8 @@ Sources (cited throughout by these short names):
                (blog.gitcode.com); sections 4.1 方案判定, 4.2 权重布局与 kernel 选择.
   [SGLang-CT]  "[SGLang] W4A8, W8A8, W4A4: 혼합 정밀도 양자화 스킴"
                (blog.secrett2633.cloud); items 3 (W8A8 INT8: 정수 양자화),
-               4 (W8A8 INT8 비대칭 양자화: AZP 보정).
+               4 (W8A8 INT8 비대칭 양자화: AZP 보정), 7 (텐서별 스케일 후처리:
+               requantize_with_max_scale), 설계 근거 3 (Fused 모듈 호환).
   [Kunlun-INT8] "MiniMax-M2.7 FP8 转昆仑芯 INT8" (README on dev.modelhub.org.cn);
                sections 转换关系 (conversion relation) and 验证 (validation).
 
@@ -38,6 +39,13 @@ pins live in tests/test_oracle_*.py and tests/golden/):
                                    illegal scales, hand-worked golden example.
   moe_forward                      pinned: segment == dense per-expert call, combine
                                    == per-token loop, empty experts.
+  requantize_with_max_scale        pinned: the max-scale partition is unchanged for
+                                   every code, power-of-two ratios reduce to
+                                   rint(q / 2^j) (ties to even), the half-step bound
+                                   of the requantized value against q * s_p.
+  moe_route                        pinned: brute-force top-k by pairwise comparison
+                                   (ties to the lower index), weights summing to 1
+                                   over all experts, hand-worked example.
 """
 
 from .w8a8_oracle import (  # noqa: F401
@@ -58,4 +66,6 @@ from .w8a8_oracle import (  # noqa: F401
     silu_mul_bf16,
     moe_sort,
     moe_forward,
+    moe_route,
+    requantize_with_max_scale,
 )

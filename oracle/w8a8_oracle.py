@@ -297,6 +297,43 @@ def quantize_weight_per_channel(w):
 
 
 # ---------------------------------------------------------------------------
+# Fused modules with per-tensor scales: one scale for the whole weight
+# ---------------------------------------------------------------------------
+
+def requantize_with_max_scale(q_w, scales, logical_widths):
+    """Unify the per-tensor scales of a fused weight (e.g. Q/K/V) to their maximum.
+
+    [SGLang-CT] item 7 (텐서별 스케일 후처리: requantize_with_max_scale) and
+    설계 근거 3 (Fused 모듈 호환): the logical partitions of a fused weight may carry
+    different per-tensor scales; the largest becomes the module's single scale and
+    the weights are quantized again against it.  The page prints only the call, so
+    the arithmetic is our reading: partition p covers the next logical_widths[p]
+    rows; each code is dequantized with one float32 multiply and requantized with
+    the weight rule (float32 division, ties to even, clamp to +-127):
+        s_max   = max_p scales[p]
+        w'[n,k] = clamp(rint(f32(f32(q[n,k]) * scales[p]) / s_max), -127, 127)
+    q_w int8 [N, K]; scales float32 [P] (positive, finite); sum(logical_widths) == N.
+    Returns (w' int8 [N, K], s_max float32).
+    """
+    q = np.asarray(q_w, dtype=np.int8)
+    sc = np.asarray(scales, dtype=F32).reshape(-1)
+    widths = [int(w) for w in logical_widths]
+    if len(widths) != sc.size or sum(widths) != q.shape[0] or any(w < 0 for w in widths):
+        raise ValueError("logical_widths must give one non-negative width per scale, summing to N")
+    if not np.all(np.isfinite(sc)) or not np.all(sc > 0):
+        raise ValueError("per-tensor scales must be positive and finite")
+    s_max = F32(sc.max())
+    out = np.empty_like(q)
+    r0 = 0
+    for p, wdt in enumerate(widths):
+        deq = (q[r0:r0 + wdt].astype(F32) * sc[p]).astype(F32)   # one float32 multiply
+        t = (deq / s_max).astype(F32)                             # IEEE float32 division
+        out[r0:r0 + wdt] = np.clip(_rint_int(t), -127, 127).astype(np.int8)
+        r0 += wdt
+    return out, s_max
+
+
+# ---------------------------------------------------------------------------
 # S8: FP8 E4M3 block-scaled -> INT8 per-row requantization
 # ---------------------------------------------------------------------------
 
@@ -392,6 +429,34 @@ def moe_sort(topk_ids, num_experts):
     seg = np.zeros(num_experts + 1, dtype=np.int64)
     seg[1:] = np.cumsum(counts)
     return (order // k).astype(np.int64), (order % k).astype(np.int64), seg
+
+
+def moe_route(logits, topk):
+    """Per-token expert choice and routing weight from router logits.
+
+    The MoE INT8 scheme ([SGLang-CT] file tree: compressed_tensors_w8a8_int8_moe;
+    [Kunlun-INT8] MoE method with experts w1/w2/w3) runs each token through the
+    experts it is routed to; the pages leave the router itself to the framework.
+    Our reading (the plainest one): ids[t] = the topk experts with the largest
+    logits, in descending order, equal logits broken by the lower expert index;
+    w[t, j] = softmax(logits[t])[ids[t, j]] over all E experts (not renormalised
+    over the chosen ones), evaluated in float64.
+    logits float32 [T, E].  Returns (ids int32 [T, topk], w float64 [T, topk]).
+    """
+    lg = np.asarray(logits, dtype=F32)
+    T, E = lg.shape
+    if not 1 <= topk <= E:
+        raise ValueError("topk must be in [1, E]")
+    ids = np.empty((T, topk), dtype=np.int32)
+    w = np.empty((T, topk), dtype=F64)
+    for t in range(T):
+        row = lg[t].astype(F64)
+        # stable sort of -logit keeps the lower index first among equal logits
+        order = np.argsort(-row, kind="stable")[:topk]
+        ids[t] = order
+        e = np.exp(row - row.max())
+        w[t] = e[order] / e.sum()
+    return ids, w
 
 
 def moe_forward(x_bits, topk_ids, topk_w, w13_q, s13, w2_q, s2, rows=None):

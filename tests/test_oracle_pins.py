@@ -392,3 +392,87 @@ def test_moe_routing_skew():
     assert counts.sum() == 16384
     assert np.all((ids[:, :, None] == ids[:, None, :]).sum(-1) == 1)  # no repeats per token
     assert counts[0] > 10 * counts[-1]                                 # Zipf-like skew
+
+
+# ---------------------------------------------------------------------------
+# requantize_with_max_scale
+# ---------------------------------------------------------------------------
+
+def test_max_scale_partition_unchanged_and_bound():
+    """The partition that already has the largest scale keeps every code (RN(RN(q*s)/s)
+    is within 1e-5 of q); every other code lands within half a step of q * s_p / s_max."""
+    rng = np.random.default_rng(11)
+    codes = np.arange(-127, 128, dtype=np.int8)
+    for _ in range(20):
+        sc = np.float32(rng.uniform(1e-4, 1e-1, size=3)).astype(np.float32)
+        widths = [2, 3, 4]
+        q = np.stack([rng.permutation(codes) for _ in range(sum(widths))])
+        out, s_max = oracle.requantize_with_max_scale(q, sc, widths)
+        assert s_max == sc.max()
+        row_scale = np.repeat(sc, widths)
+        big = row_scale == s_max
+        np.testing.assert_array_equal(out[big], q[big])
+        exact = q.astype(np.float64) * row_scale[:, None].astype(np.float64) / float(s_max)
+        assert np.all(np.abs(out - exact) <= 0.5 + 1e-5)
+
+
+def test_max_scale_power_of_two_ratios_round_half_even():
+    """s_p = s_max / 2 and s_max / 4: every step is exact, so w' = round(q / 2) and
+    round(q / 4) with ties to even (Python's round), e.g. 3 -> 2, 5 -> 2, -3 -> -2."""
+    codes = np.arange(-127, 128, dtype=np.int8)
+    q = np.stack([codes, codes, codes])
+    sc = np.array([2.0 ** -7, 2.0 ** -8, 2.0 ** -9], dtype=np.float32)
+    out, s_max = oracle.requantize_with_max_scale(q, sc, [1, 1, 1])
+    assert s_max == np.float32(2.0 ** -7)
+    np.testing.assert_array_equal(out[0], codes)
+    np.testing.assert_array_equal(out[1], [round(int(c) / 2) for c in codes])
+    np.testing.assert_array_equal(out[2], [round(int(c) / 4) for c in codes])
+    assert out[1][list(codes).index(3)] == 2 and out[1][list(codes).index(5)] == 2
+    assert out[1][list(codes).index(-3)] == -2 and out[2][list(codes).index(6)] == 2
+
+
+def test_max_scale_boundaries_and_errors():
+    """Rows take the scale of the partition they fall in (a zero-width partition in the
+    middle owns no row); mismatched widths and bad scales are rejected."""
+    q = np.full((8, 4), 100, dtype=np.int8)
+    sc = np.array([0.5, 8.0, 1.0], dtype=np.float32)  # the middle (max) partition is empty
+    out, s_max = oracle.requantize_with_max_scale(q, sc, [3, 0, 5])
+    assert s_max == np.float32(8.0)
+    np.testing.assert_array_equal(out[:3], np.full((3, 4), 6, np.int8))    # 100*0.5/8 = 6.25
+    np.testing.assert_array_equal(out[3:], np.full((5, 4), 12, np.int8))   # 100/8 = 12.5 -> 12
+    with pytest.raises(ValueError):
+        oracle.requantize_with_max_scale(q, sc, [3, 0, 4])
+    with pytest.raises(ValueError):
+        oracle.requantize_with_max_scale(q, np.array([0.5, 0.0, 1.0], np.float32), [3, 0, 5])
+
+
+# ---------------------------------------------------------------------------
+# moe_route
+# ---------------------------------------------------------------------------
+
+def test_moe_route_bruteforce_topk_and_ties():
+    """Top-k by pairwise comparison: expert e ranks r(e) = #{e' : l[e'] > l[e], or equal
+    with e' < e}; ids are the experts of rank 0..k-1 in rank order.  Logits drawn from a
+    few values so that ties are frequent."""
+    rng = np.random.default_rng(5)
+    lg = rng.integers(-3, 3, size=(40, 9)).astype(np.float32) * np.float32(0.75)
+    for k in (1, 2, 4, 9):
+        ids, w = oracle.moe_route(lg, k)
+        for t in range(lg.shape[0]):
+            l = lg[t]
+            rank = [sum(1 for f in range(9) if l[f] > l[e] or (l[f] == l[e] and f < e)) for e in range(9)]
+            want = sorted(range(9), key=lambda e: rank[e])[:k]
+            assert list(ids[t]) == want
+        if k == 9:
+            np.testing.assert_allclose(w.sum(axis=1), 1.0, rtol=0, atol=1e-12)
+
+
+def test_moe_route_worked_example():
+    """logits (0, ln 3, 0, 0): softmax = (1/6, 1/2, 1/6, 1/6); top-2 = expert 1 and, of the
+    three equal ones, expert 0, with weights 1/2 and 1/6 (not renormalised to sum 1)."""
+    lg = np.array([[0.0, math.log(3.0), 0.0, 0.0], [1.0, 3.0, 3.0, 0.0]], dtype=np.float32)
+    ids, w = oracle.moe_route(lg, 2)
+    assert list(ids[0]) == [1, 0] and list(ids[1]) == [1, 2]
+    np.testing.assert_allclose(w[0], [0.5, 1 / 6], rtol=1e-6)
+    e = np.exp(np.array([1.0, 3.0, 3.0, 0.0]) - 3.0)
+    np.testing.assert_allclose(w[1], [e[1] / e.sum(), e[2] / e.sum()], rtol=1e-6)
