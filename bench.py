@@ -368,9 +368,11 @@ def run_e2e(args, layers, w8, world, pg):
             "overlap": "copies on separate streams overlap other layers' compute"}
 
 
-def _time_launches(fn, reps=10, warm=2):
+def _time_launches(fn, reps=10, warm=2, rounds=5):
     """Median device time of one fn() call, replayed from a CUDA graph so that host-side
-    argument marshalling never shows up as device time."""
+    argument marshalling never shows up as device time.  Each event pair spans `reps`
+    back-to-back replays (event timestamps tick in steps of about 2 us, too coarse for one
+    launch of a few tens of microseconds); the median is over `rounds` such pairs."""
     for _ in range(warm):
         fn()
     torch.cuda.synchronize()
@@ -380,15 +382,16 @@ def _time_launches(fn, reps=10, warm=2):
     g.replay()
     torch.cuda.synchronize()
     evs = []
-    for _ in range(reps):
+    for _ in range(rounds):
         a = torch.cuda.Event(enable_timing=True)
         b = torch.cuda.Event(enable_timing=True)
         a.record()
-        g.replay()
+        for _ in range(reps):
+            g.replay()
         b.record()
         evs.append((a, b))
     torch.cuda.synchronize()
-    return statistics.median(a.elapsed_time(b) for a, b in evs)
+    return statistics.median(a.elapsed_time(b) / reps for a, b in evs)
 
 
 def components(w8, wl, peaks):
@@ -409,6 +412,15 @@ def components(w8, wl, peaks):
             b = 8192 * K * 3 + 8192 * 4 * (2 if mode == "dyn_asym" else 1)
             out[f"quant_{mode}_M8192_K{K}"] = {"us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
                                                 "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+        del x
+        # the affine rule on its own workload, rows ~ N(0.5, 1): bf16 quotients land on or next
+        # to half-integers far more often there, and each such value is decided by a division
+        x = wl.asym_activations(8192, K, seed=5).to(dev)
+        ms = _time_launches(lambda: (flush.zero_(), w8.quantize_act(x, "dyn_asym"))) - ms_flush
+        b = 8192 * K * 3 + 8192 * 8
+        out[f"quant_dyn_asym_M8192_K{K}_nonzero_mean_rows"] = {
+            "us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+            "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
         del x
     # S7 weight quantizer on the gate_up weight
     w = torch.randn(28672, 4096, device=dev, dtype=torch.float32).mul_(0.02).to(torch.bfloat16)

@@ -180,13 +180,72 @@ w8a8_status fp8block_to_int8_rowwise(const uint8_t* w, const float* scale_inv, i
 
 /*
  * fp8block_to_int8_rowwise_batched -- the same for `count` matrices in one launch per up to
- * 64 matrices.  The four pointer arrays and the N/K arrays are HOST arrays of length count
+ * 60 matrices.  The four pointer arrays and the N/K arrays are HOST arrays of length count
  * holding device pointers / sizes; they are read before the call returns.
  */
 w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,
                                              const float* const* scale_inv, const int64_t* N,
                                              const int64_t* K, int8_t* const* q, float* const* s,
                                              int32_t* dev_status, cudaStream_t stream);
+
+/*
+ * fp8block_to_int8_rowwise_batched_adj -- the batched requantization that also writes, for
+ * each matrix whose azp_adj[i] is non-null, the row sums of its int8 codes:
+ *   azp_adj[i][n] = sum_k q_i[n, k]   (int32, exact; 0 for a row zeroed as illegal)
+ * i.e. the weight-side correction term of asymmetric activations ([SGLang-CT] item 4,
+ * AZP 보정: azp_adj is the column sum of the int8 weight along K), produced in the same pass
+ * that converts an FP8-block checkpoint ([Kunlun-INT8] FP8 -> INT8 conversion), so the
+ * converted weight is never read again to form it.  azp_adj is a HOST array of length count
+ * (or null for none) of device int32 [N_i] pointers (4-byte aligned, or null).  Everything
+ * else is as in fp8block_to_int8_rowwise_batched.
+ */
+w8a8_status fp8block_to_int8_rowwise_batched_adj(int count, const uint8_t* const* w,
+                                                 const float* const* scale_inv, const int64_t* N,
+                                                 const int64_t* K, int8_t* const* q, float* const* s,
+                                                 int32_t* const* azp_adj, int32_t* dev_status,
+                                                 cudaStream_t stream);
+
+/*
+ * w8a8_moe_route -- the routing that feeds the MoE INT8 path ([SGLang-CT] file tree:
+ * compressed_tensors_w8a8_int8_moe; [Kunlun-INT8] MoE method over experts w1/w2/w3; the
+ * pages leave the router to the framework, so the rule is the plain one):
+ *   topk_ids[t, :] = the topk experts with the largest logits, in descending order, equal
+ *                    logits broken by the lower expert index;
+ *   topk_w[t, j]   = softmax(logits[t, :])[topk_ids[t, j]] over all E experts (fp32,
+ *                    max-subtracted; not renormalised over the chosen experts);
+ * then the T*topk (token, slot) pairs sorted stably by expert (ties keep token, then slot
+ * order) -- a counting sort:
+ *   seg_offsets[e] .. seg_offsets[e+1]  the routed rows of expert e (seg_offsets[E] = T*topk);
+ *   row_index[r]   = token of routed row r      (what w8a8_moe_quantize_gather reads);
+ *   row_of[t, j]   = routed row of (t, slot j)  (what w8a8_moe_combine reads).
+ *   logits float [T, E]; topk_ids int32 [T, topk]; topk_w float [T, topk];
+ *   seg_offsets int64 [E+1]; row_index int64 [T*topk]; row_of int64 [T, topk] (all device).
+ *   1 <= E <= 256, 1 <= topk <= min(8, E).  workspace: at least
+ *   w8a8_moe_route_workspace_size(T, E, topk) bytes (4-byte aligned; null allowed for T = 0).
+ */
+size_t w8a8_moe_route_workspace_size(int64_t T, int E, int topk);
+w8a8_status w8a8_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* topk_ids,
+                           float* topk_w, int64_t* seg_offsets, int64_t* row_index, int64_t* row_of,
+                           void* workspace, size_t workspace_bytes, cudaStream_t stream);
+
+/*
+ * w8a8_requantize_max_scale -- one per-tensor scale for a fused weight ([SGLang-CT] item 7,
+ * 텐서별 스케일 후처리: requantize_with_max_scale; 설계 근거 3, Fused 모듈 호환).  A fused
+ * module (e.g. Q/K/V stacked along the output dimension) whose P logical partitions were
+ * quantized with their own per-tensor scales gets the largest of them as its single scale,
+ * and every code is requantized against it, in place:
+ *   s_max = max_p scales[p];
+ *   wq[n, k] <- clamp(rint(RN(RN(q[n, k] * scales[p]) / s_max)), -127, 127)
+ * for the rows n of partition p (fp32 multiply, IEEE fp32 division, ties to even).
+ *   wq int8 [N, K] (device; read and rewritten in place; any K, 16-byte alignment and
+ *   K % 16 == 0 take the vector path); scales float [P] (device); logical_widths int64 [P]
+ *   (HOST, rows per partition, summing to N); 1 <= P <= 16; s_max float [1] (device, out).
+ * A scale that is not positive and finite leaves wq and s_max untouched and writes
+ * W8A8_ERR_BAD_SCALE to dev_status (may be null).
+ */
+w8a8_status w8a8_requantize_max_scale(int8_t* wq, int64_t N, int64_t K, const float* scales,
+                                      const int64_t* logical_widths, int P, float* s_max,
+                                      int32_t* dev_status, cudaStream_t stream);
 
 /*
  * w8a8_grouped_mm -- MoE expert GEMMs over token-sorted segments ([SGLang-CT] MoE INT8

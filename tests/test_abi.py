@@ -83,5 +83,13 @@ def test_host_side_argument_checks_need_no_gpu(libpath):
     # workspace too small
     assert lib.w8a8_linear(p, 4, 16, 16, 0, None, None, p, 4, 0, p, None, None, p, p, 8, None, None) == 7
     assert lib.w8a8_linear_workspace_size(4, 16, 0) == 256 + 256 + 2 * 256
+    # max-scale requantization: widths must sum to N, 1 <= P <= 16
+    w2 = (ctypes.c_int64 * 2)(3, 4)
+    assert lib.w8a8_requantize_max_scale(p, 8, 16, p, ctypes.cast(w2, ctypes.c_void_p), 2, p, None, None) == 1
+    assert lib.w8a8_requantize_max_scale(p, 7, 16, p, ctypes.cast(w2, ctypes.c_void_p), 0, p, None, None) == 1
+    assert lib.w8a8_requantize_max_scale(p, 7, 16, p, ctypes.cast(w2, ctypes.c_void_p), 17, p, None, None) == 1
+    # requantization with row sums: a negative count is an argument error, zero is a no-op
+    assert lib.fp8block_to_int8_rowwise_batched_adj(-1, p, p, p, p, p, p, None, None, None) == 1
+    assert lib.fp8block_to_int8_rowwise_batched_adj(0, None, None, None, None, None, None, None, None, None) == 0
     assert lib.w8a8_set_gemm_engine(5) == 1
     assert lib.w8a8_set_gemm_engine(0) == 0

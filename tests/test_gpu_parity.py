@@ -454,6 +454,30 @@ def test_fp8_requant_batched_mixed():
     assert int(st.item()) == 0
 
 
+def test_fp8_requant_batched_adj():
+    """The requantizer's optional row sums (the converted weight's azp_adj) on every path:
+    the shared-memory ring (K = 4096, 4112), the streaming kernel (K = 65536), the byte path
+    (K = 1500), a zero row, and rows zeroed by an illegal block scale and a NaN code; the codes
+    and scales must be unchanged by asking for the sums."""
+    mats = [wl.fp8_block_matrix(*shape, seed=6, stream=i) for i, shape in
+            enumerate([(512, 4096), (300, 1500), (5, 65536), (130, 4112)])]
+    mats = [(c.clone(), si.clone()) for c, si, _ in mats]
+    mats[0][1][1, 2] = 0.0      # rows 128..255 of the first matrix: illegal scale
+    mats[3][0][5, 7] = 0x7F     # row 5 of the last: a NaN code
+    mats[1][0][17, :] = 0       # an all-zero row
+    dev = [(c.to(DEV), si.to(DEV)) for c, si in mats]
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    outs = w8.fp8block_to_int8_rowwise_batched(dev, status=st, azp_adj=True)
+    plain = w8.fp8block_to_int8_rowwise_batched(dev)
+    for (c, si), (q, sq, adj), (q0, s0) in zip(mats, outs, plain):
+        rq, rs, _ = oracle.fp8_block_to_int8_rowwise(c.numpy(), si.numpy())
+        np.testing.assert_array_equal(q.cpu().numpy(), rq)
+        np.testing.assert_array_equal(sq.cpu().numpy(), rs)
+        np.testing.assert_array_equal(adj.cpu().numpy(), oracle.azp_adj(rq))
+        assert torch.equal(q, q0) and torch.equal(sq, s0)
+    assert int(st.item()) == 4
+
+
 def test_fp8_requant_full_config_sampled():
     """The requant workload (64 x [6144,4096] + 8 x [3000,1500]) in its batched launch;
     sampled rows of every matrix against the oracle, zero rows checked exactly."""
@@ -553,3 +577,81 @@ def test_grouped_mm_empty_segments():
         acc = oracle.int8_gemm(xq[a:b].numpy(), wq[e].numpy())
         yb, y32 = oracle.scaled_mm_epilogue(acc, sx[a:b].numpy(), sw[e].numpy())
         check_bf16(y[a:b], yb, y32)
+
+
+@pytest.mark.parametrize("widths,K", [([4096, 1024, 1024], 4096), ([300, 77, 0, 129], 1500), ([64], 512),
+                                      ([3, 5], 4112)])
+def test_requantize_max_scale(widths, K):
+    """Fused Q/K/V-style weights with per-partition tensor scales, requantized in place to
+    the largest scale: bit-exact against the oracle (Llama-3-8B q/k/v widths; a ragged K on
+    the byte path with an empty partition; one partition = no change; tiny partitions)."""
+    N = sum(widths)
+    rng = np.random.default_rng(N + K)
+    q = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    sc = rng.uniform(1e-4, 3e-3, size=len(widths)).astype(np.float32)
+    want, want_s = oracle.requantize_with_max_scale(q, sc, widths)
+    wq = torch.from_numpy(q).to(DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    s_max = w8.requantize_max_scale(wq, torch.from_numpy(sc).to(DEV), widths, status=st)
+    np.testing.assert_array_equal(wq.cpu().numpy(), want)
+    assert s_max.item() == float(want_s) and int(st.item()) == 0
+
+
+@pytest.mark.parametrize("bad", [0.0, -1.0, float("inf"), float("nan")])
+def test_requantize_max_scale_bad_scale(bad):
+    q = torch.randint(-127, 128, (40, 64), dtype=torch.int8)
+    wq = q.to(DEV)
+    s_max = torch.full((1,), 7.0, device=DEV)
+    st = torch.zeros(1, dtype=torch.int32, device=DEV)
+    sc = torch.tensor([1e-3, bad, 2e-3], dtype=torch.float32, device=DEV)
+    s_max = w8.requantize_max_scale(wq, sc, [10, 10, 20], status=st)
+    assert torch.equal(wq.cpu(), q) and int(st.item()) == 4
+
+
+def _route_expected(lg, k):
+    ids, w = oracle.moe_route(lg, k)
+    tok, slot, seg = oracle.moe_sort(ids, lg.shape[1])
+    row_of = np.zeros(ids.shape, np.int64)
+    row_of[tok, slot] = np.arange(len(tok))
+    return ids, w, seg, tok, row_of
+
+
+@pytest.mark.parametrize("T,E,k,kind", [(4096, 32, 4, "workload"), (300, 256, 8, "normal"), (777, 60, 3, "ties"),
+                                        (1, 1, 1, "normal"), (5, 33, 2, "ties"), (0, 8, 2, "normal")])
+def test_moe_route(T, E, k, kind):
+    """Top-k ids, segment offsets and both row maps bit-exact against the oracle (ties to the
+    lower expert; stable by token then slot); weights within 1e-5 relative (fp32 softmax with
+    expf against the oracle's float64: a few fp32 roundings over at most 256 terms)."""
+    if kind == "workload":
+        lg = wl.moe_workload(T=T, H=64, E=E, topk=k, inter=64, seed=3, with_weights=False)["logits"].numpy()
+    else:
+        rng = np.random.default_rng(T * 1000 + E)
+        lg = rng.standard_normal((T, E)).astype(np.float32)
+        if kind == "ties":
+            lg = np.round(lg * 2).astype(np.float32)
+    ids, w, seg, row_index, row_of = w8.moe_route(torch.from_numpy(lg).to(DEV), k)
+    rid, rw, rseg, rtok, rrow = _route_expected(lg, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    np.testing.assert_array_equal(seg.cpu().numpy(), rseg)
+    np.testing.assert_array_equal(row_index.cpu().numpy(), rtok)
+    np.testing.assert_array_equal(row_of.cpu().numpy(), rrow)
+    np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-5, atol=0)
+
+
+def test_moe_route_feeds_moe_forward():
+    """The routed outputs drive the MoE layer end to end: the same result as the oracle layer
+    given the oracle's routing (the weights within the routing tolerance)."""
+    T, H, E, k, inter = 96, 256, 8, 2, 128
+    d = wl.moe_workload(T=T, H=H, E=E, topk=k, inter=inter, seed=9)
+    ids, w, seg, row_index, row_of = w8.moe_route(d["logits"].to(DEV), k)
+    w13q, s13 = w8.quantize_weight(d["w13"].reshape(E * 2 * inter, H).to(DEV))
+    w2q, s2 = w8.quantize_weight(d["w2"].reshape(E * H, inter).to(DEV))
+    y, h, o = w8.moe_forward(d["x"].to(DEV), row_index, seg, row_of, w, w13q.view(E, 2 * inter, H),
+                             s13.view(E, 2 * inter), w2q.view(E, H, inter), s2.view(E, H))
+    rid, rw = oracle.moe_route(d["logits"].numpy(), k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), rid)
+    r = oracle.moe_forward(wl.bits(d["x"]), rid, rw.astype(np.float32), w13q.view(E, 2 * inter, H).cpu().numpy(),
+                           s13.view(E, 2 * inter).cpu().numpy(), w2q.view(E, H, inter).cpu().numpy(),
+                           s2.view(E, H).cpu().numpy())
+    np.testing.assert_array_equal(npbits(h), r["h_bits"])
+    check_bf16(y, r["y_bits"], oracle.bf16_bits_to_f32(r["y_bits"]), exact=False)

@@ -33,8 +33,10 @@ from ._binding import (  # noqa: F401
     moe_combine,
     moe_forward,
     moe_quantize_gather,
+    moe_route,
     quantize_act,
     quantize_weight,
+    requantize_max_scale,
     scaled_mm,
     set_gemm_engine,
     silu_mul_quant,

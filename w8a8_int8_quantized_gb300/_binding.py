@@ -42,6 +42,10 @@ SIGNATURES = {
     "w8a8_azp_adj": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "fp8block_to_int8_rowwise": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
     "fp8block_to_int8_rowwise_batched": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "fp8block_to_int8_rowwise_batched_adj": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+    "w8a8_requantize_max_scale": (_I, [_P, _I64, _I64, _P, _P, _I, _P, _P, _P]),
+    "w8a8_moe_route_workspace_size": (_SZ, [_I64, _I, _I]),
+    "w8a8_moe_route": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "w8a8_grouped_mm_workspace_size": (_SZ, [_I64, _I64]),
     "w8a8_grouped_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _SZ, _P, _P]),
     "w8a8_moe_quantize_gather": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
@@ -214,14 +218,18 @@ def fp8block_to_int8_rowwise(codes, scale_inv, status=None):
     return q, s
 
 
-def fp8block_to_int8_rowwise_batched(mats, outs=None, status=None):
-    """mats: list of (codes, scale_inv) CUDA tensors.  Returns list of (q, s)."""
+def fp8block_to_int8_rowwise_batched(mats, outs=None, status=None, azp_adj=False):
+    """mats: list of (codes, scale_inv) CUDA tensors.  Returns list of (q, s), or of
+    (q, s, azp_adj) when azp_adj is True (int32 [N] row sums of q, written in the same pass)."""
     n = len(mats)
     if outs is None:
         outs = []
         for c, _ in mats:
-            outs.append((torch.empty(c.shape, dtype=torch.int8, device=c.device),
-                         torch.empty(c.shape[0], dtype=torch.float32, device=c.device)))
+            o = (torch.empty(c.shape, dtype=torch.int8, device=c.device),
+                 torch.empty(c.shape[0], dtype=torch.float32, device=c.device))
+            if azp_adj:
+                o = o + (torch.empty(c.shape[0], dtype=torch.int32, device=c.device),)
+            outs.append(o)
     for c, si in mats:
         _need(c, torch.uint8, "codes", 2)
         _need(si, torch.float32, "scale_inv", 2)
@@ -231,13 +239,64 @@ def fp8block_to_int8_rowwise_batched(mats, outs=None, status=None):
     si = arr(*[s.data_ptr() for _, s in mats])
     Ns = ai(*[c.shape[0] for c, _ in mats])
     Ks = ai(*[c.shape[1] for c, _ in mats])
-    qs = arr(*[q.data_ptr() for q, _ in outs])
-    ss = arr(*[s.data_ptr() for _, s in outs])
-    code = lib().fp8block_to_int8_rowwise_batched(n, ctypes.cast(w, _P), ctypes.cast(si, _P), ctypes.cast(Ns, _P),
-                                                  ctypes.cast(Ks, _P), ctypes.cast(qs, _P), ctypes.cast(ss, _P),
-                                                  _ptr(status), _stream())
+    qs = arr(*[o[0].data_ptr() for o in outs])
+    ss = arr(*[o[1].data_ptr() for o in outs])
+    if azp_adj:
+        for o in outs:
+            _need(o[2], torch.int32, "azp_adj", 1)
+        adj = arr(*[o[2].data_ptr() for o in outs])
+        code = lib().fp8block_to_int8_rowwise_batched_adj(
+            n, ctypes.cast(w, _P), ctypes.cast(si, _P), ctypes.cast(Ns, _P), ctypes.cast(Ks, _P),
+            ctypes.cast(qs, _P), ctypes.cast(ss, _P), ctypes.cast(adj, _P), _ptr(status), _stream())
+    else:
+        code = lib().fp8block_to_int8_rowwise_batched(n, ctypes.cast(w, _P), ctypes.cast(si, _P),
+                                                      ctypes.cast(Ns, _P), ctypes.cast(Ks, _P),
+                                                      ctypes.cast(qs, _P), ctypes.cast(ss, _P), _ptr(status),
+                                                      _stream())
     _check("fp8block_to_int8_rowwise_batched", code)
     return outs
+
+
+def moe_route(logits, topk, workspace=None):
+    """Router logits float32 [T, E] -> (topk_ids int32 [T, k], topk_w float32 [T, k],
+    seg_offsets int64 [E+1], row_index int64 [T*k], row_of int64 [T, k]): top-k by logit
+    (ties to the lower expert), softmax weights over all experts, and the stable counting
+    sort of the routed rows by expert -- the inputs moe_forward takes."""
+    _need(logits, torch.float32, "logits", 2)
+    if not logits.is_contiguous():
+        raise ValueError("logits must be contiguous")
+    T, E = logits.shape
+    dev = logits.device
+    ids = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    w = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    seg = torch.empty(E + 1, dtype=torch.int64, device=dev)
+    row_index = torch.empty(T * topk, dtype=torch.int64, device=dev)
+    row_of = torch.empty((T, topk), dtype=torch.int64, device=dev)
+    need = lib().w8a8_moe_route_workspace_size(T, E, topk)
+    if workspace is None:
+        workspace = torch.empty(max(need, 4), dtype=torch.uint8, device=dev)
+    _check("w8a8_moe_route", lib().w8a8_moe_route(_ptr(logits), T, E, topk, _ptr(ids), _ptr(w), _ptr(seg),
+                                                  _ptr(row_index), _ptr(row_of), _ptr(workspace),
+                                                  workspace.numel(), _stream()))
+    return ids, w, seg, row_index, row_of
+
+
+def requantize_max_scale(wq, scales, logical_widths, status=None):
+    """Fused weight wq int8 [N, K] with per-partition tensor scales (float32 [P]) and
+    logical_widths (P row counts summing to N): requantized IN PLACE against the largest
+    scale, which is returned as a float32 [1] tensor."""
+    _need(wq, torch.int8, "wq", 2)
+    _need(scales, torch.float32, "scales", 1)
+    if not wq.is_contiguous() or not scales.is_contiguous():
+        raise ValueError("wq and scales must be contiguous")
+    N, K = wq.shape
+    widths = [int(w) for w in logical_widths]
+    arr = (ctypes.c_int64 * len(widths))(*widths)
+    s_max = torch.empty(1, dtype=torch.float32, device=wq.device)
+    _check("w8a8_requantize_max_scale",
+           lib().w8a8_requantize_max_scale(_ptr(wq), N, K, _ptr(scales), ctypes.cast(arr, _P),
+                                           len(widths), _ptr(s_max), _ptr(status), _stream()))
+    return s_max
 
 
 def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None, workspace=None):

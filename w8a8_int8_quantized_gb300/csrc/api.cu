@@ -237,6 +237,13 @@ w8a8_status w8a8_azp_adj(const int8_t* wq, int64_t N, int64_t K, const int32_t* 
 w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w, const float* const* scale_inv,
                                              const int64_t* N, const int64_t* K, int8_t* const* q, float* const* s,
                                              int32_t* dev_status, cudaStream_t stream) {
+  return fp8block_to_int8_rowwise_batched_adj(count, w, scale_inv, N, K, q, s, nullptr, dev_status, stream);
+}
+
+w8a8_status fp8block_to_int8_rowwise_batched_adj(int count, const uint8_t* const* w, const float* const* scale_inv,
+                                                 const int64_t* N, const int64_t* K, int8_t* const* q,
+                                                 float* const* s, int32_t* const* azp_adj, int32_t* dev_status,
+                                                 cudaStream_t stream) {
   if (count < 0) return W8A8_ERR_INVALID_ARG;
   if (count == 0) return W8A8_OK;
   if (!w || !scale_inv || !N || !K || !q || !s) return W8A8_ERR_INVALID_ARG;
@@ -244,6 +251,7 @@ w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,
     if (N[i] < 0 || K[i] < 0 || N[i] > 0x7FFFFFFF || K[i] > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
     if (N[i] > 0 && K[i] > 0 && (!w[i] || !scale_inv[i] || !q[i] || !s[i])) return W8A8_ERR_INVALID_ARG;
     if (N[i] > 0 && K[i] > 0 && !aligned(s[i], 4)) return W8A8_ERR_MISALIGNED;
+    if (N[i] > 0 && K[i] > 0 && azp_adj && azp_adj[i] && !aligned(azp_adj[i], 4)) return W8A8_ERR_MISALIGNED;
   }
   w8a8_status st = check_device();
   if (st != W8A8_OK) return st;
@@ -259,6 +267,7 @@ w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,
         m.sinv = scale_inv[i];
         m.q = q[i];
         m.s = s[i];
+        m.adj = azp_adj ? azp_adj[i] : nullptr;
         m.row0 = rows;
         m.N = (int32_t)N[i];
         m.K = (int32_t)K[i];
@@ -277,6 +286,56 @@ w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,
     }
   }
   return W8A8_OK;
+}
+
+static bool route_args_ok(int64_t T, int E, int topk) {
+  return T >= 0 && T <= 0x7FFFFFFF && E >= 1 && E <= 256 && topk >= 1 && topk <= 8 && topk <= E;
+}
+
+size_t w8a8_moe_route_workspace_size(int64_t T, int E, int topk) {
+  return route_args_ok(T, E, topk) ? moe_route_workspace(T, E, topk) : 0;
+}
+
+w8a8_status w8a8_moe_route(const float* logits, int64_t T, int E, int topk, int32_t* topk_ids, float* topk_w,
+                           int64_t* seg_offsets, int64_t* row_index, int64_t* row_of, void* workspace,
+                           size_t workspace_bytes, cudaStream_t stream) {
+  if (!route_args_ok(T, E, topk) || !seg_offsets) return W8A8_ERR_INVALID_ARG;
+  if (T > 0 && (!logits || !topk_ids || !topk_w || !row_index || !row_of)) return W8A8_ERR_INVALID_ARG;
+  if (T > 0 && (!workspace || workspace_bytes < moe_route_workspace(T, E, topk))) return W8A8_ERR_WORKSPACE;
+  if (!aligned(logits, 4) || !aligned(topk_ids, 4) || !aligned(topk_w, 4) || !aligned(seg_offsets, 8) ||
+      !aligned(row_index, 8) || !aligned(row_of, 8) || !aligned(workspace, 4))
+    return W8A8_ERR_MISALIGNED;
+  w8a8_status st = check_device();
+  if (st != W8A8_OK) return st;
+  return cuda_status(moe_route(logits, T, E, topk, topk_ids, topk_w, seg_offsets, row_index, row_of, workspace,
+                               stream));
+}
+
+w8a8_status w8a8_requantize_max_scale(int8_t* wq, int64_t N, int64_t K, const float* scales,
+                                      const int64_t* logical_widths, int P, float* s_max, int32_t* dev_status,
+                                      cudaStream_t stream) {
+  if (N < 0 || K < 0 || P < 1 || P > kMaxScaleParts) return W8A8_ERR_INVALID_ARG;
+  if (!scales || !logical_widths || !s_max || (N > 0 && K > 0 && !wq)) return W8A8_ERR_INVALID_ARG;
+  if (!aligned(scales, 4) || !aligned(s_max, 4)) return W8A8_ERR_MISALIGNED;
+  int64_t rows = 0;
+  for (int p = 0; p < P; ++p) {
+    if (logical_widths[p] < 0) return W8A8_ERR_INVALID_ARG;
+    rows += logical_widths[p];
+  }
+  if (rows != N) return W8A8_ERR_INVALID_ARG;
+  w8a8_status st = check_device();
+  if (st != W8A8_OK) return st;
+  MaxScaleParts parts;
+  memset(&parts, 0, sizeof(parts));
+  parts.P = P;
+  parts.vec = (K % 16 == 0 && aligned(wq, 16)) ? 1 : 0;
+  const int64_t per_row = parts.vec ? K / 16 : K;  // units of the flattened weight per row
+  int64_t end = 0;
+  for (int p = 0; p < P; ++p) {
+    end += logical_widths[p] * per_row;
+    parts.end[p] = end;
+  }
+  return cuda_status(requant_max_scale(wq, N * per_row, scales, parts, s_max, dev_status, stream));
 }
 
 w8a8_status fp8block_to_int8_rowwise(const uint8_t* w, const float* scale_inv, int64_t N, int64_t K, int8_t* q,

@@ -30,13 +30,14 @@ struct ReqMat {
   const float* sinv;
   int8_t* q;
   float* s;
+  int32_t* adj;  // optional [N]: row sums of q (the weight's azp_adj), or null
   int64_t row0;  // first global row of this matrix in the batch
   int32_t N;
   int32_t K;
   int32_t vec;   // 1: 16-byte vector path
   int32_t pad;
 };
-constexpr int kReqMaxBatch = 64;
+constexpr int kReqMaxBatch = 60;
 struct ReqBatch {
   int32_t count;
   int32_t pad;
@@ -46,6 +47,20 @@ struct ReqBatch {
 static_assert(sizeof(ReqBatch) <= 4096, "kernel parameter block must stay within 4 KB");
 cudaError_t requant_batch(const ReqBatch& b, int32_t* st, cudaStream_t stream);
 bool requant_vec_ok(const uint8_t* w, const int8_t* q, int64_t K);
+// MoE routing: top-k + softmax weights per token, stable counting sort into expert segments.
+size_t moe_route_workspace(int64_t T, int E, int topk);
+cudaError_t moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* w, int64_t* seg,
+                      int64_t* row_index, int64_t* row_of, void* ws, cudaStream_t st);
+// Fused weight with per-tensor scales -> one scale (the largest): partition p covers the
+// units [end[p-1], end[p]) of the flattened weight, in 16-byte chunks (vec) or bytes.
+constexpr int kMaxScaleParts = 16;
+struct MaxScaleParts {
+  int32_t P;
+  int32_t vec;
+  int64_t end[kMaxScaleParts];
+};
+cudaError_t requant_max_scale(int8_t* wq, int64_t units, const float* scales, const MaxScaleParts& parts,
+                              float* s_out, int32_t* st, cudaStream_t stream);
 
 // GEMM problem description shared by both GEMM engines.  Rows of A are grouped into
 // segments; segment e multiplies weight rows [e*N, (e+1)*N).  A dense GEMM is one segment.

@@ -47,6 +47,13 @@ __device__ __forceinline__ bool scale_ok(float s) { return (s > 0.f) && (s <= 3.
 // and blocks whose scale or factor lies outside [2^-100, 2^100] (where the products above
 // could leave the normal range), are decided by the IEEE division itself.
 
+// sum over the warp (the row sums of the codes: the weight's azp_adj)
+__device__ __forceinline__ int warp_sum_i(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
 // largest |value| of n16 groups of 16 codes as fp16 bits (> 0x7C00: a NaN code)
 __device__ __forceinline__ uint32_t habsmax_nan(uint32_t acc, uint32_t h) {
   asm("max.NaN.xorsign.abs.f16x2 %0, %0, %1;" : "+r"(acc) : "r"(h));
@@ -220,18 +227,24 @@ requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
     row_absmax_smem(rowv, srow, nv, nbc, lane, amax, bad);
     const float s = row_scale(amax, bad);
     uint4* qr = reinterpret_cast<uint4*>(mt.q + i * (int64_t)K);
+    int qsum = 0;
     if (!bad) {
       const float r = __frcp_rn(s);
       for (int bb = lane; bb < nbc; bb += 32) cb[bb] = block_factor(srow[bb], r);
       __syncwarp();
 #pragma unroll 2
-      for (int idx = lane; idx < nv; idx += 32)
-        qr[idx] = requant_group(rowv[idx], cb[idx >> 3], srow + (idx >> 3), s);
+      for (int idx = lane; idx < nv; idx += 32) {
+        const uint4 o = requant_group(rowv[idx], cb[idx >> 3], srow + (idx >> 3), s);
+        qr[idx] = o;
+        if (mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
+      }
     } else {
       for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
     }
+    if (mt.adj) qsum = warp_sum_i(qsum);
     if (lane == 0) {
       mt.s[i] = s;
+      if (mt.adj) mt.adj[i] = qsum;
       if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
     }
     __syncwarp();  // every lane is done with the slot (and with cb)
@@ -266,16 +279,22 @@ requant_stream_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
     }
     const float s = row_scale(amax, bad);
     uint4* qr = reinterpret_cast<uint4*>(mt.q + i * (int64_t)K);
+    int qsum = 0;
     if (!bad) {
       const float r = __frcp_rn(s);
 #pragma unroll 2
-      for (int idx = lane; idx < nv; idx += 32)
-        qr[idx] = requant_group(wr[idx], block_factor(srow[idx >> 3], r), srow + (idx >> 3), s);
+      for (int idx = lane; idx < nv; idx += 32) {
+        const uint4 o = requant_group(wr[idx], block_factor(srow[idx >> 3], r), srow + (idx >> 3), s);
+        qr[idx] = o;
+        if (mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
+      }
     } else {
       for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
     }
+    if (mt.adj) qsum = warp_sum_i(qsum);
     if (lane == 0) {
       mt.s[i] = s;
+      if (mt.adj) mt.adj[i] = qsum;
       if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
     }
   }
@@ -362,13 +381,17 @@ __device__ __forceinline__ void req_row_generic(const ReqMat& mt, int64_t i, int
   float s = 1.f;
   if (!bad && amax != 0.f) s = __fdiv_rn(amax, 127.f);
   int8_t* qr = mt.q + i * K;
+  int qsum = 0;
   for (int64_t j = lane; j < K; j += 32) {
     int v = 0;
     if (!bad) v = quant_sym(__fmul_rn(e4m3_value(wr[j]), srow[j >> 7]), s);
     qr[j] = (int8_t)v;
+    qsum += v;
   }
+  if (mt.adj) qsum = warp_sum_i(qsum);
   if (lane == 0) {
     mt.s[i] = s;
+    if (mt.adj) mt.adj[i] = qsum;
     if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
   }
 }
@@ -412,6 +435,118 @@ cudaError_t requant_batch(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
     const int64_t blocks = (gb.total_rows + kReqWarps - 1) / kReqWarps;
     requant_generic_kernel<<<(unsigned)blocks, kReqWarps * 32, 0, stream>>>(gb, st);
   }
+  return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Per-tensor scales of a fused weight (Q/K/V partitions) unified to their maximum:
+//   w'[n,k] = clamp(rint(RN(RN(q[n,k] * s_p) / s_max)), -127, 127)
+// The result depends only on the code and its partition, so every CTA first evaluates that
+// rule (one fp32 multiply, the IEEE division, ties-to-even conversion) for the 256 codes of
+// each partition into a shared-memory table; the weight is then streamed through the table,
+// 16 bytes per load, in place.  A partition scale that is not positive and finite leaves the
+// weight and s_out untouched and reports W8A8_ERR_BAD_SCALE.
+// ---------------------------------------------------------------------------
+constexpr int kMsThreads = 256;
+constexpr int kMsUnroll = 4;
+
+__device__ __forceinline__ uint32_t lut_map4(const int8_t* lut, uint32_t w) {
+  const uint32_t b0 = (uint8_t)lut[w & 0xFFu], b1 = (uint8_t)lut[(w >> 8) & 0xFFu];
+  const uint32_t b2 = (uint8_t)lut[(w >> 16) & 0xFFu], b3 = (uint8_t)lut[w >> 24];
+  return b0 | (b1 << 8) | (b2 << 16) | (b3 << 24);
+}
+
+template <bool VEC>
+__global__ void __launch_bounds__(kMsThreads)
+max_scale_requant_kernel(int8_t* __restrict__ wq, int64_t units, const float* __restrict__ scales,
+                         const __grid_constant__ MaxScaleParts parts, float* __restrict__ s_out, int32_t* st) {
+  __shared__ int8_t lut[kMaxScaleParts][256];
+  __shared__ float sh_max;
+  __shared__ int sh_ok;
+  const int P = parts.P;
+  if (threadIdx.x < 32) {
+    float m = 0.f;
+    bool ok = true;
+    for (int p = threadIdx.x; p < P; p += 32) {
+      const float v = scales[p];
+      ok &= (v > 0.f) && (v <= 3.402823466e38f);
+      m = fmaxf(m, v);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    ok = __all_sync(0xffffffffu, ok);
+    if (threadIdx.x == 0) {
+      sh_max = m;
+      sh_ok = ok ? 1 : 0;
+    }
+  }
+  __syncthreads();
+  if (!sh_ok) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) report_status(st, W8A8_ERR_BAD_SCALE);
+    return;
+  }
+  const float smax = sh_max;
+  for (int i = threadIdx.x; i < P * 256; i += kMsThreads) {
+    const int p = i >> 8;
+    const float c = (float)(int)(int8_t)(uint8_t)(i & 255);  // the code whose byte is i & 255
+    const int n = __float2int_rn(__fdiv_rn(__fmul_rn(c, scales[p]), smax));
+    lut[p][i & 255] = (int8_t)min(127, max(-127, n));
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0) *s_out = smax;
+  __syncthreads();
+  const int64_t stride = (int64_t)gridDim.x * kMsThreads * kMsUnroll;
+  for (int64_t u0 = (int64_t)blockIdx.x * kMsThreads * kMsUnroll + threadIdx.x; u0 < units; u0 += stride) {
+    if (VEC) {
+      uint4 v[kMsUnroll];
+#pragma unroll
+      for (int j = 0; j < kMsUnroll; ++j) {
+        const int64_t u = u0 + (int64_t)j * kMsThreads;
+        if (u < units) v[j] = *reinterpret_cast<const uint4*>(wq + u * 16);
+      }
+#pragma unroll
+      for (int j = 0; j < kMsUnroll; ++j) {
+        const int64_t u = u0 + (int64_t)j * kMsThreads;
+        if (u < units) {
+          int p = 0;
+          while (p + 1 < P && u >= parts.end[p]) ++p;
+          const int8_t* t = lut[p];
+          *reinterpret_cast<uint4*>(wq + u * 16) =
+              make_uint4(lut_map4(t, v[j].x), lut_map4(t, v[j].y), lut_map4(t, v[j].z), lut_map4(t, v[j].w));
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < kMsUnroll; ++j) {
+        const int64_t u = u0 + (int64_t)j * kMsThreads;
+        if (u < units) {
+          int p = 0;
+          while (p + 1 < P && u >= parts.end[p]) ++p;
+          wq[u] = lut[p][(uint8_t)wq[u]];
+        }
+      }
+    }
+  }
+}
+
+cudaError_t requant_max_scale(int8_t* wq, int64_t units, const float* scales, const MaxScaleParts& parts,
+                              float* s_out, int32_t* st, cudaStream_t stream) {
+  static int s_dev = -1, s_sms = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != s_dev) {
+    e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    s_dev = dev;
+  }
+  // enough CTAs for every unit in one sweep, at most 8 per SM (each builds its own table)
+  const int64_t need = (units + kMsThreads * kMsUnroll - 1) / (kMsThreads * kMsUnroll);
+  const int64_t cap = (int64_t)s_sms * 8;
+  const unsigned grid = (unsigned)(need < 1 ? 1 : (need < cap ? need : cap));
+  if (parts.vec)
+    max_scale_requant_kernel<true><<<grid, kMsThreads, 0, stream>>>(wq, units, scales, parts, s_out, st);
+  else
+    max_scale_requant_kernel<false><<<grid, kMsThreads, 0, stream>>>(wq, units, scales, parts, s_out, st);
   return cudaGetLastError();
 }
 

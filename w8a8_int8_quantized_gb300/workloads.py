@@ -94,7 +94,8 @@ def moe_workload(T=4096, H=4096, E=32, topk=4, inter=1408, seed=0, with_weights=
     probs = torch.softmax(logits, dim=1)
     ids = top.indices.to(torch.int32)
     w = torch.gather(probs, 1, top.indices).to(torch.float32)
-    out = dict(x=x, topk_ids=ids, topk_w=w, E=E, topk=topk, inter=inter, H=H, T=T)
+    out = dict(x=x, topk_ids=ids, topk_w=w, E=E, topk=topk, inter=inter, H=H, T=T,
+               logits=logits.to(torch.float32))
     if with_weights:
         out["w13"] = _normal((E, 2 * inter, H), 0.0, 0.02, seed, 42).to(torch.bfloat16)
         out["w2"] = _normal((E, H, inter), 0.0, 0.02, seed, 43).to(torch.bfloat16)
