@@ -422,13 +422,22 @@ def components(w8, wl, peaks):
             "us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
             "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
         del x
-    # S7 weight quantizer on the gate_up weight
-    w = torch.randn(28672, 4096, device=dev, dtype=torch.float32).mul_(0.02).to(torch.bfloat16)
-    ms = _time_launches(lambda: w8.quantize_weight(w, with_azp_adj=True))
-    b = 28672 * 4096 * 3 + 28672 * 8
-    out["quant_weight_28672x4096"] = {"us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
-                                      "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
-    del w
+    # S7 weight quantizer (+ azp_adj) on the four Llama-3-8B weights
+    for N, K in ((6144, 4096), (4096, 4096), (28672, 4096), (4096, 14336)):
+        w = torch.randn(N, K, device=dev, dtype=torch.float32).mul_(0.02).to(torch.bfloat16)
+        ms = _time_launches(lambda: (flush.zero_(), w8.quantize_weight(w, with_azp_adj=True))) - ms_flush
+        b = N * K * 3 + N * 8
+        out[f"quant_weight_{N}x{K}"] = {"us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                        "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+        del w
+    # fused Q/K/V weight with per-partition tensor scales -> one (max) scale, in place
+    wq = torch.randint(-127, 128, (6144, 4096), dtype=torch.int8, device=dev)
+    sc = torch.tensor([1.1e-3, 1.7e-3, 1.3e-3], dtype=torch.float32, device=dev)
+    ms = _time_launches(lambda: (flush.zero_(), w8.requantize_max_scale(wq, sc, [4096, 1024, 1024]))) - ms_flush
+    b = 6144 * 4096 * 2
+    out["requant_max_scale_qkv_6144x4096"] = {"us": round(ms * 1e3, 2), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+                                              "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+    del wq
     # S8 requant: 64 x [6144, 4096] + 8 x [3000, 1500], one batched call
     g = torch.Generator(device=dev).manual_seed(7)
     mats = []
@@ -445,6 +454,13 @@ def components(w8, wl, peaks):
     out["requant_64x6144x4096_plus_8x3000x1500"] = {"us": round(ms * 1e3, 1),
                                                     "GBps": round(b / (ms * 1e-3) / 1e9, 1),
                                                     "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
+    # the same conversion writing each weight's azp_adj (row sums of the codes) in the pass
+    outs = [o + (torch.empty(o[0].shape[0], dtype=torch.int32, device=dev),) for o in outs]
+    ms = _time_launches(lambda: w8.fp8block_to_int8_rowwise_batched(mats, outs, azp_adj=True), reps=5)
+    b += sum(c.shape[0] * 4 for c, _ in mats)
+    out["requant_with_azp_adj_64x6144x4096_plus_8x3000x1500"] = {
+        "us": round(ms * 1e3, 1), "GBps": round(b / (ms * 1e-3) / 1e9, 1),
+        "frac_hbm": round(b / (ms * 1e-3) / 1e9 / hbm, 3)}
     del mats, outs
     # S2/S3 asymmetric linears, K = N = 4096
     for M in (128, 4096):
@@ -474,6 +490,19 @@ def components(w8, wl, peaks):
     ms = _time_launches(lambda: w8.moe_forward(*md["args"]), reps=5)
     out["moe_T4096_E32_top4"] = {"us": round(ms * 1e3, 1), "TOPS": round(md["ops"] / (ms * 1e-3) / 1e12, 1),
                                  "frac_tensor": round(md["ops"] / (ms * 1e-3) / 1e12 / tf, 3)}
+    # routing on the GPU (top-4 of 32 + counting sort), alone and in front of the layer
+    logits = wl.moe_workload(T=4096, H=64, E=32, topk=4, inter=64, seed=0, with_weights=False)["logits"].to(dev)
+    rws = torch.empty(max(w8.lib().w8a8_moe_route_workspace_size(4096, 32, 4), 4), dtype=torch.uint8, device=dev)
+    ms = _time_launches(lambda: w8.moe_route(logits, 4, workspace=rws), reps=20)
+    out["moe_route_T4096_E32_top4"] = {"us": round(ms * 1e3, 2)}
+    x, _, _, _, _, w13, s13, w2, s2 = md["args"]
+
+    def routed_layer():
+        ids, tw, seg, row_index, row_of = w8.moe_route(logits, 4, workspace=rws)
+        return w8.moe_forward(x, row_index, seg, row_of, tw, w13, s13, w2, s2)
+    ms = _time_launches(routed_layer, reps=5)
+    out["moe_T4096_E32_top4_with_routing"] = {"us": round(ms * 1e3, 1),
+                                              "TOPS": round(md["ops"] / (ms * 1e-3) / 1e12, 1)}
     return out
 
 

@@ -180,7 +180,7 @@ w8a8_status fp8block_to_int8_rowwise(const uint8_t* w, const float* scale_inv, i
 
 /*
  * fp8block_to_int8_rowwise_batched -- the same for `count` matrices in one launch per up to
- * 60 matrices.  The four pointer arrays and the N/K arrays are HOST arrays of length count
+ * 64 matrices.  The four pointer arrays and the N/K arrays are HOST arrays of length count
  * holding device pointers / sizes; they are read before the call returns.
  */
 w8a8_status fp8block_to_int8_rowwise_batched(int count, const uint8_t* const* w,

@@ -387,7 +387,8 @@ def test_llama_full_size_sampled(name, N, K):
 
 # ------------------------------------------------------------------ FP8 -> INT8 requant
 
-@pytest.mark.parametrize("N,K", [(256, 4096), (300, 1500), (129, 1500), (5, 17), (384, 512)])
+@pytest.mark.parametrize("N,K", [(256, 4096), (300, 1500), (129, 1500), (5, 17), (384, 512), (70, 4), (130, 516),
+                                 (33, 4092), (20, 4100)])
 def test_fp8_requant(N, K):
     codes, sinv, _ = wl.fp8_block_matrix(N, K, seed=3, stream=N + K, zero_frac=0.01)
     st = torch.zeros(1, dtype=torch.int32, device=DEV)
@@ -398,9 +399,10 @@ def test_fp8_requant(N, K):
     assert int(st.item()) == 0 and not bad.any()
 
 
+@pytest.mark.parametrize("K", [384, 1500])
 @pytest.mark.parametrize("bad_val", [0.0, -1.0, float("inf"), float("nan")])
-def test_fp8_requant_illegal_scale(bad_val):
-    codes, sinv, _ = wl.fp8_block_matrix(256, 384, seed=2, stream=9, zero_frac=0.0)
+def test_fp8_requant_illegal_scale(bad_val, K):
+    codes, sinv, _ = wl.fp8_block_matrix(256, K, seed=2, stream=9, zero_frac=0.0)
     c, si = codes.clone(), sinv.clone()
     si[1, 2] = bad_val
     c[5, 7] = 0x7F

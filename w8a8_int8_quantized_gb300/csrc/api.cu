@@ -260,7 +260,7 @@ w8a8_status fp8block_to_int8_rowwise_batched_adj(int count, const uint8_t* const
     ReqBatch b;
     memset(&b, 0, sizeof(b));
     int64_t rows = 0;
-    while (i < count && b.count < kReqMaxBatch) {
+    while (i < count && b.count < kReqMaxBatch && rows + N[i] <= 0x7FFFFFFF) {
       if (N[i] > 0 && K[i] > 0) {
         ReqMat& m = b.m[b.count++];
         m.w = w[i];
@@ -268,10 +268,10 @@ w8a8_status fp8block_to_int8_rowwise_batched_adj(int count, const uint8_t* const
         m.q = q[i];
         m.s = s[i];
         m.adj = azp_adj ? azp_adj[i] : nullptr;
-        m.row0 = rows;
+        m.row0 = (int32_t)rows;
         m.N = (int32_t)N[i];
         m.K = (int32_t)K[i];
-        m.vec = requant_vec_ok(w[i], q[i], K[i]) ? 1 : 0;
+        m.vec = requant_path(w[i], q[i], K[i]);
         rows += N[i];
       } else if (N[i] > 0 && K[i] == 0) {
         // no columns: every row is an all-zero row (q empty, s = 1)

@@ -31,13 +31,12 @@ struct ReqMat {
   int8_t* q;
   float* s;
   int32_t* adj;  // optional [N]: row sums of q (the weight's azp_adj), or null
-  int64_t row0;  // first global row of this matrix in the batch
+  int32_t row0;  // first row of this matrix in the batch (a batch holds fewer than 2^31 rows)
   int32_t N;
   int32_t K;
-  int32_t vec;   // 1: 16-byte vector path
-  int32_t pad;
+  int32_t vec;   // requant_path(): 1 vector rows, 2 word rows, 0 byte rows
 };
-constexpr int kReqMaxBatch = 60;
+constexpr int kReqMaxBatch = 64;
 struct ReqBatch {
   int32_t count;
   int32_t pad;
@@ -46,7 +45,8 @@ struct ReqBatch {
 };
 static_assert(sizeof(ReqBatch) <= 4096, "kernel parameter block must stay within 4 KB");
 cudaError_t requant_batch(const ReqBatch& b, int32_t* st, cudaStream_t stream);
-bool requant_vec_ok(const uint8_t* w, const int8_t* q, int64_t K);
+// 1: 16-byte vector path, 2: 4-byte word path (K % 4 == 0, K <= 4096), 0: byte path
+int requant_path(const uint8_t* w, const int8_t* q, int64_t K);
 // MoE routing: top-k + softmax weights per token, stable counting sort into expert segments.
 size_t moe_route_workspace(int64_t T, int E, int topk);
 cudaError_t moe_route(const float* logits, int64_t T, int E, int topk, int32_t* ids, float* w, int64_t* seg,

@@ -75,32 +75,59 @@ route_topk_kernel(const float* __restrict__ logits, int64_t T, int E, int topk, 
   }
 }
 
+// The routed entries of one warp's range, kSortChunk / 32 per lane, all loaded before use so
+// that the range costs one memory round trip (-1 past the end).
+constexpr int kSortPerLane = kSortChunk / 32;
+__device__ __forceinline__ void load_range(const int32_t* __restrict__ ids, int64_t R, int64_t r0, int lane,
+                                           int (&id)[kSortPerLane]) {
+#pragma unroll
+  for (int j = 0; j < kSortPerLane; ++j) {
+    const int64_t i = r0 + 32 * j + lane;
+    id[j] = i < R ? ids[i] : -1;
+  }
+}
+
 // Pass 1: expert histogram of each warp's range of kSortChunk routed entries.
 __global__ void __launch_bounds__(32)
 route_hist_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int32_t* __restrict__ counts) {
   __shared__ int hist[256];
   const int lane = threadIdx.x;
+  int id[kSortPerLane];
+  load_range(ids, R, (int64_t)blockIdx.x * kSortChunk, lane, id);
   for (int e = lane; e < E; e += 32) hist[e] = 0;
   __syncwarp();
-  const int64_t r0 = (int64_t)blockIdx.x * kSortChunk;
-  for (int64_t i = r0 + lane; i < R && i < r0 + kSortChunk; i += 32) atomicAdd(&hist[ids[i]], 1);
+#pragma unroll
+  for (int j = 0; j < kSortPerLane; ++j)
+    if (id[j] >= 0) atomicAdd(&hist[id[j]], 1);
   __syncwarp();
   for (int e = lane; e < E; e += 32) counts[(int64_t)blockIdx.x * E + e] = hist[e];
 }
 
 // Pass 2 (one CTA, thread e = expert e): column prefix over the ranges (in place: counts[b][e]
-// becomes the number of expert-e entries before range b), then the segment offsets.
+// becomes the number of expert-e entries before range b), then the segment offsets.  The
+// [B, E] table is walked in tiles of 32 ranges, loaded and stored coalesced through shared
+// memory.
+constexpr int kScanTile = 32;
 __global__ void __launch_bounds__(256)
 route_scan_kernel(int32_t* __restrict__ counts, int64_t B, int E, int64_t* __restrict__ seg) {
-  __shared__ int64_t tot[257];
+  __shared__ int tile[kScanTile * 256];
+  __shared__ int64_t tot[256];
   const int e = threadIdx.x;
   int64_t run = 0;
-  if (e < E) {
-    for (int64_t b = 0; b < B; ++b) {
-      const int c = counts[b * E + e];
-      counts[b * E + e] = (int32_t)run;
-      run += c;
+  for (int64_t b0 = 0; b0 < B; b0 += kScanTile) {
+    const int nb = (int)(B - b0 < kScanTile ? B - b0 : kScanTile);
+    for (int i = threadIdx.x; i < nb * E; i += 256) tile[i] = counts[b0 * E + i];
+    __syncthreads();
+    if (e < E) {
+      for (int j = 0; j < nb; ++j) {
+        const int c = tile[j * E + e];
+        tile[j * E + e] = (int)run;
+        run += c;
+      }
     }
+    __syncthreads();
+    for (int i = threadIdx.x; i < nb * E; i += 256) counts[b0 * E + i] = tile[i];
+    __syncthreads();
   }
   tot[e] = e < E ? run : 0;
   __syncthreads();
@@ -123,19 +150,21 @@ route_scatter_kernel(const int32_t* __restrict__ ids, int64_t R, int E, int topk
                      int64_t* __restrict__ row_index, int64_t* __restrict__ row_of) {
   __shared__ int64_t next[256];
   const int lane = threadIdx.x;
+  const int64_t r0 = (int64_t)blockIdx.x * kSortChunk;
+  int id[kSortPerLane];
+  load_range(ids, R, r0, lane, id);
   for (int e = lane; e < E; e += 32) next[e] = seg[e] + counts[(int64_t)blockIdx.x * E + e];
   __syncwarp();
-  const int64_t r0 = (int64_t)blockIdx.x * kSortChunk;
   const uint32_t lt = (1u << lane) - 1u;
-  for (int64_t c0 = r0; c0 < R && c0 < r0 + kSortChunk; c0 += 32) {
-    const int64_t i = c0 + lane;
-    const bool valid = i < R && i < r0 + kSortChunk;
-    const int id = valid ? ids[i] : -1;
-    const uint32_t peers = __match_any_sync(0xffffffffu, id);
+#pragma unroll
+  for (int j = 0; j < kSortPerLane; ++j) {
+    const int64_t i = r0 + 32 * j + lane;
+    const bool valid = id[j] >= 0;
+    const uint32_t peers = __match_any_sync(0xffffffffu, id[j]);
     int64_t pos = 0;
-    if (valid) pos = next[id] + __popc(peers & lt);
+    if (valid) pos = next[id[j]] + __popc(peers & lt);
     __syncwarp();
-    if (valid && (peers & lt) == 0u) next[id] += __popc(peers);  // the lowest lane of each group
+    if (valid && (peers & lt) == 0u) next[id[j]] += __popc(peers);  // the lowest lane of each group
     __syncwarp();
     if (valid) {
       row_index[pos] = i / topk;

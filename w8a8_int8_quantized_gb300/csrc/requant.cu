@@ -85,12 +85,15 @@ __device__ __forceinline__ float block_factor(float sc, float r) {
   return (sc >= 0x1p-100f && c >= 0x1p-100f && c <= 0x1p100f) ? c : -1.f;
 }
 
-// 16 codes -> 16 int8 codes (see the note above); c < 0 takes the exact path for all 16.
-__device__ __forceinline__ uint4 requant_group(const uint4& cd, float c, const float* sc_ptr, float s) {
-  const uint32_t wd[4] = {cd.x, cd.y, cd.z, cd.w};
-  float f[16];
+// 4*NW codes (NW words) -> 4*NW int8 codes (see the note above); c < 0 takes the exact path
+// for all of them.
+template <int NW>
+__device__ __forceinline__ void requant_words(const uint32_t* wd, float c, const float* sc_ptr, float s,
+                                              uint32_t* out) {
+  constexpr int NV = 4 * NW;
+  float f[NV];
 #pragma unroll
-  for (int g = 0; g < 4; ++g) {
+  for (int g = 0; g < NW; ++g) {
     uint32_t h01, h23;
     e4m3x4_to_f16x4(wd[g], h01, h23);
     const __half2 a = *reinterpret_cast<const __half2*>(&h01), b = *reinterpret_cast<const __half2*>(&h23);
@@ -101,10 +104,10 @@ __device__ __forceinline__ uint4 requant_group(const uint4& cd, float c, const f
   }
   const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
   const uint64_t c2 = f2pack(c, c);
-  uint32_t bq[16];
+  uint32_t bq[NV];
   float emax = 0.f;
 #pragma unroll
-  for (int j = 0; j < 16; j += 2) {
+  for (int j = 0; j < NV; j += 2) {
     const uint64_t t = f2mul(f2pack(f[j], f[j + 1]), c2);
     const uint64_t m = f2add(t, kMagic);
     float e0, e1, m0, m1;
@@ -117,16 +120,21 @@ __device__ __forceinline__ uint4 requant_group(const uint4& cd, float c, const f
   if (!(emax < 0.49993896484375f) || c < 0.f) {  // 0.5 - 2^-14
     const float sc = *sc_ptr;
 #pragma unroll
-    for (int j = 0; j < 16; ++j) {
+    for (int j = 0; j < NV; ++j) {
       const float t = __fmul_rn(f[j], c);
       const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, 12582912.0f), 12582912.0f));
       if (c < 0.f || !(fabsf(e) < 0.49993896484375f))
         bq[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(__fmul_rn(f[j], sc), s)));
     }
   }
-  uint32_t out[4];
 #pragma unroll
-  for (int g = 0; g < 4; ++g) out[g] = pack4_i8_prmt(bq[4 * g], bq[4 * g + 1], bq[4 * g + 2], bq[4 * g + 3]);
+  for (int g = 0; g < NW; ++g) out[g] = pack4_i8_prmt(bq[4 * g], bq[4 * g + 1], bq[4 * g + 2], bq[4 * g + 3]);
+}
+
+__device__ __forceinline__ uint4 requant_group(const uint4& cd, float c, const float* sc_ptr, float s) {
+  const uint32_t wd[4] = {cd.x, cd.y, cd.z, cd.w};
+  uint32_t out[4];
+  requant_words<4>(wd, c, sc_ptr, s, out);
   return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
@@ -191,7 +199,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
 // batch's rows gw, gw + warps, ...; a row is brought in by one bulk copy (issued right after
 // the warp has finished the previous row), so many rows per SM are in flight while other
 // warps compute.  slot >= the largest K of the batch, a multiple of 128.
-template <int WARPS>
+template <int WARPS, bool ADJ>
 __global__ void __launch_bounds__(WARPS * 32, 1024 / (WARPS * 32))
 requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -236,15 +244,15 @@ requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
       for (int idx = lane; idx < nv; idx += 32) {
         const uint4 o = requant_group(rowv[idx], cb[idx >> 3], srow + (idx >> 3), s);
         qr[idx] = o;
-        if (mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
+        if (ADJ && mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
       }
     } else {
       for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (mt.adj) qsum = warp_sum_i(qsum);
+    if (ADJ && mt.adj) qsum = warp_sum_i(qsum);
     if (lane == 0) {
       mt.s[i] = s;
-      if (mt.adj) mt.adj[i] = qsum;
+      if (ADJ && mt.adj) mt.adj[i] = qsum;
       if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
     }
     __syncwarp();  // every lane is done with the slot (and with cb)
@@ -259,6 +267,9 @@ requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
 // Rows too long for a shared-memory slot: a warp streams its row from global memory twice
 // (the second pass mostly from L1/L2).
 constexpr int kReqStreamWarps = 8;
+constexpr int kReqWordWarps = 8;
+constexpr int kReqWordMaxK = 128 * 32;
+template <bool ADJ>
 __global__ void __launch_bounds__(kReqStreamWarps * 32)
 requant_stream_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
   const int lane = threadIdx.x & 31;
@@ -286,15 +297,15 @@ requant_stream_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
       for (int idx = lane; idx < nv; idx += 32) {
         const uint4 o = requant_group(wr[idx], block_factor(srow[idx >> 3], r), srow + (idx >> 3), s);
         qr[idx] = o;
-        if (mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
+        if (ADJ && mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
       }
     } else {
       for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
     }
-    if (mt.adj) qsum = warp_sum_i(qsum);
+    if (ADJ && mt.adj) qsum = warp_sum_i(qsum);
     if (lane == 0) {
       mt.s[i] = s;
-      if (mt.adj) mt.adj[i] = qsum;
+      if (ADJ && mt.adj) mt.adj[i] = qsum;
       if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
     }
   }
@@ -306,7 +317,7 @@ static size_t ring_smem(int warps, int slot) {
   return (size_t)warps * slot + (size_t)warps * (slot / 128) * 4 + (size_t)warps * 8;
 }
 
-template <int WARPS>
+template <int WARPS, bool ADJ>
 static cudaError_t launch_ring(const ReqBatch& b, int slot, int32_t* st, cudaStream_t stream) {
   static int s_dev = -1, s_sms = 0;
   static size_t s_attr = 0;
@@ -321,43 +332,134 @@ static cudaError_t launch_ring(const ReqBatch& b, int slot, int32_t* st, cudaStr
     s_attr = 0;
   }
   if (smem > s_attr) {
-    e = cudaFuncSetAttribute(requant_ring_kernel<WARPS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    e = cudaFuncSetAttribute(requant_ring_kernel<WARPS, ADJ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     s_attr = smem;
   }
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_ring_kernel<WARPS>, WARPS * 32, smem);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_ring_kernel<WARPS, ADJ>, WARPS * 32, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) per_sm = 1;
   const int64_t need = (b.total_rows + WARPS - 1) / WARPS;
   const int64_t cap = (int64_t)s_sms * per_sm;
-  requant_ring_kernel<WARPS><<<(unsigned)(need < cap ? need : cap), WARPS * 32, smem, stream>>>(b, slot, st);
+  requant_ring_kernel<WARPS, ADJ><<<(unsigned)(need < cap ? need : cap), WARPS * 32, smem, stream>>>(b, slot, st);
   return cudaGetLastError();
 }
 
+template <bool ADJ>
 static cudaError_t launch_vec(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
   int64_t kmax = 0;
   for (int k = 0; k < b.count; ++k) kmax = b.m[k].K > kmax ? b.m[k].K : kmax;
   const int slot = ring_slot(kmax);
   // slots of 16 warps up to 112 KB per CTA, so that two CTAs share an SM
-  if (ring_smem(16, slot) <= (size_t)112 * 1024) return launch_ring<16>(b, slot, st, stream);
-  if (ring_smem(8, slot) <= (size_t)112 * 1024) return launch_ring<8>(b, slot, st, stream);
-  if (ring_smem(4, slot) <= (size_t)200 * 1024) return launch_ring<4>(b, slot, st, stream);
+  if (ring_smem(16, slot) <= (size_t)112 * 1024) return launch_ring<16, ADJ>(b, slot, st, stream);
+  if (ring_smem(8, slot) <= (size_t)112 * 1024) return launch_ring<8, ADJ>(b, slot, st, stream);
+  if (ring_smem(4, slot) <= (size_t)200 * 1024) return launch_ring<4, ADJ>(b, slot, st, stream);
   static unsigned cached = 0;
   if (cached == 0) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
         cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_stream_kernel, kReqStreamWarps * 32, 0) !=
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_stream_kernel<ADJ>, kReqStreamWarps * 32, 0) !=
             cudaSuccess ||
         per_sm < 1)
       per_sm = 1;
     cached = (unsigned)((sms < 1 ? 1 : sms) * per_sm);
   }
   const int64_t need = (b.total_rows + kReqStreamWarps - 1) / kReqStreamWarps;
-  requant_stream_kernel<<<(unsigned)(need < (int64_t)cached ? need : (int64_t)cached), kReqStreamWarps * 32, 0,
+  requant_stream_kernel<ADJ><<<(unsigned)(need < (int64_t)cached ? need : (int64_t)cached), kReqStreamWarps * 32, 0,
                           stream>>>(b, st);
   return cudaGetLastError();
+}
+
+// Rows of K % 4 == 0 (K <= 128 * WPL) on 4-byte aligned but not 16-byte aligned storage
+// (e.g. K = 1500): a warp holds its row in registers as 32-bit words, word 32 j + l in lane l,
+// so a lane's j-th word lies in the row's 128-column block j.  The row absmax is then one warp
+// reduction of the per-lane maxima of RN(max|v| * sc_j), the codes are rewritten with the same
+// one-multiply rule as the vector path (exact fallback included), and each word is stored
+// back with one 4-byte store.
+template <int WPL, bool ADJ>
+__global__ void __launch_bounds__(kReqWordWarps * 32)
+requant_word_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
+  const int lane = threadIdx.x & 31;
+  const int64_t tw = (int64_t)gridDim.x * kReqWordWarps;
+  for (int64_t grow = (int64_t)blockIdx.x * kReqWordWarps + (threadIdx.x >> 5); grow < b.total_rows; grow += tw) {
+    const ReqMat& mt = find_mat(b, grow);
+    const int64_t i = grow - mt.row0;
+    const int K = mt.K, nw = K / 4, nbc = (K + 127) / 128;
+    const uint32_t* wr = reinterpret_cast<const uint32_t*>(mt.w + i * (int64_t)K);
+    const float* srow = mt.sinv + (i / 128) * nbc;
+    uint32_t v[WPL];
+#pragma unroll
+    for (int j = 0; j < WPL; ++j) {
+      const int w = 32 * j + lane;
+      v[j] = w < nw ? __ldg(wr + w) : 0u;  // code 0 (+0) past the end: no effect on the max
+    }
+    float amax = 0.f;
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < WPL; ++j) {
+      if (j < nbc) {
+        uint32_t h01, h23;
+        e4m3x4_to_f16x4(v[j], h01, h23);
+        amax = fmaxf(amax, block_amax(habsmax_nan(habsmax_nan(0u, h01), h23), srow[j], bad));
+      }
+    }
+    const float s = row_scale(amax, bad);
+    uint32_t* qr = reinterpret_cast<uint32_t*>(mt.q + i * (int64_t)K);
+    int qsum = 0;
+    if (!bad) {
+      const float r = __frcp_rn(s);
+#pragma unroll
+      for (int j = 0; j < WPL; ++j) {
+        const int w = 32 * j + lane;
+        if (w < nw) {
+          uint32_t o;
+          requant_words<1>(&v[j], block_factor(srow[j], r), srow + j, s, &o);
+          qr[w] = o;
+          if (ADJ && mt.adj) qsum = sum4_i8(o, qsum);
+        }
+      }
+    } else {
+#pragma unroll
+      for (int j = 0; j < WPL; ++j)
+        if (32 * j + lane < nw) qr[32 * j + lane] = 0u;
+    }
+    if (ADJ && mt.adj) qsum = warp_sum_i(qsum);
+    if (lane == 0) {
+      mt.s[i] = s;
+      if (ADJ && mt.adj) mt.adj[i] = qsum;
+      if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
+    }
+  }
+}
+
+template <int WPL, bool ADJ>
+static cudaError_t launch_word(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
+  static unsigned cached = 0;
+  if (cached == 0) {
+    int dev = 0, sms = 0, per_sm = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, requant_word_kernel<WPL, ADJ>, kReqWordWarps * 32,
+                                                      0) != cudaSuccess ||
+        per_sm < 1)
+      per_sm = 1;
+    cached = (unsigned)((sms < 1 ? 1 : sms) * per_sm);
+  }
+  const int64_t need = (b.total_rows + kReqWordWarps - 1) / kReqWordWarps;
+  requant_word_kernel<WPL, ADJ><<<(unsigned)(need < (int64_t)cached ? need : (int64_t)cached), kReqWordWarps * 32,
+                                  0, stream>>>(b, st);
+  return cudaGetLastError();
+}
+
+template <bool ADJ>
+static cudaError_t launch_words(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
+  int64_t kmax = 0;
+  for (int k = 0; k < b.count; ++k) kmax = b.m[k].K > kmax ? b.m[k].K : kmax;
+  if (kmax <= 128 * 4) return launch_word<4, ADJ>(b, st, stream);
+  if (kmax <= 128 * 12) return launch_word<12, ADJ>(b, st, stream);
+  return launch_word<32, ADJ>(b, st, stream);
 }
 
 // Any K and alignment: byte loads, two passes over the row.
@@ -416,19 +518,27 @@ cudaError_t requant_batch(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
   if (b.total_rows == 0) return cudaSuccess;
   // one launch per path: rows of vector matrices and rows of the others come in separate
   // row ranges of the two descriptor tables
-  ReqBatch vb, gb;
-  vb.count = gb.count = 0;
-  vb.pad = gb.pad = 0;
-  vb.total_rows = gb.total_rows = 0;
+  ReqBatch vb, wb, gb;
+  vb.count = wb.count = gb.count = 0;
+  vb.pad = wb.pad = gb.pad = 0;
+  vb.total_rows = wb.total_rows = gb.total_rows = 0;
   for (int k = 0; k < b.count; ++k) {
-    ReqBatch& t = b.m[k].vec ? vb : gb;
+    ReqBatch& t = b.m[k].vec == 1 ? vb : (b.m[k].vec == 2 ? wb : gb);
     t.m[t.count] = b.m[k];
-    t.m[t.count].row0 = t.total_rows;
+    t.m[t.count].row0 = (int32_t)t.total_rows;
     t.total_rows += b.m[k].N;
     ++t.count;
   }
   if (vb.total_rows > 0) {
-    cudaError_t e = launch_vec(vb, st, stream);
+    bool adj = false;
+    for (int k = 0; k < vb.count; ++k) adj |= vb.m[k].adj != nullptr;
+    cudaError_t e = adj ? launch_vec<true>(vb, st, stream) : launch_vec<false>(vb, st, stream);
+    if (e != cudaSuccess) return e;
+  }
+  if (wb.total_rows > 0) {
+    bool adj = false;
+    for (int k = 0; k < wb.count; ++k) adj |= wb.m[k].adj != nullptr;
+    cudaError_t e = adj ? launch_words<true>(wb, st, stream) : launch_words<false>(wb, st, stream);
     if (e != cudaSuccess) return e;
   }
   if (gb.total_rows > 0) {
@@ -550,9 +660,11 @@ cudaError_t requant_max_scale(int8_t* wq, int64_t units, const float* scales, co
   return cudaGetLastError();
 }
 
-bool requant_vec_ok(const uint8_t* w, const int8_t* q, int64_t K) {
-  return (K % 16 == 0) &&
-         ((reinterpret_cast<uintptr_t>(w) & 15) == 0) && ((reinterpret_cast<uintptr_t>(q) & 15) == 0);
+int requant_path(const uint8_t* w, const int8_t* q, int64_t K) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(w) | reinterpret_cast<uintptr_t>(q);
+  if (K % 16 == 0 && (a & 15) == 0) return 1;
+  if (K % 4 == 0 && K <= kReqWordMaxK && (a & 3) == 0) return 2;
+  return 0;
 }
 
 }  // namespace w8a8
