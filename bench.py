@@ -200,7 +200,7 @@ def run_ours(args, world, rank, pg):
                 e1.record()
             rc |= lib.w8a8_scaled_mm_packed(P(L["packed"].data_ptr()), P(L["wq"].data_ptr()), M_TOKENS, L["N"],
                                             L["K"], 0, P(L["sx"].data_ptr()), None, None, 0,
-                                            P(L["sw"].data_ptr()), None, P(L["y"].data_ptr()), None, sptr)
+                                            P(L["sw"].data_ptr()), None, None, P(L["y"].data_ptr()), None, sptr)
             if record:
                 e2.record()
                 L.setdefault("ev", []).append((e0, e1, e2))
@@ -466,10 +466,11 @@ def components(w8, wl, peaks):
     for M in (128, 4096):
         x = wl.asym_activations(M, 4096, seed=3).to(dev)
         w = torch.randn(4096, 4096, device=dev).mul_(0.02).to(torch.bfloat16)
-        wq, sw, adj = w8.quantize_weight(w, with_azp_adj=True)
+        wq, sw, adj, wsq = w8.quantize_weight(w, with_azp_adj=True, with_sumsq=True)
         ws = torch.empty(w8.linear_workspace_size(M, 4096, "dyn_asym"), dtype=torch.uint8, device=dev)
         yb = torch.empty(M, 4096, dtype=torch.bfloat16, device=dev)
-        ms = _time_launches(lambda: w8.linear(x, wq, sw, act_mode="dyn_asym", azp_adj=adj, workspace=ws, out=yb))
+        ms = _time_launches(lambda: w8.linear(x, wq, sw, act_mode="dyn_asym", azp_adj=adj, workspace=ws, out=yb,
+                                              w_sumsq=wsq))
         out[f"linear_dyn_asym_M{M}_4096x4096"] = {"us": round(ms * 1e3, 2),
                                                   "TOPS": round(2 * M * 4096 * 4096 / (ms * 1e-3) / 1e12, 1)}
     # small-M (weight streaming) linears on the gate_up shape

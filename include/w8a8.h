@@ -104,12 +104,19 @@ w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, 
  *             STATIC_ASYM      s_x float [1]; azp_adj int32 [N] premultiplied by the
  *                              input zero point; zp unused.
  *   w_mode  W8A8_W_CHANNEL: s_w float [N];  W8A8_W_TENSOR: s_w float [1].
+ *   w_sumsq int32 [N] = sum_k wq[n,k]^2 (w8a8_weight_sumsq / w8a8_quantize_weight), or NULL.
+ *           Optional, results do not depend on it: with an asymmetric act_mode, the
+ *           tensor-core engine may then finish more tiles in one exact fp32 pass.  Each
+ *           partial sum is at most ||x_m||_2 * ||w_n||_2, and a tile is exact in fp32 when
+ *           that stays below 2^24.  Without it, the test is 127 * L1(x_m) < 2^24 alone;
+ *           affine codes usually fail that test and their tiles then accumulate in 1024-K
+ *           chunks.  Ignored for symmetric modes.
  *   bias    bf16 [N] or NULL.
  *   y       bf16 [M, N] contiguous (output).
  *   workspace  device scratch of at least w8a8_scaled_mm_workspace_size(M, K) bytes,
  *              256-byte aligned (the tensor-core engine stages the activations there as
- *              fp16 integer codes with their row L1 norms).  May be NULL only when the
- *              warp-MMA engine runs (M <= 16 under automatic selection).
+ *              fp16 integer codes with their row L1 norms and sums of squares).  May be
+ *              NULL only when the warp-MMA engine runs (M <= 16 under automatic selection).
  * Epilogue, float32 with one rounding per step and no fused multiply-add:
  *   c = acc - zp[m]*azp_adj[n] (exact integer, rounded to float32);
  *   y = bf16_rne( (s_x[m]*s_w[n]) * c (+ bias[n]) ).
@@ -122,13 +129,13 @@ size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t K);
 w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
                            int act_mode, const float* s_x, const int32_t* zp,
                            const int32_t* azp_adj, int w_mode, const float* s_w,
-                           const void* bias, void* y, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, cudaStream_t stream);
+                           const int32_t* w_sumsq, const void* bias, void* y, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
 /*
  * w8a8_linear -- the whole layer forward: quantize x (any act_mode) then w8a8_scaled_mm
  * ([SGLang-CT] item 3 apply_weights; [vLLM-W8A8] 4.2 apply_weights(layer, x, bias)).
- *   x bf16 [M, K] (row stride ldx); wq/s_w/azp_adj/bias as for w8a8_scaled_mm.
+ *   x bf16 [M, K] (row stride ldx); wq/s_w/azp_adj/w_sumsq/bias as for w8a8_scaled_mm.
  *   input_scale / input_zero_point: float [1] / int32 [1] for the static modes, else NULL.
  *   workspace: device buffer of at least w8a8_linear_workspace_size(M, K, act_mode) bytes,
  *   256-byte aligned; it holds the quantized activations (in the format the selected GEMM
@@ -138,7 +145,7 @@ size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode);
 w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int act_mode,
                         const float* input_scale, const int32_t* input_zero_point,
                         const int8_t* wq, int64_t N, int w_mode, const float* s_w,
-                        const int32_t* azp_adj, const void* bias, void* y,
+                        const int32_t* azp_adj, const int32_t* w_sumsq, const void* bias, void* y,
                         void* workspace, size_t workspace_bytes,
                         int32_t* dev_status, cudaStream_t stream);
 
@@ -149,9 +156,21 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
  * q = clamp(round(W/s), -127, 127), all-zero row -> q = 0, s = 1).
  *   w bf16 [N, K] contiguous;  wq int8 [N, K] (output);  s_w float [N] (output);
  *   azp_adj int32 [N] (optional output, NULL to skip): sum_k wq[n, k] ([SGLang-CT] item 4).
+ *   w_sumsq int32 [N] (optional output, NULL to skip): sum_k wq[n, k]^2 (see
+ *   w8a8_weight_sumsq).
  */
 w8a8_status w8a8_quantize_weight(const void* w, int64_t N, int64_t K, int8_t* wq, float* s_w,
-                                 int32_t* azp_adj, cudaStream_t stream);
+                                 int32_t* azp_adj, int32_t* w_sumsq, cudaStream_t stream);
+
+/*
+ * w8a8_weight_sumsq -- w_sumsq[n] = sum_k wq[n, k]^2 (int32, exact for K <= 131072) of an
+ * already-quantized weight, the optional operand of the GEMM entry points that lets them
+ * prove more tiles exact in one fp32 pass (Cauchy-Schwarz; see w8a8_scaled_mm).  The pages
+ * have no counterpart: it is this engine's exactness bookkeeping, computed once per weight
+ * like azp_adj.  wq int8 [N, K] (device); w_sumsq int32 [N] (device, 4-byte aligned).
+ */
+w8a8_status w8a8_weight_sumsq(const int8_t* wq, int64_t N, int64_t K, int32_t* w_sumsq,
+                              cudaStream_t stream);
 
 /*
  * w8a8_azp_adj -- azp_adj[n] = input_zero_point * sum_k wq[n, k] for an int8 weight that
@@ -298,7 +317,8 @@ w8a8_status w8a8_moe_combine(const void* out, const int64_t* row_of, const float
  * which tells the GEMM whether a single fp32 pass over K is provably exact.  The "packed"
  * entry points produce and consume that format in one caller buffer of
  * w8a8_act_packed_size(M, K) bytes (256-byte aligned): fp16 codes [M, K] row-major, then
- * int32 norms [M] at byte offset roundup(M*K*2, 256).  The codes are the same integers the
+ * int32 row L1 norms [M] at byte offset roundup(M*K*2, 256), immediately followed by the
+ * int32 row sums of squares [M] of the codes (written by the asymmetric modes only).  The codes are the same integers the
  * int8 entry points produce; only their storage differs.  w8a8_linear runs
  * w8a8_quantize_act_packed followed by w8a8_scaled_mm_packed (for M > 16).
  * K % 16 == 0 for every packed entry point.
@@ -313,8 +333,8 @@ w8a8_status w8a8_quantize_act_packed(const void* x, int64_t M, int64_t K, int64_
 w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t M, int64_t N,
                                   int64_t K, int act_mode, const float* s_x, const int32_t* zp,
                                   const int32_t* azp_adj, int w_mode, const float* s_w,
-                                  const void* bias, void* y, int32_t* dev_status,
-                                  cudaStream_t stream);
+                                  const int32_t* w_sumsq, const void* bias, void* y,
+                                  int32_t* dev_status, cudaStream_t stream);
 
 /* w8a8_grouped_mm reading packed activations. */
 w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const int8_t* w,
@@ -340,7 +360,7 @@ w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void
  *   no workspace: the activations are staged in a 36 MiB buffer owned by the library (a
  *   device array placed in GPU memory when the library's module is loaded on a device and
  *   kept until the process exits).  It always runs the tensor-core engine.
- *   Limit: roundup(M*K*2, 256) + roundup(M*4, 256) <= 36 MiB (e.g. M*K up to 4096 x 4096);
+ *   Limit: roundup(M*K*2, 256) + roundup(M*8, 256) <= 36 MiB (e.g. M*K up to 4096 x 4096);
  *   larger problems return W8A8_ERR_WORKSPACE before any launch.
  *   The first call on each device looks up the buffer's device address (no allocation) and
  *   caches it; make that first call before any stream capture.

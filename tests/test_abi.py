@@ -64,24 +64,27 @@ def test_host_side_argument_checks_need_no_gpu(libpath):
     """Argument errors are returned before any CUDA call, so they work on a GPU-less host."""
     lib = _binding.lib()
     # K not a multiple of 16
-    assert lib.w8a8_scaled_mm(None, None, 4, 4, 24, 0, None, None, None, 0, None, None, None, None, 0, None,
+    assert lib.w8a8_scaled_mm(None, None, 4, 4, 24, 0, None, None, None, 0, None, None, None, None, None, 0, None,
                               None) == 3
     # negative sizes / bad mode
     assert lib.w8a8_quantize_act(None, -1, 4, 4, 0, None, None, None, None) == 1
     assert lib.w8a8_quantize_act(None, 1, 4, 4, 9, None, None, None, None) == 1
     # empty problems are no-ops
     assert lib.w8a8_quantize_act(None, 0, 4, 4, 0, None, None, None, None) == 0
-    assert lib.w8a8_scaled_mm(None, None, 0, 4, 16, 0, None, None, None, 0, None, None, None, None, 0, None,
+    assert lib.w8a8_scaled_mm(None, None, 0, 4, 16, 0, None, None, None, 0, None, None, None, None, None, 0, None,
                               None) == 0
     # asymmetric GEMM without azp_adj
     p = ctypes.c_void_p(16)
-    assert lib.w8a8_scaled_mm(p, p, 4, 4, 16, 1, p, p, None, 0, p, None, p, None, 0, None, None) == 1
+    assert lib.w8a8_scaled_mm(p, p, 4, 4, 16, 1, p, p, None, 0, p, None, None, p, None, 0, None, None) == 1
     # the tensor-core engine needs its staging workspace
-    assert lib.w8a8_scaled_mm(p, p, 64, 4, 16, 0, p, None, None, 0, p, None, p, None, 0, None, None) == 7
-    assert lib.w8a8_scaled_mm_workspace_size(64, 16) == 2048 + 256
+    assert lib.w8a8_scaled_mm(p, p, 64, 4, 16, 0, p, None, None, 0, p, None, None, p, None, 0, None, None) == 7
+    assert lib.w8a8_scaled_mm_workspace_size(64, 16) == 2048 + 512  # codes, then 2 * 64 int32 row sums
     assert lib.w8a8_act_packed_size(3, 32) == 256 + 256
     # workspace too small
-    assert lib.w8a8_linear(p, 4, 16, 16, 0, None, None, p, 4, 0, p, None, None, p, p, 8, None, None) == 7
+    assert lib.w8a8_linear(p, 4, 16, 16, 0, None, None, p, 4, 0, p, None, None, None, p, p, 8, None, None) == 7
+    # weight sums of squares: negative sizes are argument errors, empty weights no-ops
+    assert lib.w8a8_weight_sumsq(p, -1, 16, p, None) == 1
+    assert lib.w8a8_weight_sumsq(None, 0, 16, None, None) == 0
     assert lib.w8a8_linear_workspace_size(4, 16, 0) == 256 + 256 + 2 * 256
     # max-scale requantization: widths must sum to N, 1 <= P <= 16
     w2 = (ctypes.c_int64 * 2)(3, 4)

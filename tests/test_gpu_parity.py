@@ -161,7 +161,8 @@ def test_quantize_act_static(M, K):
 @pytest.mark.parametrize("mode", ["dyn_sym", "dyn_asym", "static_sym", "static_asym"])
 @pytest.mark.parametrize("M,K", [(16, 512), (37, 4096), (3, 14336)])
 def test_quantize_act_packed(mode, M, K):
-    """The packed format holds the same integer codes as fp16, plus each row's L1 norm."""
+    """The packed format holds the same integer codes as fp16, plus each row's L1 norm (and, for
+    the affine modes, its sum of squares)."""
     x = (wl.asym_activations if "asym" in mode else wl.llama_activations)(M, K, seed=M + 3)
     if M > 2:
         x[2] = 0
@@ -184,6 +185,8 @@ def test_quantize_act_packed(mode, M, K):
     codes = pa.codes().float().cpu().numpy()
     np.testing.assert_array_equal(codes, rq.astype(np.float32))
     np.testing.assert_array_equal(pa.norms().cpu().numpy(), np.abs(rq.astype(np.int64)).sum(1))
+    if "asym" in mode:  # the affine modes also carry each row's sum of squares
+        np.testing.assert_array_equal(pa.sumsq().cpu().numpy(), (rq.astype(np.int64) ** 2).sum(1))
     if rs is not None:
         np.testing.assert_array_equal(pa.scale.cpu().numpy(), rs)
 
@@ -657,3 +660,61 @@ def test_moe_route_feeds_moe_forward():
                            s2.view(E, H).cpu().numpy())
     np.testing.assert_array_equal(npbits(h), r["h_bits"])
     check_bf16(y, r["y_bits"], oracle.bf16_bits_to_f32(r["y_bits"]), exact=False)
+
+
+
+@pytest.mark.parametrize("act", ["dyn_asym", "static_asym"])
+@pytest.mark.parametrize("M", [300, 4096])
+def test_asym_linear_cauchy_schwarz(act, M):
+    """Affine codes of nonzero-mean rows at K = 4096 have L1 norms above 2^17, so without the
+    weight's sums of squares every tile runs the chunked mode; with them the Cauchy-Schwarz
+    bound admits single-pass tiles.  Both must equal the oracle bit for bit (M = 4096 on
+    sampled rows)."""
+    N, K = 520, 4096
+    d = _gemm_case(M, N, K, seed=M + 17, act=act)
+    xs = d["x"].float().numpy()
+    sc, z = oracle.static_scale_from_tensor(xs)
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    kw = {}
+    if act == "dyn_asym":
+        kw["azp_adj"] = w8.azp_adj(wq)
+    else:
+        kw["input_scale"] = torch.tensor([sc], dtype=torch.float32, device=DEV)
+        kw["input_zero_point"] = torch.tensor([z], dtype=torch.int32, device=DEV)
+        kw["azp_adj"] = w8.azp_adj(wq, kw["input_zero_point"])
+    wsq = w8.weight_sumsq(wq)
+    np.testing.assert_array_equal(wsq.cpu().numpy(), (d["rq"].astype(np.int64) ** 2).sum(1))
+    x = d["x"].to(DEV)
+    y_cs = w8.linear(x, wq, sw, act_mode=act, bias=d["b"].to(DEV), w_sumsq=wsq, **kw)
+    y_l1 = w8.linear(x, wq, sw, act_mode=act, bias=d["b"].to(DEV), **kw)
+    assert torch.equal(y_cs, y_l1)
+    rows = np.arange(M) if M <= 300 else np.concatenate([np.arange(0, M, 97), [M - 1]])
+    r = oracle.w8a8_linear(d["xb"][rows], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]), mode=act,
+                           input_scale=sc, input_zero_point=z)
+    check_bf16(y_cs[torch.from_numpy(rows).to(DEV)], r["y_bits"], r["y32"])
+
+
+@pytest.mark.parametrize("qv,wv,cs_ok", [(40, 20, True), (127, 127, False), (-90, 31, True)])
+def test_gemm_cauchy_schwarz_bound_exact(qv, wv, cs_ok):
+    """Rows of |q| = qv over K = 4096 have L1 norm 4096 qv >= 2^17, so only the Cauchy-Schwarz
+    test (K qv^2 * K wv^2 < 2^48) can make their tiles single pass; signs are chosen so that
+    every product in a row/column pair has the same sign (the largest partial sums the bound
+    allows).  (127, 127) fails both tests and runs chunked.  All exact."""
+    M, N, K = 256, 512, 4096
+    assert (K * qv * qv) * (K * wv * wv) < 2 ** 48 if cs_ok else (K * qv * qv) * (K * wv * wv) >= 2 ** 48
+    rng = np.random.default_rng(abs(qv) + wv)
+    sx = rng.choice([-1, 1], size=(M, 1)).astype(np.int64)
+    sk = rng.choice([-1, 1], size=(1, K)).astype(np.int64)
+    sn = rng.choice([-1, 1], size=(N, 1)).astype(np.int64)
+    xq = (qv * sx * sk).astype(np.int8)
+    wq = (wv * sn * sk).astype(np.int8)
+    xq[7, :100] = 0  # a row of smaller norm in the same tile
+    s_x = np.full(M, 2.0 ** -10, np.float32)
+    s_w = np.full(N, 2.0 ** -12, np.float32)
+    wq_d = torch.from_numpy(wq).to(DEV)
+    y = w8.scaled_mm(torch.from_numpy(xq).to(DEV), wq_d, torch.from_numpy(s_x).to(DEV), torch.from_numpy(s_w).to(DEV),
+                     "dyn_sym", w_sumsq=w8.weight_sumsq(wq_d))
+    acc = oracle.int8_gemm(xq, wq)
+    yb, y32 = oracle.scaled_mm_epilogue(acc, s_x, s_w)
+    check_bf16(y, yb, y32)

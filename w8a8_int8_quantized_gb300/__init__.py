@@ -39,5 +39,6 @@ from ._binding import (  # noqa: F401
     requantize_max_scale,
     scaled_mm,
     set_gemm_engine,
+    weight_sumsq,
     silu_mul_quant,
 )

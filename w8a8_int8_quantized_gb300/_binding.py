@@ -35,10 +35,11 @@ SIGNATURES = {
     "w8a8_set_gemm_engine": (_I, [_I]),
     "w8a8_quantize_act": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
     "w8a8_scaled_mm_workspace_size": (_SZ, [_I64, _I64]),
-    "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _SZ, _P, _P]),
+    "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "w8a8_linear_workspace_size": (_SZ, [_I64, _I64, _I]),
-    "w8a8_linear": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
-    "w8a8_quantize_weight": (_I, [_P, _I64, _I64, _P, _P, _P, _P]),
+    "w8a8_linear": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
+    "w8a8_quantize_weight": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
+    "w8a8_weight_sumsq": (_I, [_P, _I64, _I64, _P, _P]),
     "w8a8_azp_adj": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "fp8block_to_int8_rowwise": (_I, [_P, _P, _I64, _I64, _P, _P, _P, _P]),
     "fp8block_to_int8_rowwise_batched": (_I, [_I, _P, _P, _P, _P, _P, _P, _P, _P]),
@@ -53,7 +54,7 @@ SIGNATURES = {
     "w8a8_moe_combine": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _P]),
     "w8a8_act_packed_size": (_SZ, [_I64, _I64]),
     "w8a8_quantize_act_packed": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
-    "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
+    "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_gather_packed": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     "w8a8_silu_mul_quant_packed": (_I, [_P, _I64, _I64, _P, _P, _P]),
@@ -145,7 +146,7 @@ def _workspace(nbytes, device, given):
 
 
 def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mode=W_CHANNEL, bias=None,
-              out=None, status=None, workspace=None):
+              out=None, status=None, workspace=None, w_sumsq=None):
     """y[M, N] bf16 = epilogue(xq @ wq.T) (see w8a8_scaled_mm in include/w8a8.h)."""
     _need(xq, torch.int8, "xq", 2)
     _need(wq, torch.int8, "wq", 2)
@@ -157,8 +158,8 @@ def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mod
         out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
     ws = _workspace(lib().w8a8_scaled_mm_workspace_size(M, K), xq.device, workspace)
     code = lib().w8a8_scaled_mm(_ptr(xq), _ptr(wq), M, N, K, _mode(act_mode), _ptr(s_x), _ptr(zp), _ptr(azp_adj),
-                                int(w_mode), _ptr(s_w), _ptr(bias), _ptr(out), _ptr(ws), ws.numel(), _ptr(status),
-                                _stream())
+                                int(w_mode), _ptr(s_w), _ptr(w_sumsq), _ptr(bias), _ptr(out), _ptr(ws), ws.numel(),
+                                _ptr(status), _stream())
     _check("w8a8_scaled_mm", code)
     return out
 
@@ -168,7 +169,7 @@ def linear_workspace_size(M, K, act_mode="dyn_sym"):
 
 
 def linear(x, wq, s_w, act_mode="dyn_sym", input_scale=None, input_zero_point=None, azp_adj=None, bias=None,
-           w_mode=W_CHANNEL, workspace=None, out=None, status=None):
+           w_mode=W_CHANNEL, workspace=None, out=None, status=None, w_sumsq=None):
     """Whole W8A8 linear: y = epilogue(quant(x) @ wq.T)."""
     _need(x, torch.bfloat16, "x", 2)
     _need(wq, torch.int8, "wq", 2)
@@ -179,22 +180,32 @@ def linear(x, wq, s_w, act_mode="dyn_sym", input_scale=None, input_zero_point=No
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     code = lib().w8a8_linear(_ptr(x), M, K, K, m, _ptr(input_scale), _ptr(input_zero_point), _ptr(wq), N,
-                             int(w_mode), _ptr(s_w), _ptr(azp_adj), _ptr(bias), _ptr(out), _ptr(workspace),
-                             workspace.numel(), _ptr(status), _stream())
+                             int(w_mode), _ptr(s_w), _ptr(azp_adj), _ptr(w_sumsq), _ptr(bias), _ptr(out),
+                             _ptr(workspace), workspace.numel(), _ptr(status), _stream())
     _check("w8a8_linear", code)
     return out
 
 
-def quantize_weight(w, with_azp_adj=False):
-    """Per-channel symmetric int8 weight.  Returns (wq, s_w[, azp_adj])."""
+def quantize_weight(w, with_azp_adj=False, with_sumsq=False):
+    """Per-channel symmetric int8 weight.  Returns (wq, s_w[, azp_adj][, w_sumsq])."""
     _need(w, torch.bfloat16, "w", 2)
     N, K = w.shape
     wq = torch.empty((N, K), dtype=torch.int8, device=w.device)
     s = torch.empty(N, dtype=torch.float32, device=w.device)
     adj = torch.empty(N, dtype=torch.int32, device=w.device) if with_azp_adj else None
-    _check("w8a8_quantize_weight", lib().w8a8_quantize_weight(_ptr(w), N, K, _ptr(wq), _ptr(s), _ptr(adj),
+    sq = torch.empty(N, dtype=torch.int32, device=w.device) if with_sumsq else None
+    _check("w8a8_quantize_weight", lib().w8a8_quantize_weight(_ptr(w), N, K, _ptr(wq), _ptr(s), _ptr(adj), _ptr(sq),
                                                               _stream()))
-    return (wq, s, adj) if with_azp_adj else (wq, s)
+    return (wq, s) + ((adj,) if with_azp_adj else ()) + ((sq,) if with_sumsq else ())
+
+
+def weight_sumsq(wq):
+    """int32 [N] row sums of squares of an int8 weight (the GEMM's optional w_sumsq)."""
+    _need(wq, torch.int8, "wq", 2)
+    N, K = wq.shape
+    out = torch.empty(N, dtype=torch.int32, device=wq.device)
+    _check("w8a8_weight_sumsq", lib().w8a8_weight_sumsq(_ptr(wq), N, K, _ptr(out), _stream()))
+    return out
 
 
 def azp_adj(wq, input_zero_point=None):
@@ -352,10 +363,11 @@ def moe_combine(out_rows, row_of, topk_w):
 
 
 class PackedActivations:
-    """Quantized activations in the tensor-core engine's format (fp16 codes + row L1 norms).
+    """Quantized activations in the tensor-core engine's format (fp16 codes, row L1 norms and,
+    for the affine modes, row sums of squares).
 
     buf: uint8 CUDA tensor of w8a8_act_packed_size(M, K) bytes; scale / zp as produced by the
-    quantizer.  codes() and norms() are views for inspection.
+    quantizer.  codes(), norms() and sumsq() are views for inspection.
     """
 
     def __init__(self, buf, M, K, scale, zp=None):
@@ -366,6 +378,10 @@ class PackedActivations:
 
     def norms(self):
         off = (self.M * self.K * 2 + 255) // 256 * 256
+        return self.buf[off: off + 4 * self.M].view(torch.int32)
+
+    def sumsq(self):
+        off = (self.M * self.K * 2 + 255) // 256 * 256 + 4 * self.M
         return self.buf[off: off + 4 * self.M].view(torch.int32)
 
 
@@ -392,15 +408,15 @@ def quantize_act_packed(x, mode="dyn_sym", scale=None, zp=None, buf=None):
 
 
 def scaled_mm_packed(pa, wq, s_w, act_mode="dyn_sym", azp_adj=None, w_mode=W_CHANNEL, bias=None, out=None,
-                     status=None):
+                     status=None, w_sumsq=None):
     """y = epilogue(A @ wq.T) with A given as PackedActivations (scales taken from it)."""
     _need(wq, torch.int8, "wq", 2)
     N = wq.shape[0]
     if out is None:
         out = torch.empty((pa.M, N), dtype=torch.bfloat16, device=wq.device)
     code = lib().w8a8_scaled_mm_packed(_ptr(pa.buf), _ptr(wq), pa.M, N, pa.K, _mode(act_mode), _ptr(pa.scale),
-                                       _ptr(pa.zp), _ptr(azp_adj), int(w_mode), _ptr(s_w), _ptr(bias), _ptr(out),
-                                       _ptr(status), _stream())
+                                       _ptr(pa.zp), _ptr(azp_adj), int(w_mode), _ptr(s_w), _ptr(w_sumsq), _ptr(bias),
+                                       _ptr(out), _ptr(status), _stream())
     _check("w8a8_scaled_mm_packed", code)
     return out
 

@@ -41,8 +41,9 @@ bool use_small_engine(int64_t rows, bool dense) { return g_engine == 2 || (g_eng
 
 size_t a256(size_t v) { return (v + 255) & ~(size_t)255; }
 
-// Workspace of the tcgen05 engine: fp16 activation codes, then their row L1 norms.
-size_t ready_bytes(int64_t rows, int64_t K) { return a256((size_t)rows * (size_t)K * 2) + a256((size_t)rows * 4); }
+// Workspace of the tcgen05 engine: fp16 activation codes, then their row L1 norms [rows] and
+// row sums of squares [rows] (one region of 2 * rows int32).
+size_t ready_bytes(int64_t rows, int64_t K) { return a256((size_t)rows * (size_t)K * 2) + a256((size_t)rows * 8); }
 
 w8a8_status run_gemm(GemmArgs g, cudaStream_t st, void* ws, bool small, bool a_is_ready) {
   cudaError_t e;
@@ -122,8 +123,8 @@ size_t w8a8_scaled_mm_workspace_size(int64_t M, int64_t K) {
 
 w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K, int act_mode,
                            const float* s_x, const int32_t* zp, const int32_t* azp_adj, int w_mode,
-                           const float* s_w, const void* bias, void* y, void* workspace, size_t workspace_bytes,
-                           int32_t* dev_status, cudaStream_t stream) {
+                           const float* s_w, const int32_t* w_sumsq, const void* bias, void* y, void* workspace,
+                           size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
   w8a8_status s = check_scaled_mm_args(xq, wq, M, N, K, act_mode, s_x, zp, azp_adj, w_mode, s_w, bias, y);
   if (s != W8A8_OK || M == 0 || N == 0) return s;
   const bool small = use_small_engine(M, true);
@@ -145,6 +146,7 @@ w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_
   g.zp = zp;
   g.azp = azp_adj;
   g.s_w = s_w;
+  g.wsq = w_sumsq;
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
@@ -159,8 +161,9 @@ size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode) {
 
 w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int act_mode, const float* input_scale,
                         const int32_t* input_zero_point, const int8_t* wq, int64_t N, int w_mode,
-                        const float* s_w, const int32_t* azp_adj, const void* bias, void* y, void* workspace,
-                        size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+                        const float* s_w, const int32_t* azp_adj, const int32_t* w_sumsq, const void* bias,
+                        void* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                        cudaStream_t stream) {
   if (M < 0 || N < 0 || K < 1 || K > kMaxK || !valid_act_mode(act_mode) || !valid_w_mode(w_mode))
     return W8A8_ERR_INVALID_ARG;
   if (K % 16 != 0) return W8A8_ERR_MISALIGNED;
@@ -206,6 +209,7 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
   g.zp = zp;
   g.azp = azp_adj;
   g.s_w = s_w;
+  g.wsq = w_sumsq;
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
@@ -213,15 +217,27 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
 }
 
 w8a8_status w8a8_quantize_weight(const void* w, int64_t N, int64_t K, int8_t* wq, float* s_w, int32_t* azp_adj,
-                                 cudaStream_t stream) {
+                                 int32_t* w_sumsq, cudaStream_t stream) {
   if (N < 0 || K < 0) return W8A8_ERR_INVALID_ARG;
   if (N == 0 || K == 0) return W8A8_OK;
   if (!w || !wq || !s_w || K > kMaxK || N > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
   if (!aligned(w, 2)) return W8A8_ERR_MISALIGNED;
   w8a8_status s = check_device();
   if (s != W8A8_OK) return s;
-  return cuda_status(
-      quant_rows(W8A8_ACT_DYN_TOKEN_SYM, w, N, K, K, nullptr, wq, nullptr, s_w, nullptr, azp_adj, nullptr, stream));
+  cudaError_t e =
+      quant_rows(W8A8_ACT_DYN_TOKEN_SYM, w, N, K, K, nullptr, wq, nullptr, s_w, nullptr, azp_adj, nullptr, stream);
+  if (e == cudaSuccess && w_sumsq) e = sumsq_rows(wq, N, K, w_sumsq, stream);
+  return cuda_status(e);
+}
+
+w8a8_status w8a8_weight_sumsq(const int8_t* wq, int64_t N, int64_t K, int32_t* w_sumsq, cudaStream_t stream) {
+  if (N < 0 || K < 0 || K > kMaxK || N > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;
+  if (N == 0) return W8A8_OK;
+  if (!w_sumsq || (K > 0 && !wq)) return W8A8_ERR_INVALID_ARG;
+  if (!aligned(w_sumsq, 4)) return W8A8_ERR_MISALIGNED;
+  w8a8_status s = check_device();
+  if (s != W8A8_OK) return s;
+  return cuda_status(sumsq_rows(wq, N, K, w_sumsq, stream));
 }
 
 w8a8_status w8a8_azp_adj(const int8_t* wq, int64_t N, int64_t K, const int32_t* input_zero_point, int32_t* azp_adj,
@@ -442,8 +458,8 @@ w8a8_status w8a8_quantize_act_packed(const void* x, int64_t M, int64_t K, int64_
 
 w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t M, int64_t N, int64_t K, int act_mode,
                                   const float* s_x, const int32_t* zp, const int32_t* azp_adj, int w_mode,
-                                  const float* s_w, const void* bias, void* y, int32_t* dev_status,
-                                  cudaStream_t stream) {
+                                  const float* s_w, const int32_t* w_sumsq, const void* bias, void* y,
+                                  int32_t* dev_status, cudaStream_t stream) {
   const int8_t* dummy = static_cast<const int8_t*>(packed);
   w8a8_status s = check_scaled_mm_args(dummy, wq, M, N, K, act_mode, s_x, zp, azp_adj, w_mode, s_w, bias, y);
   if (s != W8A8_OK || M == 0 || N == 0) return s;
@@ -462,6 +478,7 @@ w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t 
   g.zp = zp;
   g.azp = azp_adj;
   g.s_w = s_w;
+  g.wsq = w_sumsq;
   g.bias = bias;
   g.y = y;
   g.status = dev_status;

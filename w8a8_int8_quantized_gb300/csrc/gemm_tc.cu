@@ -276,12 +276,20 @@ struct KParams {
   int E;
   const int64_t* seg;
   const int32_t* norms;  // [rows] sum_k |a[r, k]|
+  const int32_t* asq;    // [rows] sum_k a[r, k]^2, or null (dense GEMMs with weight squares only)
+  const int32_t* wsq;    // [N] sum_k w[n, k]^2, or null
   EpiParams ep;
   __nv_bfloat16* y;
   int32_t* status;
 };
 
 // Whether the pair tile starting at row0 can run single pass (warp-wide, all lanes agree).
+// Every partial sum of the fp32 accumulation is an integer bounded by sum_k |a_k| |w_k|, so
+// the pass is exact when that bound stays below 2^24.  Two bounds: 127 * (row L1 norm), i.e.
+// a norm below 2^17; or, when the row and weight sums of squares are known (asymmetric
+// activations with the weight's squares given), Cauchy-Schwarz: ||a||_2 ||w||_2 < 2^24,
+// tested exactly as max_rows(sum a^2) * max_cols(sum w^2) < 2^48 in 64-bit integers.  The
+// second is only evaluated when the first fails.
 __device__ __forceinline__ bool tile_single_pass(const KParams& p, const Tile& tl, int lane) {
   int32_t mx = 0;
 #pragma unroll
@@ -291,7 +299,24 @@ __device__ __forceinline__ bool tile_single_pass(const KParams& p, const Tile& t
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = max(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-  return mx < kNormSingle;
+  if (mx < kNormSingle || !p.asq) return mx < kNormSingle;
+  int32_t mq = 0, mw = 0;
+#pragma unroll
+  for (int j = 0; j < BM / 32; ++j) {
+    const int64_t r = tl.row0 + lane + 32 * j;
+    if (r < tl.row_end) mq = max(mq, p.asq[r]);
+  }
+#pragma unroll
+  for (int j = 0; j < BN / 32; ++j) {
+    const int64_t n = tl.n0 + lane + 32 * j;
+    if (n < p.N) mw = max(mw, p.wsq[n]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    mq = max(mq, __shfl_xor_sync(0xffffffffu, mq, o));
+    mw = max(mw, __shfl_xor_sync(0xffffffffu, mw, o));
+  }
+  return (uint64_t)(uint32_t)mq * (uint64_t)(uint32_t)mw < (1ull << 48);
 }
 
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
@@ -665,12 +690,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   }
 }
 
-// int8 -> fp16 integer codes and row L1 norms (the GEMM-ready activation format)
+// int8 -> fp16 integer codes, row L1 norms and row sums of squares (the GEMM-ready
+// activation format: norms[row], then norms[gridDim.x + row] for the squares)
 __global__ void __launch_bounds__(256)
 to_gemm_ready_kernel(const int8_t* __restrict__ a, int64_t K, __half* __restrict__ a16, int32_t* __restrict__ norms) {
-  __shared__ int sh[8];
+  __shared__ int sh[8], sh2[8];
   const int64_t row = blockIdx.x;
-  int s = 0;
+  int s = 0, s2 = 0;
   const int8_t* ar = a + row * K;
   __half* hr = a16 + row * K;
   for (int64_t i = threadIdx.x; i < K / 16; i += 256) {
@@ -682,17 +708,28 @@ to_gemm_ready_kernel(const int8_t* __restrict__ a, int64_t K, __half* __restrict
       i8x4_to_f16x4(w[j], o[2 * j], o[2 * j + 1]);
 #pragma unroll
       for (int b = 0; b < 4; ++b) s += abs((int)(int8_t)(w[j] >> (8 * b)));
+      s2 = __dp4a((int)w[j], (int)w[j], s2);
     }
     reinterpret_cast<uint4*>(hr)[2 * i] = make_uint4(o[0], o[1], o[2], o[3]);
     reinterpret_cast<uint4*>(hr)[2 * i + 1] = make_uint4(o[4], o[5], o[6], o[7]);
   }
-  for (int o = 16; o > 0; o >>= 1) s += __shfl_xor_sync(0xffffffffu, s, o);
-  if ((threadIdx.x & 31) == 0) sh[threadIdx.x >> 5] = s;
+  for (int o = 16; o > 0; o >>= 1) {
+    s += __shfl_xor_sync(0xffffffffu, s, o);
+    s2 += __shfl_xor_sync(0xffffffffu, s2, o);
+  }
+  if ((threadIdx.x & 31) == 0) {
+    sh[threadIdx.x >> 5] = s;
+    sh2[threadIdx.x >> 5] = s2;
+  }
   __syncthreads();
   if (threadIdx.x == 0) {
-    int t = 0;
-    for (int i = 0; i < 8; ++i) t += sh[i];
+    int t = 0, t2 = 0;
+    for (int i = 0; i < 8; ++i) {
+      t += sh[i];
+      t2 += sh2[i];
+    }
     norms[row] = t;
+    norms[gridDim.x + row] = t2;
   }
 }
 
@@ -765,6 +802,11 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   p.E = g.E;
   p.seg = g.seg;
   p.norms = g.norms;
+  // the squares follow the L1 norms in the activation format, written for the asymmetric
+  // modes (whose affine codes usually fail the L1 test); dense GEMMs only
+  const bool asym = g.act_mode == W8A8_ACT_DYN_TOKEN_ASYM || g.act_mode == W8A8_ACT_STATIC_TENSOR_ASYM;
+  p.asq = (!g.seg && g.wsq && asym) ? g.norms + g.rows : nullptr;
+  p.wsq = p.asq ? g.wsq : nullptr;
   p.ep.act_mode = g.act_mode;
   p.ep.w_mode = g.w_mode;
   p.ep.s_x = g.s_x;

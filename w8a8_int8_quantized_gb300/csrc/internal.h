@@ -18,6 +18,7 @@ cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t
                        int32_t* sum_out, int32_t* norm_out, cudaStream_t st);
 cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, int32_t* out,
                      cudaStream_t st);
+cudaError_t sumsq_rows(const int8_t* w, int64_t N, int64_t K, int32_t* out, cudaStream_t st);
 // gq: int8 codes, or g16 + norms: the packed (fp16 codes + row L1 norms) format
 cudaError_t silu_mul_quant(const void* h, int64_t R, int64_t I, int8_t* gq, void* g16, int32_t* norms, float* sg,
                            cudaStream_t st);
@@ -78,6 +79,8 @@ struct GemmArgs {
   const int32_t* zp;
   const int32_t* azp;
   const float* s_w;     // [E*N] (channel) or [1] (tensor)
+  const int32_t* wsq;   // [N] sum_k w[n, k]^2 (dense only, optional): admits single-pass tiles
+                        // by the Cauchy-Schwarz bound
   const void* bias;     // [N] or nullptr
   void* y;              // [rows, N] bf16
   int32_t* status;

@@ -66,7 +66,8 @@ extern "C" w8a8_status w8a8_scaled_mm_noalloc(const int8_t* xq, const int8_t* wq
   if (((reinterpret_cast<uintptr_t>(xq) | reinterpret_cast<uintptr_t>(wq) | reinterpret_cast<uintptr_t>(y)) & 15) != 0)
     return W8A8_ERR_MISALIGNED;
   const size_t codes_bytes = round256((size_t)M * (size_t)K * 2);
-  if (codes_bytes + round256((size_t)M * 4) > kNoallocScratchBytes) return W8A8_ERR_WORKSPACE;
+  // codes, then the row L1 norms and sums of squares (2 * M int32) that the conversion writes
+  if (codes_bytes + round256((size_t)M * 8) > kNoallocScratchBytes) return W8A8_ERR_WORKSPACE;
   int dev = -1, major = 0, minor = 0;
   if (cudaGetDevice(&dev) != cudaSuccess ||
       cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

@@ -114,18 +114,20 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
 // of q (weight azp_adj).
 // ---------------------------------------------------------------------------
 template <int MODE, int THREADS, int NV, bool F16, bool SUM>
-__global__ void __launch_bounds__(THREADS)
+__global__ void __launch_bounds__(THREADS, THREADS >= 512 ? 2 : 0)
 quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int64_t ldx,
                const int64_t* __restrict__ row_index, int8_t* __restrict__ q, __half* __restrict__ q16,
                float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out,
                int32_t* __restrict__ norm_out) {
   constexpr int W = THREADS / 32;
   constexpr bool DYN = (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM);
+  // row sums of squares of the codes (the GEMM's Cauchy-Schwarz test) for the affine modes only
+  constexpr bool SQ = F16 && (MODE == W8A8_ACT_DYN_TOKEN_ASYM || MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
   // One CTA barrier per row: per-warp partials go to a double-buffered shared array, so a
   // warp may start writing row k+1's partials while slower warps still read row k's; the
   // row sums of row k (SUM / F16) are completed behind row k+1's barrier.
   __shared__ float sh_lo[2][W], sh_hi[2][W];
-  __shared__ int sh_sum[2][W], sh_abs[2][W];
+  __shared__ int sh_sum[2][W], sh_abs[2][W], sh_sq[2][W];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = (int)(K / 8);
   // Persistent: this CTA quantizes rows blockIdx.x, + gridDim.x, ...; the next row's loads
@@ -143,14 +145,16 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
     }
   };
   auto finish_sums = [&](int b, int64_t r) {
-    int s = 0, a = 0;
+    int s = 0, a = 0, q2 = 0;
 #pragma unroll
     for (int i = 0; i < W; ++i) {
       if (SUM) s += sh_sum[b][i];
       if (F16) a += sh_abs[b][i];
+      if (SQ) q2 += sh_sq[b][i];
     }
     if (SUM) sum_out[r] = s;
-    if (F16) norm_out[r] = a;
+    if (F16) norm_out[r] = a;         // L1 norm of the codes
+    if (SQ) norm_out[rows + r] = q2;  // sum of their squares, right after the rows' L1 norms
   };
   if (row < rows) load_row(row, nxt);
   for (; row < rows; row += gridDim.x, buf ^= 1) {
@@ -231,7 +235,7 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       const float tmax = __fmul_rn(fmaxf(fabsf(rq_lo), fabsf(rq_hi)), r);
       thr = __fsub_rd(0.5f, __fmul_rn(tmax, 0x1p-21f));
     }
-    int qsum = 0, qabs = 0;
+    int qsum = 0, qabs = 0, qsq = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int idx = threadIdx.x + i * THREADS;
@@ -265,6 +269,7 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
         }
         if (SUM) qsum = sum4_i8(w1, sum4_i8(w0, qsum));
         if (F16) qabs = abssum4_i8(w1, abssum4_i8(w0, qabs));
+        if (SQ) qsq = __dp4a((int)w1, (int)w1, __dp4a((int)w0, (int)w0, qsq));
         if (F16) {
           uint4 o;
           i8x4_to_f16x4(w0, o.x, o.y);
@@ -284,10 +289,12 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       for (int o = 16; o > 0; o >>= 1) {
         if (SUM) qsum += __shfl_xor_sync(0xffffffffu, qsum, o);
         if (F16) qabs += __shfl_xor_sync(0xffffffffu, qabs, o);
+        if (SQ) qsq += __shfl_xor_sync(0xffffffffu, qsq, o);
       }
       if (lane == 0) {
         sh_sum[buf][warp] = qsum;
         sh_abs[buf][warp] = qabs;
+        if (SQ) sh_sq[buf][warp] = qsq;
       }
       prev = row;
     }
@@ -345,13 +352,14 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
     rq.zp = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM) ? zp[0] : 0;
     rq.affine = (MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
   }
-  int qsum = 0, qabs = 0;
+  int qsum = 0, qabs = 0, qsq = 0;
   for (int64_t k = threadIdx.x; k < K; k += THREADS) {
     const int c = apply_rq(rq, __bfloat162float(xr[k]));
     if (q16) q16[row * K + k] = __int2half_rn(c);
     else q[row * K + k] = (int8_t)c;
     qsum += c;
     qabs += abs(c);
+    qsq += c * c;
   }
   if (threadIdx.x == 0) {
     if (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM) scale[row] = rq.s;
@@ -364,6 +372,8 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
   if (norm_out) {
     const int tot = block_reduce_sum_i<THREADS>(qabs, shi);
     if (threadIdx.x == 0) norm_out[row] = tot;
+    const int tot2 = block_reduce_sum_i<THREADS>(qsq, shi);
+    if (threadIdx.x == 0) norm_out[gridDim.x + row] = tot2;  // one CTA per row: gridDim.x rows
   }
 }
 
@@ -438,7 +448,9 @@ cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t
 // ---------------------------------------------------------------------------
 // azp_adj[n] = zp * sum_k wq[n, k] for an already-quantized weight.
 // ---------------------------------------------------------------------------
-template <int THREADS>
+// Per-row sums of int8 codes (azp_adj, optionally times a zero point) or of their squares (SQ:
+// the weight side of the GEMM's Cauchy-Schwarz exactness bound).
+template <int THREADS, bool SQ>
 __global__ void __launch_bounds__(THREADS)
 row_sum_i8(const int8_t* __restrict__ w, int64_t K, const int32_t* __restrict__ zp,
            int32_t* __restrict__ out) {
@@ -452,18 +464,23 @@ row_sum_i8(const int8_t* __restrict__ w, int64_t K, const int32_t* __restrict__ 
       const uint4 u = v[i];
       const uint32_t wd[4] = {u.x, u.y, u.z, u.w};
 #pragma unroll
-      for (int j = 0; j < 4; ++j) s = __dp4a((int)wd[j], 0x01010101, s);
+      for (int j = 0; j < 4; ++j) s = __dp4a((int)wd[j], SQ ? (int)wd[j] : 0x01010101, s);
     }
   } else {
-    for (int64_t k = threadIdx.x; k < K; k += THREADS) s += wr[k];
+    for (int64_t k = threadIdx.x; k < K; k += THREADS) s += SQ ? (int)wr[k] * (int)wr[k] : (int)wr[k];
   }
   s = block_reduce_sum_i<THREADS>(s, shi);
-  if (threadIdx.x == 0) out[row] = zp ? s * zp[0] : s;
+  if (threadIdx.x == 0) out[row] = (!SQ && zp) ? s * zp[0] : s;
 }
 
 cudaError_t azp_rows(const int8_t* w, int64_t N, int64_t K, const int32_t* zp, int32_t* out,
                      cudaStream_t st) {
-  row_sum_i8<256><<<(unsigned)N, 256, 0, st>>>(w, K, zp, out);
+  row_sum_i8<256, false><<<(unsigned)N, 256, 0, st>>>(w, K, zp, out);
+  return cudaGetLastError();
+}
+
+cudaError_t sumsq_rows(const int8_t* w, int64_t N, int64_t K, int32_t* out, cudaStream_t st) {
+  row_sum_i8<256, true><<<(unsigned)N, 256, 0, st>>>(w, K, nullptr, out);
   return cudaGetLastError();
 }
 
