@@ -15,6 +15,11 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
                  2^17, so their tiles run the 1024-K chunked mode
   small          w8a8_linear at M=16 (warp-MMA engine), N=28672, K=4096
   moe            the MoE layer: 4096 tokens, 32 experts, top-4
+  moe_routed     the same layer behind w8a8_moe_route (router logits in, every step on the GPU)
+  route          w8a8_moe_route alone: 4096 tokens, 32 experts, top-4
+  requant_word   fp8block_to_int8_rowwise_batched over 8 x [3000, 1500] (rows on 4-byte words)
+  max_scale      w8a8_requantize_max_scale on a fused q/k/v weight [4096+1024+1024, 4096]
+  asym_linear    w8a8_linear, dynamic asymmetric, M=N=K=4096, with the weight's sums of squares
 
 Every case uses a few GB of device memory at most, so a profiler capture of one launch
 stays small.
@@ -91,6 +96,41 @@ def case_fn(name):
         args = (x, order // k, seg, row_of.view(T, k), tw, w13q.view(E, 2 * inter, H), s13.view(E, 2 * inter),
                 w2q.view(E, H, inter), s2.view(E, H))
         return lambda: w8.moe_forward(*args)
+    if name in ("moe_routed", "route"):
+        T, H, E, k, inter = 4096, 4096, 32, 4, 1408
+        logits = wl.moe_workload(T=T, H=64, E=E, topk=k, inter=64, seed=0, with_weights=False)["logits"].to(dev)
+        ws = torch.empty(max(int(w8.lib().w8a8_moe_route_workspace_size(T, E, k)), 4), dtype=torch.uint8, device=dev)
+        if name == "route":
+            return lambda: w8.moe_route(logits, k, workspace=ws)
+        x = _bf16((T, H), 1.0, 11)
+        w13q, s13 = w8.quantize_weight(_bf16((E * 2 * inter, H), 0.02, 12))
+        w2q, s2 = w8.quantize_weight(_bf16((E * H, inter), 0.02, 13))
+
+        def layer():
+            ids, tw, seg, row_index, row_of = w8.moe_route(logits, k, workspace=ws)
+            return w8.moe_forward(x, row_index, seg, row_of, tw, w13q.view(E, 2 * inter, H), s13.view(E, 2 * inter),
+                                  w2q.view(E, H, inter), s2.view(E, H))
+        return layer
+    if name == "requant_word":
+        g = _gen(14)
+        mats = []
+        for _ in range(8):
+            c = torch.randn(3000, 1500, device=dev, generator=g).to(torch.float8_e4m3fn).view(torch.uint8)
+            s = torch.exp(torch.empty(24, 12, device=dev).uniform_(math.log(1e-4), math.log(1e-2), generator=g))
+            mats.append((c, s))
+        outs = [(torch.empty(c.shape, dtype=torch.int8, device=dev), torch.empty(c.shape[0], device=dev))
+                for c, _ in mats]
+        return lambda: w8.fp8block_to_int8_rowwise_batched(mats, outs)
+    if name == "max_scale":
+        wq = torch.randint(-127, 128, (6144, 4096), dtype=torch.int8, device=dev, generator=_gen(15))
+        sc = torch.tensor([1.1e-3, 1.7e-3, 1.3e-3], dtype=torch.float32, device=dev)
+        return lambda: w8.requantize_max_scale(wq, sc, [4096, 1024, 1024])
+    if name == "asym_linear":
+        x = wl.asym_activations(4096, 4096, seed=16).to(dev)
+        wq, sw, adj, wsq = w8.quantize_weight(_bf16((4096, 4096), 0.02, 17), with_azp_adj=True, with_sumsq=True)
+        ws = torch.empty(w8.linear_workspace_size(4096, 4096, "dyn_asym"), dtype=torch.uint8, device=dev)
+        y = torch.empty(4096, 4096, dtype=torch.bfloat16, device=dev)
+        return lambda: w8.linear(x, wq, sw, act_mode="dyn_asym", azp_adj=adj, w_sumsq=wsq, workspace=ws, out=y)
     raise SystemExit(f"unknown case {name}")
 
 
