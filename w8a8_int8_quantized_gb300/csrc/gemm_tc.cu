@@ -278,6 +278,7 @@ struct KParams {
   const int32_t* norms;  // [rows] sum_k |a[r, k]|
   const int32_t* asq;    // [rows] sum_k a[r, k]^2, or null (dense GEMMs with weight squares only)
   const int32_t* wsq;    // [N] sum_k w[n, k]^2, or null
+  int az_small;          // 127 * K < 2^22: every azp_adj = sum_k w[n, k] is below 2^22 in magnitude
   EpiParams ep;
   __nv_bfloat16* y;
   int32_t* status;
@@ -604,10 +605,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                   const int4 z0 = __ldg(reinterpret_cast<const int4*>(ep.azp + n0 + 8 * j));
                   const int4 z1 = __ldg(reinterpret_cast<const int4*>(ep.azp + n0 + 8 * j + 4));
                   const int az[8] = {z0.x, z0.y, z0.z, z0.w, z1.x, z1.y, z1.z, z1.w};
+                  // acc, zp and azp_adj are exact floats here: one fma forms f32(acc - zp * azp)
+                  // with a single rounding.  azp_adj below 2^22 converts exactly by adding it
+                  // into the mantissa of 1.5 * 2^23 (integer add, float subtract) instead of a
+                  // conversion instruction per output.
+                  if (zp_exact && p.az_small) {
 #pragma unroll
-                  for (int i = 0; i < 8; ++i)
-                    cf[i] = zp_exact ? __fmaf_rn(-zpf, __int2float_rn(az[i]), cf[i])
-                                     : __ll2float_rn((long long)cf[i] - (long long)zpm * (long long)az[i]);
+                    for (int i = 0; i < 8; ++i)
+                      cf[i] = __fmaf_rn(-zpf, __fsub_rn(__int_as_float(az[i] + 0x4B400000), 12582912.0f), cf[i]);
+                  } else if (zp_exact) {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i) cf[i] = __fmaf_rn(-zpf, __int2float_rn(az[i]), cf[i]);
+                  } else {
+#pragma unroll
+                    for (int i = 0; i < 8; ++i)
+                      cf[i] = __ll2float_rn((long long)cf[i] - (long long)zpm * (long long)az[i]);
+                  }
                 }
                 float f[8];
 #pragma unroll
@@ -807,6 +820,7 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   const bool asym = g.act_mode == W8A8_ACT_DYN_TOKEN_ASYM || g.act_mode == W8A8_ACT_STATIC_TENSOR_ASYM;
   p.asq = (!g.seg && g.wsq && asym) ? g.norms + g.rows : nullptr;
   p.wsq = p.asq ? g.wsq : nullptr;
+  p.az_small = 127 * g.K < (int64_t(1) << 22) ? 1 : 0;
   p.ep.act_mode = g.act_mode;
   p.ep.w_mode = g.w_mode;
   p.ep.s_x = g.s_x;
