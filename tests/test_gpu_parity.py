@@ -718,3 +718,24 @@ def test_gemm_cauchy_schwarz_bound_exact(qv, wv, cs_ok):
     acc = oracle.int8_gemm(xq, wq)
     yb, y32 = oracle.scaled_mm_epilogue(acc, s_x, s_w)
     check_bf16(y, yb, y32)
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 520, 4112), (3, 5000, 4096), (8, 300, 64), (8, 1000, 11200), (5, 4104, 4096)])
+def test_decode_linear_fused_quant(M, N, K):
+    """Decode linears (dynamic symmetric, at most 8 rows) quantize inside the small-M GEMM:
+    bf16 outputs equal the oracle's quantizer + GEMM + epilogue bit for bit, including a zero
+    row and rows built on exact and near ties of x / s."""
+    d = _gemm_case(M, N, K, seed=M * 31 + K)
+    x = d["x"].clone()
+    if M >= 3:
+        x[1] = 0
+        ties = _sym_tie_rows(K)
+        x[2] = ties[2 % ties.shape[0]]
+    if M >= 5:
+        x[4] = ties[0]
+    xb = wl.bits(x)
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    y = w8.linear(x.to(DEV), wq, sw, bias=d["b"].to(DEV))
+    r = oracle.w8a8_linear(xb, d["rq"], d["rs"], bias_bits=wl.bits(d["b"]))
+    check_bf16(y, r["y_bits"], r["y32"])

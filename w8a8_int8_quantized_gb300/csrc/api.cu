@@ -181,6 +181,22 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
   w8a8_status s = check_device();
   if (s != W8A8_OK) return s;
   const bool small = use_small_engine(M, true);
+  if (small && act_mode == W8A8_ACT_DYN_TOKEN_SYM && gemm_small_m_fused_ok(M, K) && aligned(x, 16) && ldx % 8 == 0) {
+    // decode: the quantizer runs inside the small-M GEMM (no separate launch)
+    GemmArgs g{};
+    g.w = wq;
+    g.rows = M;
+    g.N = N;
+    g.K = K;
+    g.E = 1;
+    g.act_mode = act_mode;
+    g.w_mode = w_mode;
+    g.s_w = s_w;
+    g.bias = bias;
+    g.y = y;
+    g.status = dev_status;
+    return cuda_status(gemm_small_m_fused(x, ldx, g, stream));
+  }
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   size_t off = ready_bytes(M, K);
   float* sx = const_cast<float*>(input_scale);

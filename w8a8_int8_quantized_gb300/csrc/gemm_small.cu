@@ -243,6 +243,172 @@ gemm_small_m_xs_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__
   asm volatile("cp.async.wait_all;\n" ::: "memory");  // warps that read no chunk still own copies
 }
 
+// Decode launches of dynamic per-token symmetric activations with the quantizer fused in
+// (at most 8 bf16 token rows whose codes fit the 96 KB shared-memory copy): every CTA
+// quantizes the rows itself, straight into its shared-memory copy, with the stand-alone
+// quantizer's exact row rule (s = RN(absmax / 127), or 1 for a zero row; codes
+// rint(RN(x / s)) from the division-free rounding with exact near-tie resolution).  This
+// takes the separate quantizer launch and its int8 round trip through memory off a decode
+// step.  The first round of weight loads is issued before the quantization so that it
+// overlaps the row reads.
+__global__ void __launch_bounds__(kSmWarps * 32)
+gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const int8_t* __restrict__ wq,
+                       int64_t rows, int64_t N, int64_t K, EpiParams ep, __nv_bfloat16* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t xs[];
+  __shared__ int red[kSmWarps][16][17];
+  __shared__ float sh_amax[kSmWarps][8];
+  __shared__ float sh_s[8], sh_r[8];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, tq = lane & 3;
+  const int nr = (int)rows;  // <= 8
+  const int64_t ld = xs_stride(K);
+  const int64_t nchunks = (K + 63) / 64;
+  const int64_t nbn = (N + 15) / 16;
+  const int nvec = (int)(K / 8);
+  auto load_round = [&](int64_t nb, int64_t c0, uint4 (&wa)[kXsUnroll][2]) {
+    const int64_t n0 = nb * 16;
+    const bool wr0 = (n0 + g) < N, wr1 = (n0 + g + 8) < N;
+    const int8_t* pw0 = wq + (n0 + g) * K;
+    const int8_t* pw1 = wq + (n0 + g + 8) * K;
+#pragma unroll
+    for (int u = 0; u < kXsUnroll; ++u) {
+      const int64_t c = c0 + (int64_t)u * kSmWarps;
+      const int64_t kb = c * 64 + tq * 16;
+      const bool kin = (c < nchunks) && (kb < K);
+      wa[u][0] = ld16_stream_or_zero(pw0 + kb, kin && wr0);
+      wa[u][1] = ld16_stream_or_zero(pw1 + kb, kin && wr1);
+    }
+  };
+  uint4 wa[kXsUnroll][2];
+  bool preloaded = false;
+  if ((int64_t)blockIdx.x < nbn) {
+    load_round(blockIdx.x, warp, wa);
+    preloaded = true;
+  }
+  // row absmax (exact: a max of exact values), one CTA reduction for all rows
+  float am[8];
+#pragma unroll
+  for (int r = 0; r < 8; ++r) {
+    am[r] = 0.f;
+    if (r < nr) {
+      const uint4* xr = reinterpret_cast<const uint4*>(x + r * ldx);
+      for (int c = threadIdx.x; c < nvec; c += kSmWarps * 32) {
+        const uint4 v = __ldg(xr + c);
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int k = 0; k < 4; ++k) am[r] = fmaxf(am[r], fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) am[r] = fmaxf(am[r], __shfl_xor_sync(0xffffffffu, am[r], o));
+  }
+  if (lane == 0) {
+#pragma unroll
+    for (int r = 0; r < 8; ++r) sh_amax[warp][r] = am[r];
+  }
+  __syncthreads();
+  if (threadIdx.x < 8) {
+    float a = 0.f;
+#pragma unroll
+    for (int w = 0; w < kSmWarps; ++w) a = fmaxf(a, sh_amax[w][threadIdx.x]);
+    const float sc = (a == 0.f) ? 1.f : __fdiv_rn(a, 127.f);
+    sh_s[threadIdx.x] = sc;
+    sh_r[threadIdx.x] = __frcp_rn(sc);
+  }
+  __syncthreads();
+  // codes into the shared-memory copy (|x| <= absmax: every code within +-127)
+  for (int r = 0; r < nr; ++r) {
+    const float sc = sh_s[r], rc = sh_r[r];
+    const uint4* xr = reinterpret_cast<const uint4*>(x + r * ldx);
+    for (int c = threadIdx.x; c < nvec; c += kSmWarps * 32) {
+      const uint4 v = __ldg(xr + c);
+      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+      float f[8];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        f[2 * k] = bf16_lo(w[k]);
+        f[2 * k + 1] = bf16_hi(w[k]);
+      }
+      uint32_t b[8];
+      quant_row_group_x2<8>(f, sc, rc, b);
+      *reinterpret_cast<uint2*>(xs + r * ld + (int64_t)c * 8) =
+          make_uint2(pack4_i8_prmt(b[0], b[1], b[2], b[3]), pack4_i8_prmt(b[4], b[5], b[6], b[7]));
+    }
+  }
+  __syncthreads();
+  const bool xr0 = g < nr;
+  const uint8_t* sx0 = xs + g * ld;
+  for (int64_t nb = blockIdx.x; nb < nbn; nb += gridDim.x) {
+    const int64_t n0 = nb * 16;
+    int acc0[2][4] = {};
+    for (int64_t c0 = warp; c0 < nchunks; c0 += (int64_t)kSmWarps * kXsUnroll) {
+      if (!preloaded) load_round(nb, c0, wa);
+      preloaded = false;
+#pragma unroll
+      for (int u = 0; u < kXsUnroll; ++u) {
+        const int64_t c = c0 + (int64_t)u * kSmWarps;
+        const int64_t kb = c * 64 + tq * 16;
+        const bool kin = (c < nchunks) && (kb < K);
+        const uint4 x0 = (kin && xr0) ? *reinterpret_cast<const uint4*>(sx0 + kb) : make_uint4(0, 0, 0, 0);
+        const uint32_t A0[4] = {wa[u][0].x, wa[u][0].y, wa[u][0].z, wa[u][0].w};
+        const uint32_t A1[4] = {wa[u][1].x, wa[u][1].y, wa[u][1].z, wa[u][1].w};
+        const uint32_t B0[4] = {x0.x, x0.y, x0.z, x0.w};
+#pragma unroll
+        for (int j = 0; j < 2; ++j)
+          mma_s8_16832(acc0[j], A0[2 * j], A1[2 * j], A0[2 * j + 1], A1[2 * j + 1], B0[2 * j], B0[2 * j + 1]);
+      }
+    }
+    preloaded = false;  // a warp with no chunk in the first block discards its preload
+    red[warp][g][2 * tq] = acc0[0][0] + acc0[1][0];
+    red[warp][g][2 * tq + 1] = acc0[0][1] + acc0[1][1];
+    red[warp][g + 8][2 * tq] = acc0[0][2] + acc0[1][2];
+    red[warp][g + 8][2 * tq + 1] = acc0[0][3] + acc0[1][3];
+    __syncthreads();
+    const int tok = threadIdx.x >> 4, ch = threadIdx.x & 15;
+    const int64_t n = n0 + ch;
+    if (tok < nr && n < N) {
+      int sum = 0;
+#pragma unroll
+      for (int w = 0; w < kSmWarps; ++w) sum += red[w][ch][tok];
+      y[tok * N + n] = __float2bfloat16_rn(epi_apply(ep, sum, sh_s[tok], 0, n));
+    }
+    __syncthreads();  // red is rewritten by the next block
+  }
+}
+
+bool gemm_small_m_fused_ok(int64_t rows, int64_t K) { return rows == 1 && xs_stride(K) <= 96 * 1024; }
+
+cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cudaStream_t st) {
+  EpiParams ep;
+  ep.act_mode = W8A8_ACT_DYN_TOKEN_SYM;
+  ep.w_mode = g.w_mode;
+  ep.s_x = nullptr;
+  ep.zp = nullptr;
+  ep.azp = nullptr;
+  ep.s_w = g.s_w;
+  ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
+  static int s_dev = -1, s_grid = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != s_dev) {
+    e = cudaFuncSetAttribute(gemm_small_m_fq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    s_grid = 2 * sms;
+    s_dev = dev;
+  }
+  const int64_t gx = (g.N + 15) / 16;
+  const unsigned grid = (unsigned)(gx < s_grid ? gx : s_grid);
+  const size_t xs_bytes = (size_t)(g.rows * xs_stride(g.K));
+  gemm_small_m_fq_kernel<<<grid, kSmWarps * 32, xs_bytes, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, g.w,
+                                                                g.rows, g.N, g.K, ep,
+                                                                static_cast<__nv_bfloat16*>(g.y));
+  return cudaGetLastError();
+}
+
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st) {
   EpiParams ep;
   ep.act_mode = g.act_mode;

@@ -88,6 +88,10 @@ struct GemmArgs {
 
 // gemm_small.cu: mma.sync s8 weight-streaming kernel (small M)
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st);
+// Dynamic per-token symmetric decode (at most 8 bf16 rows x) with the quantizer fused into the
+// small-M GEMM; g carries the weight side and the output (g.a, g.s_x unused).
+bool gemm_small_m_fused_ok(int64_t rows, int64_t K);
+cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cudaStream_t st);
 // gemm_tc.cu: tcgen05 kernel; returns cudaErrorNotSupported when it cannot run
 cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st);
 // int8 codes -> fp16 codes + row L1 norms (K % 16 == 0, 16-byte aligned rows)
