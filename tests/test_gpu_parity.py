@@ -739,3 +739,23 @@ def test_decode_linear_fused_quant(M, N, K):
     y = w8.linear(x.to(DEV), wq, sw, bias=d["b"].to(DEV))
     r = oracle.w8a8_linear(xb, d["rq"], d["rs"], bias_bits=wl.bits(d["b"]))
     check_bf16(y, r["y_bits"], r["y32"])
+
+
+@pytest.mark.parametrize("kind", ["normal", "zero", "tie_s1", "tie_near", "tie_small"])
+@pytest.mark.parametrize("N,K", [(520, 4112), (300, 64), (1000, 11200)])
+def test_decode_linear_fused_single_row(kind, N, K):
+    """A single token row takes the fused quantizer + small-M GEMM: bit-exact against the
+    oracle for ordinary, zero and tie-heavy rows (exact ties with s = 1, bf16 near-ties with
+    s = RN(100/127), values around +-s/2 and +-3s/2)."""
+    d = _gemm_case(1, N, K, seed=K + N)
+    x = d["x"].clone()
+    ties = _sym_tie_rows(K)
+    if kind == "zero":
+        x[0] = 0
+    elif kind != "normal":
+        x[0] = ties[{"tie_s1": 0, "tie_near": 2, "tie_small": 3}[kind]]
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    y = w8.linear(x.to(DEV), wq, sw, bias=d["b"].to(DEV))
+    r = oracle.w8a8_linear(wl.bits(x), d["rq"], d["rs"], bias_bits=wl.bits(d["b"]))
+    check_bf16(y, r["y_bits"], r["y32"])
