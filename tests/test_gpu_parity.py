@@ -759,3 +759,16 @@ def test_decode_linear_fused_single_row(kind, N, K):
     y = w8.linear(x.to(DEV), wq, sw, bias=d["b"].to(DEV))
     r = oracle.w8a8_linear(wl.bits(x), d["rq"], d["rs"], bias_bits=wl.bits(d["b"]))
     check_bf16(y, r["y_bits"], r["y32"])
+
+
+@pytest.mark.parametrize("bias", [True, False])
+def test_decode_linear_fused_tensor_scale(bias):
+    """The fused single-row path with a per-tensor weight scale, with and without bias."""
+    N, K = 1000, 4096
+    d = _gemm_case(1, N, K, seed=77, bias=bias, w_mode=w8.W_TENSOR)
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    b = d["b"].to(DEV) if bias else None
+    y = w8.linear(d["x"].to(DEV), wq, sw, bias=b, w_mode=w8.W_TENSOR)
+    r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]) if bias else None)
+    check_bf16(y, r["y_bits"], r["y32"])
