@@ -22,8 +22,8 @@ w8a8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W8A8_OK : W8A
 w8a8_status check_device() {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return W8A8_ERR_CUDA;
-  static int cached_dev = -2;
-  static w8a8_status cached = W8A8_OK;
+  static thread_local int cached_dev = -2;
+  static thread_local w8a8_status cached = W8A8_OK;
   if (dev == cached_dev) return cached;
   int major = 0, minor = 0;
   if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||

@@ -387,7 +387,7 @@ cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cu
   ep.azp = nullptr;
   ep.s_w = g.s_w;
   ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
-  static int s_dev = -1, s_grid = 0;
+  static thread_local int s_dev = -1, s_grid = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -422,7 +422,7 @@ cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st) {
   {
     const int64_t xs_bytes = g.rows * xs_stride(g.K);
     if (!g.seg && g.rows > 0 && g.rows <= 8 && xs_bytes <= 96 * 1024) {
-      static int s_dev = -1, s_grid = 0;
+      static thread_local int s_dev = -1, s_grid = 0;
       int dev = 0;
       cudaError_t e = cudaGetDevice(&dev);
       if (e != cudaSuccess) return e;

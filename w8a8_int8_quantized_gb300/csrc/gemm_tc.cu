@@ -792,8 +792,8 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  static int s_attr_dev = -1;
-  static int s_sms = 0;
+  static thread_local int s_attr_dev = -1;
+  static thread_local int s_sms = 0;
   if (s_attr_dev != dev) {
     e = cudaFuncSetAttribute(tc::gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return e;

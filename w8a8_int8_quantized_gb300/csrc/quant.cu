@@ -382,7 +382,7 @@ static void launch_vec(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t 
                        int8_t* q, __half* q16, float* scale, int32_t* zp, int32_t* sum_out, int32_t* norm_out,
                        cudaStream_t st) {
   auto kern = quant_rows_vec<MODE, THREADS, NV, F16, SUM>;
-  static unsigned cached = 0;  // per instantiation: CTAs that fill the GPU once
+  static thread_local unsigned cached = 0;  // per instantiation: CTAs that fill the GPU once
   if (cached == 0) cached = persistent_grid(kern, THREADS, (int64_t)1 << 40);
   const unsigned grid = (unsigned)(rows < (int64_t)cached ? rows : (int64_t)cached);
   kern<<<grid, THREADS, 0, st>>>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out);
@@ -594,7 +594,7 @@ template <int THREADS, int NV, bool F16>
 static void launch_silu(const __nv_bfloat16* h, int64_t R, int64_t I, int8_t* gq, __half* g16, int32_t* norms,
                         float* sg, cudaStream_t st) {
   auto kern = silu_mul_quant_kernel<THREADS, NV, F16>;
-  static unsigned cached = 0;
+  static thread_local unsigned cached = 0;
   if (cached == 0) cached = persistent_grid(kern, THREADS, (int64_t)1 << 40);
   const unsigned grid = (unsigned)(R < (int64_t)cached ? R : (int64_t)cached);
   kern<<<grid, THREADS, 0, st>>>(h, R, I, gq, g16, norms, sg);

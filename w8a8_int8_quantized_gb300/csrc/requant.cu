@@ -319,8 +319,8 @@ static size_t ring_smem(int warps, int slot) {
 
 template <int WARPS, bool ADJ>
 static cudaError_t launch_ring(const ReqBatch& b, int slot, int32_t* st, cudaStream_t stream) {
-  static int s_dev = -1, s_sms = 0;
-  static size_t s_attr = 0;
+  static thread_local int s_dev = -1, s_sms = 0;
+  static thread_local size_t s_attr = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
@@ -355,7 +355,7 @@ static cudaError_t launch_vec(const ReqBatch& b, int32_t* st, cudaStream_t strea
   if (ring_smem(16, slot) <= (size_t)112 * 1024) return launch_ring<16, ADJ>(b, slot, st, stream);
   if (ring_smem(8, slot) <= (size_t)112 * 1024) return launch_ring<8, ADJ>(b, slot, st, stream);
   if (ring_smem(4, slot) <= (size_t)200 * 1024) return launch_ring<4, ADJ>(b, slot, st, stream);
-  static unsigned cached = 0;
+  static thread_local unsigned cached = 0;
   if (cached == 0) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -436,7 +436,7 @@ requant_word_kernel(const __grid_constant__ ReqBatch b, int32_t* st) {
 
 template <int WPL, bool ADJ>
 static cudaError_t launch_word(const ReqBatch& b, int32_t* st, cudaStream_t stream) {
-  static unsigned cached = 0;
+  static thread_local unsigned cached = 0;
   if (cached == 0) {
     int dev = 0, sms = 0, per_sm = 0;
     if (cudaGetDevice(&dev) != cudaSuccess ||
@@ -640,7 +640,7 @@ max_scale_requant_kernel(int8_t* __restrict__ wq, int64_t units, const float* __
 
 cudaError_t requant_max_scale(int8_t* wq, int64_t units, const float* scales, const MaxScaleParts& parts,
                               float* s_out, int32_t* st, cudaStream_t stream) {
-  static int s_dev = -1, s_sms = 0;
+  static thread_local int s_dev = -1, s_sms = 0;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
