@@ -772,3 +772,39 @@ def test_decode_linear_fused_tensor_scale(bias):
     y = w8.linear(d["x"].to(DEV), wq, sw, bias=b, w_mode=w8.W_TENSOR)
     r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]) if bias else None)
     check_bf16(y, r["y_bits"], r["y32"])
+
+
+def test_concurrent_host_threads():
+    """Two host threads, each on its own stream, call the library concurrently (the per-device
+    launch caches are per thread): both results equal a single-threaded run bit for bit."""
+    import threading
+    cases = []
+    for i, (M, N, K) in enumerate([(300, 520, 4096), (1, 4096, 4096)]):
+        d = _gemm_case(M, N, K, seed=300 + i)
+        wq = torch.from_numpy(d["rq"]).to(DEV)
+        sw = torch.from_numpy(d["rs"]).to(DEV)
+        x = d["x"].to(DEV)
+        ref = w8.linear(x, wq, sw)
+        cases.append((x, wq, sw, ref))
+    torch.cuda.synchronize()
+    errors = []
+
+    def run(case):
+        x, wq, sw, ref = case
+        s = torch.cuda.Stream()
+        try:
+            with torch.cuda.stream(s):
+                for _ in range(10):
+                    y = w8.linear(x, wq, sw)
+                    s.synchronize()
+                    if not torch.equal(y, ref):
+                        errors.append("mismatch")
+        except Exception as e:  # reported below
+            errors.append(repr(e))
+
+    threads = [threading.Thread(target=run, args=(c,)) for c in cases]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    assert not errors, errors
