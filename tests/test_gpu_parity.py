@@ -221,6 +221,7 @@ def _gemm_case(M, N, K, seed, act="dyn_sym", bias=True, w_mode=w8.W_CHANNEL):
 
 @pytest.mark.parametrize("engine", [1, 2])
 @pytest.mark.parametrize("M,N,K", [(16, 512, 512), (1, 256, 64), (300, 520, 1040), (129, 257, 2064),
+                                   (17, 8, 16), (16, 24, 16), (2, 5, 32), (257, 1, 48), (600, 300, 16),
                                    (256, 512, 4096), (7, 1000, 4112)])
 def test_scaled_mm_dyn_sym(engine, M, N, K):
     d = _gemm_case(M, N, K, seed=M * 7 + N)
