@@ -473,6 +473,19 @@ def components(w8, wl, peaks):
                                               w_sumsq=wsq))
         out[f"linear_dyn_asym_M{M}_4096x4096"] = {"us": round(ms * 1e3, 2),
                                                   "TOPS": round(2 * M * 4096 * 4096 / (ms * 1e-3) / 1e12, 1)}
+        if M == 4096:
+            # static per-tensor asymmetric (config 3b): scale and int8 zero point of the whole tensor
+            xf = x.float()
+            lo, hi = float(xf.min()), float(xf.max())
+            sc = torch.tensor([(hi - lo) / 255.0], dtype=torch.float32, device=dev)
+            zp = torch.tensor([max(-128, min(127, round(-128 - lo / float(sc))))], dtype=torch.int32, device=dev)
+            adj_s = w8.azp_adj(wq, zp)
+            ws_s = torch.empty(w8.linear_workspace_size(M, 4096, "static_asym"), dtype=torch.uint8, device=dev)
+            ms = _time_launches(lambda: w8.linear(x, wq, sw, act_mode="static_asym", input_scale=sc,
+                                                  input_zero_point=zp, azp_adj=adj_s, workspace=ws_s, out=yb,
+                                                  w_sumsq=wsq))
+            out["linear_static_asym_M4096_4096x4096"] = {"us": round(ms * 1e3, 2),
+                                                         "TOPS": round(2 * M * 4096 * 4096 / (ms * 1e-3) / 1e12, 1)}
     # small-M (weight streaming) linears on the gate_up shape
     wq = torch.randint(-127, 128, (28672, 4096), dtype=torch.int8, device=dev)
     sw = torch.rand(28672, device=dev)

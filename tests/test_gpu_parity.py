@@ -809,3 +809,29 @@ def test_concurrent_host_threads():
     for t in threads:
         t.join()
     assert not errors, errors
+
+
+@pytest.mark.parametrize("engine", [1, 2])
+def test_static_asym_epilogue_ranges(engine):
+    """Static asymmetric outputs are (s_x s_w) f32(acc - azp'[n]) with the premultiplied azp'.
+    Groups of 8 columns put azp' below 2^22, in [2^22, 2^24) and beyond 2^24 (each handled
+    differently by the tensor-core epilogue); every output equals the oracle's exact int64
+    difference rounded once."""
+    w8.set_gemm_engine(engine)
+    M, N, K = 300, 512, 1024
+    rng = np.random.default_rng(41)
+    xq = rng.integers(-128, 128, size=(M, K), dtype=np.int8)
+    wq = rng.integers(-127, 128, size=(N, K), dtype=np.int8)
+    mags = np.array([2 ** 10, 2 ** 21 + 3, 2 ** 23 - 5, 2 ** 24 + 7, 2 ** 30 + 11], dtype=np.int64)
+    adj = np.empty(N, dtype=np.int64)
+    for gi in range(N // 8):
+        m = mags[gi % len(mags)]
+        adj[8 * gi: 8 * gi + 8] = rng.integers(-m, m, size=8)
+    adj = adj.astype(np.int32)
+    s_x = np.array([2.0 ** -9], dtype=np.float32)
+    s_w = (rng.random(N) * 1e-3 + 1e-4).astype(np.float32)
+    y = w8.scaled_mm(torch.from_numpy(xq).to(DEV), torch.from_numpy(wq).to(DEV), torch.from_numpy(s_x).to(DEV),
+                     torch.from_numpy(s_w).to(DEV), "static_asym", azp_adj=torch.from_numpy(adj).to(DEV))
+    acc = oracle.int8_gemm(xq, wq)
+    yb, y32 = oracle.scaled_mm_epilogue(acc, np.repeat(s_x, M), s_w, adj=adj, adj_premultiplied=True)
+    check_bf16(y, yb, y32)
