@@ -1,13 +1,19 @@
 // Weight-streaming INT8 GEMM for few activation rows (decode-sized M).
 //
 // With M <= 16 the layer is bound by reading the int8 weight once from HBM (2*M ops per
-// weight byte), so the kernel is shaped for bandwidth, not for tensor-core peak: each CTA
-// owns 16 output channels and 16 token rows, its 8 warps split K into interleaved
-// 64-byte chunks so that neighbouring warps read neighbouring bytes of a weight row, and
-// each thread keeps four chunks of 16-byte loads in flight.  The integer products run on
-// the exact s8 x s8 -> s32 warp MMA (m16n8k32), with the weight as the 16-row operand
-// and the tokens as the 8-column operand.  The partial sums of the 8 warps are added in
-// shared memory and the scale/azp/bias epilogue is applied before one bf16 store.
+// weight byte), so the kernels are shaped for bandwidth, not for tensor-core peak.  Blocks
+// of 16 output channels; 8 warps split K into interleaved 64-byte chunks so that
+// neighbouring warps read neighbouring bytes of a weight row; the integer products run on
+// the exact s8 x s8 -> s32 warp MMA (m16n8k32), with the weight as the 16-row operand and
+// the tokens as the 8-column operand; the partial sums of the 8 warps are added in shared
+// memory and the scale/azp/bias epilogue is applied before one bf16 store.  Three forms:
+//   gemm_small_m_kernel     one block of 16 channels x 16 token rows per CTA, four chunks of
+//                           16-byte loads in flight per thread (9-16 rows, grouped segments,
+//                           rows too long to stage);
+//   gemm_small_m_xs_kernel  at most 8 rows staged in shared memory once per persistent CTA,
+//                           eight chunks in flight per thread;
+//   gemm_small_m_fq_kernel  one dynamic-symmetric bf16 row quantized inside the CTA (the
+//                           stand-alone quantizer's exact rule) before the same streaming.
 //
 // K order inside a 64-byte chunk: each thread loads 16 contiguous bytes of a row and
 // feeds them to the MMA as its k-slots; A and B use the same mapping, so the sum over k
