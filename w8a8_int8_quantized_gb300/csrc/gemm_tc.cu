@@ -9,7 +9,9 @@
 // output tile in one of two ways:
 //   - single pass: if every activation row r of the tile has sum_k |a[r,k]| < 2^17, then
 //     |any partial sum| <= 2^17 * 128 = 2^24 and the fp32 accumulator over the whole K is
-//     exact (the activation producer writes these row L1 norms next to the fp16 codes);
+//     exact (the activation producer writes these row L1 norms next to the fp16 codes); or,
+//     for asymmetric activations with the weight's row sums of squares given, if
+//     ||a_r||_2 * ||w_n||_2 < 2^24 over the tile (Cauchy-Schwarz bounds every partial sum);
 //   - chunked: otherwise the K loop is cut into chunks of 1024 (1024 * 128 * 128 = 2^24),
 //     each chunk goes to TMEM buffer 0, and the epilogue adds the chunk's exact fp32 result
 //     into an int32 running sum kept in TMEM buffer 1 (tcgen05.ld / tcgen05.st).

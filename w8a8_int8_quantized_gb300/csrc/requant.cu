@@ -5,9 +5,12 @@
 //   s[i]   = max_j |W[i,j]| / 127 ;  q = clamp(round(W / s), -127, 127) ;  zero row -> q=0, s=1.
 // Rows are independent (the README's tool also works matrix by matrix, row chunk by row
 // chunk), so one warp owns one row at a time.  Aligned rows (K % 16 == 0) are brought into
-// shared memory by one bulk copy each and read twice on chip (absmax, then quantize); the
-// others take a warp-per-row byte-load path.  One launch per path covers a whole batch of
-// matrices through a by-value descriptor table.
+// shared memory by one bulk copy each and read twice on chip (absmax, then quantize); rows
+// of K % 4 == 0 up to 4096 on 4-byte boundaries are held in registers as words; the others
+// take a warp-per-row byte-load path.  One launch per path covers a whole batch of matrices
+// through a by-value descriptor table, optionally writing each row's code sum (azp_adj).
+// Also here: the requantization of a fused weight's per-tensor partitions to their largest
+// scale ("[SGLang] W4A8, W8A8, W4A4", item 7, requantize_with_max_scale).
 #include "common.cuh"
 #include "internal.h"
 
