@@ -504,7 +504,8 @@ def components(w8, wl, peaks):
         wbytes = 28672 * 4096
         out[f"linear_M{M}_28672x4096"] = {"us": round(ms * 1e3, 2),
                                           "TOPS": round(2 * M * 28672 * 4096 / (ms * 1e-3) / 1e12, 2),
-                                          "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1)}
+                                          "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
+                                          "frac_hbm": round(wbytes / (ms * 1e-3) / 1e9 / hbm, 3)}
     # S9 MoE layer (4096 tokens, 32 experts, top-4)
     md = moe_device_inputs(w8, wl)
     ms = _time_launches(lambda: w8.moe_forward(*md["args"]), reps=5)
