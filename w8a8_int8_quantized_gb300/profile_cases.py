@@ -14,6 +14,7 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
   gemm_chunked   M=4096, N=28672, K=4096 with N(0,1) activations: many rows' L1 norms exceed
                  2^17, so their tiles run the 1024-K chunked mode
   small          w8a8_linear at M=16 (warp-MMA engine), N=28672, K=4096
+  decode8        w8a8_scaled_mm on 8 quantized token rows (staged small-M kernel), N=28672, K=4096
   moe            the MoE layer: 4096 tokens, 32 experts, top-4
   moe_routed     the same layer behind w8a8_moe_route (router logits in, every step on the GPU)
   route          w8a8_moe_route alone: 4096 tokens, 32 experts, top-4
@@ -80,6 +81,13 @@ def case_fn(name):
         ws = torch.empty(w8.linear_workspace_size(16, 4096), dtype=torch.uint8, device=dev)
         y = torch.empty(16, 28672, dtype=torch.bfloat16, device=dev)
         return lambda: w8.linear(x, wq, sw, workspace=ws, out=y)
+    if name == "decode8":
+        xq = torch.randint(-127, 128, (8, 4096), dtype=torch.int8, device=dev, generator=_gen(18))
+        sx = torch.rand(8, device=dev, generator=_gen(19)).mul_(1e-2)
+        wq = torch.randint(-127, 128, (28672, 4096), dtype=torch.int8, device=dev, generator=_gen(20))
+        sw = torch.rand(28672, device=dev, generator=_gen(21)).mul_(1e-3)
+        y = torch.empty(8, 28672, dtype=torch.bfloat16, device=dev)
+        return lambda: w8.scaled_mm(xq, wq, sx, sw, "dyn_sym", out=y)
     if name == "moe":
         T, H, E, k, inter = 4096, 4096, 32, 4, 1408
         g = _gen(10)
