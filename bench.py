@@ -473,7 +473,7 @@ def components(w8, wl, peaks):
         x = wl.asym_activations(M, 4096, seed=3).to(dev)
         w = torch.randn(4096, 4096, device=dev).mul_(0.02).to(torch.bfloat16)
         wq, sw, adj, wsq = w8.quantize_weight(w, with_azp_adj=True, with_sumsq=True)
-        ws = torch.empty(w8.linear_workspace_size(M, 4096, "dyn_asym"), dtype=torch.uint8, device=dev)
+        ws = torch.empty(w8.linear_workspace_size(M, 4096, "dyn_asym", 4096), dtype=torch.uint8, device=dev)
         yb = torch.empty(M, 4096, dtype=torch.bfloat16, device=dev)
         ms = _time_launches(lambda: w8.linear(x, wq, sw, act_mode="dyn_asym", azp_adj=adj, workspace=ws, out=yb,
                                               w_sumsq=wsq))
@@ -497,7 +497,7 @@ def components(w8, wl, peaks):
     sw = torch.rand(28672, device=dev)
     for M in (1, 16, 128, 1024):
         x = wl.llama_activations(M, 4096, seed=4).to(dev)
-        ws = torch.empty(max(w8.linear_workspace_size(M, 4096), 16), dtype=torch.uint8, device=dev)
+        ws = torch.empty(max(w8.linear_workspace_size(M, 4096, "dyn_sym", 28672), 16), dtype=torch.uint8, device=dev)
         yb = torch.empty(M, 28672, dtype=torch.bfloat16, device=dev)
         f0 = _time_launches(lambda: flush.zero_())
         ms = _time_launches(lambda: (flush.zero_(), w8.linear(x, wq, sw, workspace=ws, out=yb))) - f0
@@ -506,6 +506,19 @@ def components(w8, wl, peaks):
                                           "TOPS": round(2 * M * 28672 * 4096 / (ms * 1e-3) / 1e12, 2),
                                           "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
                                           "frac_hbm": round(wbytes / (ms * 1e-3) / 1e9 / hbm, 3)}
+    # a few hundred tokens on the down projection: 16 tiles, split along K over the idle pairs
+    wq = torch.randint(-127, 128, (4096, 14336), dtype=torch.int8, device=dev)
+    sw = torch.rand(4096, device=dev)
+    for M in (128, 256):
+        x = wl.llama_activations(M, 14336, seed=5).to(dev)
+        ws = torch.empty(w8.linear_workspace_size(M, 14336, "dyn_sym", 4096), dtype=torch.uint8, device=dev)
+        yb = torch.empty(M, 4096, dtype=torch.bfloat16, device=dev)
+        f0 = _time_launches(lambda: flush.zero_())
+        ms = _time_launches(lambda: (flush.zero_(), w8.linear(x, wq, sw, workspace=ws, out=yb))) - f0
+        out[f"linear_M{M}_4096x14336_split_k"] = {"us": round(ms * 1e3, 2),
+                                                  "TOPS": round(2 * M * 4096 * 14336 / (ms * 1e-3) / 1e12, 1),
+                                                  "frac_tensor": round(2 * M * 4096 * 14336 / (ms * 1e-3) / 1e12 / tf,
+                                                                       3)}
     # S9 MoE layer (4096 tokens, 32 experts, top-4)
     md = moe_device_inputs(w8, wl)
     ms = _time_launches(lambda: w8.moe_forward(*md["args"]), reps=5)

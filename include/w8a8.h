@@ -117,6 +117,7 @@ w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, 
  *              256-byte aligned (the tensor-core engine stages the activations there as
  *              fp16 integer codes with their row L1 norms and sums of squares).  May be
  *              NULL only when the warp-MMA engine runs (M <= 16 under automatic selection).
+ *              Bytes past that size are split scratch (see w8a8_splitk_workspace_size).
  * Epilogue, float32 with one rounding per step and no fused multiply-add:
  *   c = acc - zp[m]*azp_adj[n] (exact integer, rounded to float32);
  *   y = bf16_rne( (s_x[m]*s_w[n]) * c (+ bias[n]) ).
@@ -133,13 +134,31 @@ w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_
                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
 /*
+ * w8a8_splitk_workspace_size -- scratch for K-split GEMMs of few tiles.
+ *   The tensor-core engine runs persistent CTA pairs over 256 x 256 output tiles.  A launch
+ *   with fewer tiles than two waves of pairs (M of a few hundred rows or less) leaves pairs
+ *   idle; with this much scratch it cuts the tiles past its first full wave (all of them
+ *   when there is none) along K at 1024-element boundaries, runs the parts on the idle pairs,
+ *   and a second kernel adds their int32 partial sums and applies the epilogue: the result
+ *   is the same integer, so y is unchanged.
+ *   Returns the extra bytes a w8a8_scaled_mm or w8a8_linear call of this shape uses for it on
+ *   the current device, placed right after the call's own workspace size (so a workspace of
+ *   w8a8_linear_workspace_size(M, K, mode) + w8a8_splitk_workspace_size(M, N, K) bytes).  0
+ *   when the shape does not split, or for invalid sizes or devices.  The scratch needs no
+ *   initialization; calls that share a workspace must not overlap.  At most
+ *   (SMs / 2) * 256 KiB.
+ */
+size_t w8a8_splitk_workspace_size(int64_t M, int64_t N, int64_t K);
+
+/*
  * w8a8_linear -- the whole layer forward: quantize x (any act_mode) then w8a8_scaled_mm
  * ([SGLang-CT] item 3 apply_weights; [vLLM-W8A8] 4.2 apply_weights(layer, x, bias)).
  *   x bf16 [M, K] (row stride ldx); wq/s_w/azp_adj/w_sumsq/bias as for w8a8_scaled_mm.
  *   input_scale / input_zero_point: float [1] / int32 [1] for the static modes, else NULL.
  *   workspace: device buffer of at least w8a8_linear_workspace_size(M, K, act_mode) bytes,
  *   256-byte aligned; it holds the quantized activations (in the format the selected GEMM
- *   engine reads), their scales and zero points between the two kernels.
+ *   engine reads), their scales and zero points between the two kernels.  Bytes past that
+ *   size are split scratch (see w8a8_splitk_workspace_size).
  */
 size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode);
 w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int act_mode,

@@ -86,6 +86,10 @@ def test_host_side_argument_checks_need_no_gpu(libpath):
     assert lib.w8a8_weight_sumsq(p, -1, 16, p, None) == 1
     assert lib.w8a8_weight_sumsq(None, 0, 16, None, None) == 0
     assert lib.w8a8_linear_workspace_size(4, 16, 0) == 256 + 256 + 2 * 256
+    # K-split scratch: invalid sizes need none (answered before any CUDA call)
+    assert lib.w8a8_splitk_workspace_size(0, 4096, 4096) == 0
+    assert lib.w8a8_splitk_workspace_size(128, -1, 4096) == 0
+    assert lib.w8a8_splitk_workspace_size(128, 4096, 0) == 0
     # max-scale requantization: widths must sum to N, 1 <= P <= 16
     w2 = (ctypes.c_int64 * 2)(3, 4)
     assert lib.w8a8_requantize_max_scale(p, 8, 16, p, ctypes.cast(w2, ctypes.c_void_p), 2, p, None, None) == 1

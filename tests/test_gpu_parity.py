@@ -330,6 +330,106 @@ def test_gemm_single_pass_bound(K, fill):
     check_bf16(y, yb, y32)
 
 
+def _split_bytes_expected(M, N, K):
+    """The K-split scratch from the plan stated in include/w8a8.h: launches with fewer tiles
+    than two waves of CTA pairs cut the tiles past the first full wave into as many parts as
+    fill the idle pairs, at most one per 1024-K chunk."""
+    pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
+    tiles = -(-M // 256) * -(-N // 256)
+    if M <= 16 or tiles >= 2 * pairs:
+        return 0
+    tail = tiles - (pairs if tiles >= pairs else 0)
+    f = min(pairs // tail, -(-K // 1024))
+    if f < 2:
+        return 0
+    return tail * f * 256 * 256 * 4
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 4096, 4096), (300, 1000, 14336), (256, 20480, 2048), (17, 520, 3072),
+                                   (130, 8, 1040), (512, 4104, 4096), (64, 256, 1024)])
+def test_splitk_workspace_size(M, N, K):
+    assert w8.splitk_workspace_size(M, N, K) == _split_bytes_expected(M, N, K)
+
+
+@pytest.mark.parametrize("act", ["dyn_sym", "dyn_asym", "static_asym"])
+@pytest.mark.parametrize("M,N,K,acts", [(128, 4096, 4096, "llama"), (300, 1000, 14336, "llama"),
+                                        (256, 20480, 2048, "llama"), (77, 520, 3072, "normal"),
+                                        (130, 264, 5120, "normal")])
+def test_linear_split_k(act, M, N, K, acts):
+    """Launches with fewer tiles than two waves split tiles along K when the workspace holds
+    the split scratch: only one row tile (M = 128: 16 tiles in 4 parts), unequal parts
+    (K = 14336: 14 chunks in parts of 3 and 4), a full first wave plus split tail tiles
+    (256 x 20480: 80 tiles), ragged rows and columns, and N(0, 1) rows whose L1 norms exceed
+    2^17 so each part runs 1024-K chunks.  Bit-exact against the oracle and against the same
+    call without the scratch."""
+    if _split_bytes_expected(M, N, K) == 0:
+        pytest.skip("shape does not split on this device")
+    rng = np.random.default_rng(M + N + K)
+    if acts == "normal":
+        x = torch.from_numpy(rng.standard_normal((M, K)).astype(np.float32)).to(torch.bfloat16)
+        if "asym" in act:
+            x = x + 0.5
+    elif "asym" in act:
+        x = wl.asym_activations(M, K, seed=K)
+    else:
+        x = wl.llama_activations(M, K, seed=K)
+    w = wl.weight_bf16(N, K, seed=N)
+    b = wl.weight_bf16(1, N, seed=N + 1, std=0.1)[0]
+    rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+    xs = x.float().numpy()
+    sc, z = oracle.static_scale_from_tensor(xs)
+    wq = torch.from_numpy(rq).to(DEV)
+    sw = torch.from_numpy(rs).to(DEV)
+    kw = {}
+    if act == "dyn_asym":
+        kw["azp_adj"] = w8.azp_adj(wq)
+    if act == "static_asym":
+        kw["input_scale"] = torch.tensor([sc], dtype=torch.float32, device=DEV)
+        kw["input_zero_point"] = torch.tensor([z], dtype=torch.int32, device=DEV)
+        kw["azp_adj"] = w8.azp_adj(wq, kw["input_zero_point"])
+    xd = x.to(DEV)
+    base = w8.linear_workspace_size(M, K, act)
+    extra = w8.splitk_workspace_size(M, N, K)
+    ws_split = torch.full((base + extra,), 0xA5, dtype=torch.uint8, device=DEV)  # stale scratch
+    ws_plain = torch.empty(base, dtype=torch.uint8, device=DEV)
+    ws_short = torch.empty(base + extra - 256, dtype=torch.uint8, device=DEV)  # too small: no split
+    y_split = w8.linear(xd, wq, sw, act_mode=act, bias=b.to(DEV), workspace=ws_split, **kw)
+    y_again = w8.linear(xd, wq, sw, act_mode=act, bias=b.to(DEV), workspace=ws_split, **kw)
+    y_plain = w8.linear(xd, wq, sw, act_mode=act, bias=b.to(DEV), workspace=ws_plain, **kw)
+    y_short = w8.linear(xd, wq, sw, act_mode=act, bias=b.to(DEV), workspace=ws_short, **kw)
+    torch.cuda.synchronize()
+    r = oracle.w8a8_linear(wl.bits(x), rq, rs, bias_bits=wl.bits(b), mode=act, input_scale=sc, input_zero_point=z)
+    check_bf16(y_split, r["y_bits"], r["y32"])
+    for y in (y_again, y_plain, y_short):
+        assert torch.equal(y.view(torch.int16), y_split.view(torch.int16))
+
+
+@pytest.mark.parametrize("w_mode", [w8.W_CHANNEL, w8.W_TENSOR])
+def test_scaled_mm_split_k_extremes(w_mode):
+    """acc = +-128*127*K at K = 14336 through split parts (2 tiles in 14 one-chunk parts),
+    with zero points on every row: exact."""
+    M, N, K = 130, 260, 14336
+    xq = torch.full((M, K), -128, dtype=torch.int8)
+    xq[1::2] = 127
+    xq[5, ::3] = -1
+    wq = torch.full((N, K), 127, dtype=torch.int8)
+    wq[1::2] = -127
+    wq[7, 1000:] = 3
+    sx = torch.full((M,), 1.0, dtype=torch.float32)
+    sw = torch.full((N if w_mode == w8.W_CHANNEL else 1,), 2.0 ** -20, dtype=torch.float32)
+    zp = torch.arange(M, dtype=torch.int32) - 60
+    adj = torch.from_numpy(oracle.azp_adj(wq.numpy()))
+    assert w8.splitk_workspace_size(M, N, K) > 0
+    ws = torch.empty(w8.lib().w8a8_scaled_mm_workspace_size(M, K) + w8.splitk_workspace_size(M, N, K),
+                     dtype=torch.uint8, device=DEV)
+    y = w8.scaled_mm(xq.to(DEV), wq.to(DEV), sx.to(DEV), sw.to(DEV), "dyn_asym", zp=zp.to(DEV), azp_adj=adj.to(DEV),
+                     w_mode=w_mode, workspace=ws)
+    acc = oracle.int8_gemm(xq.numpy(), wq.numpy())
+    swn = sw.numpy() if w_mode == w8.W_CHANNEL else np.full(N, sw.numpy()[0], dtype=np.float32)
+    yb, y32 = oracle.scaled_mm_epilogue(acc, sx.numpy(), swn, zp=zp.numpy(), adj=adj.numpy())
+    check_bf16(y, yb, y32)
+
+
 def test_packed_linear_matches_int8_path():
     d = _gemm_case(200, 512, 2048, seed=21)
     wq = torch.from_numpy(d["rq"]).to(DEV)

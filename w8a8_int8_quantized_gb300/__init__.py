@@ -39,6 +39,7 @@ from ._binding import (  # noqa: F401
     requantize_max_scale,
     scaled_mm,
     set_gemm_engine,
+    splitk_workspace_size,
     weight_sumsq,
     silu_mul_quant,
 )

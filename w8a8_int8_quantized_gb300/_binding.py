@@ -37,6 +37,7 @@ SIGNATURES = {
     "w8a8_scaled_mm_workspace_size": (_SZ, [_I64, _I64]),
     "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "w8a8_linear_workspace_size": (_SZ, [_I64, _I64, _I]),
+    "w8a8_splitk_workspace_size": (_SZ, [_I64, _I64, _I64]),
     "w8a8_linear": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _I64, _I, _P, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "w8a8_quantize_weight": (_I, [_P, _I64, _I64, _P, _P, _P, _P, _P]),
     "w8a8_weight_sumsq": (_I, [_P, _I64, _I64, _P, _P]),
@@ -156,7 +157,8 @@ def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mod
         raise ValueError("K mismatch")
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=xq.device)
-    ws = _workspace(lib().w8a8_scaled_mm_workspace_size(M, K), xq.device, workspace)
+    ws = _workspace(lib().w8a8_scaled_mm_workspace_size(M, K) + splitk_workspace_size(M, N, K), xq.device,
+                    workspace)
     code = lib().w8a8_scaled_mm(_ptr(xq), _ptr(wq), M, N, K, _mode(act_mode), _ptr(s_x), _ptr(zp), _ptr(azp_adj),
                                 int(w_mode), _ptr(s_w), _ptr(w_sumsq), _ptr(bias), _ptr(out), _ptr(ws), ws.numel(),
                                 _ptr(status), _stream())
@@ -164,8 +166,15 @@ def scaled_mm(xq, wq, s_x, s_w, act_mode="dyn_sym", zp=None, azp_adj=None, w_mod
     return out
 
 
-def linear_workspace_size(M, K, act_mode="dyn_sym"):
-    return int(lib().w8a8_linear_workspace_size(M, K, _mode(act_mode)))
+def splitk_workspace_size(M, N, K):
+    """Extra workspace bytes with which a GEMM of few tiles splits along K (0: no split)."""
+    return int(lib().w8a8_splitk_workspace_size(M, N, K))
+
+
+def linear_workspace_size(M, K, act_mode="dyn_sym", N=None):
+    """Workspace of w8a8_linear; with N, including the K-split scratch for that shape."""
+    n = int(lib().w8a8_linear_workspace_size(M, K, _mode(act_mode)))
+    return n + (splitk_workspace_size(M, N, K) if N is not None else 0)
 
 
 def linear(x, wq, s_w, act_mode="dyn_sym", input_scale=None, input_zero_point=None, azp_adj=None, bias=None,
@@ -176,7 +185,7 @@ def linear(x, wq, s_w, act_mode="dyn_sym", input_scale=None, input_zero_point=No
     M, K = x.shape
     N = wq.shape[0]
     m = _mode(act_mode)
-    workspace = _workspace(linear_workspace_size(M, K, m), x.device, workspace)
+    workspace = _workspace(linear_workspace_size(M, K, m, N), x.device, workspace)
     if out is None:
         out = torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
     code = lib().w8a8_linear(_ptr(x), M, K, K, m, _ptr(input_scale), _ptr(input_zero_point), _ptr(wq), N,

@@ -150,7 +150,18 @@ w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
+  if (!small && workspace_bytes > ready_bytes(M, K)) {
+    g.split_ws = static_cast<uint8_t*>(workspace) + ready_bytes(M, K);
+    g.split_bytes = workspace_bytes - ready_bytes(M, K);
+  }
   return run_gemm(g, stream, workspace, small, false);
+}
+
+size_t w8a8_splitk_workspace_size(int64_t M, int64_t N, int64_t K) {
+  if (M <= 0 || N <= 0 || K <= 0 || K > kMaxK) return 0;
+  if (check_device() != W8A8_OK) return 0;
+  if (use_small_engine(M, true)) return 0;
+  return gemm_split_bytes(M, N, K);
 }
 
 size_t w8a8_linear_workspace_size(int64_t M, int64_t K, int act_mode) {
@@ -229,6 +240,10 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
+  if (!small && workspace_bytes > need) {
+    g.split_ws = ws + need;
+    g.split_bytes = workspace_bytes - need;
+  }
   return run_gemm(g, stream, workspace, small, true);
 }
 

@@ -32,6 +32,15 @@
 // The pair is persistent and walks a static list of (segment, row tile, column tile) work
 // items, so grouped (MoE) and dense launches are the same kernel.
 //
+// Under-filled launches.  A dense launch with fewer tiles than two waves of pairs (a few
+// hundred tokens or less) leaves pairs idle for most of its run.  Given scratch, the tiles
+// past its first full wave (all of them when there is none) are cut along K at 1024-element
+// boundaries into parts that run on the idle pairs (a separate instantiation, so launches
+// that do not split run the kernel without this code).  A part is a run of whole chunks, so
+// its sums are exact by the argument above; it stores them as an int32 partial tile, and a
+// second kernel adds the parts and applies the same epilogue: the integer is the same, so is
+// the output.
+//
 // Every wait is bounded in time: a wait that runs out records W8A8_ERR_TIMEOUT, raises a
 // CTA-wide abort flag, and all roles leave their loops; each CTA then waits (bounded) for
 // its own outstanding TMA copies and MMAs, both CTAs meet at a cluster barrier, and TMEM is
@@ -281,10 +290,43 @@ struct KParams {
   const int32_t* asq;    // [rows] sum_k a[r, k]^2, or null (dense GEMMs with weight squares only)
   const int32_t* wsq;    // [N] sum_k w[n, k]^2, or null
   int az_small;          // 127 * K < 2^22: every azp_adj = sum_k w[n, k] is below 2^22 in magnitude
+  int dp_units;          // split launches: work items that are whole tiles (the first)
+  int split;             // split launches: parts per remaining tile
+  int32_t* partials;     // split launches: [split tiles][split][BM][BN] int32 partial sums
   EpiParams ep;
   __nv_bfloat16* y;
   int32_t* status;
 };
+
+// One work item: a whole tile (tail < 0) or part `part` of split tile `tail`, over the K
+// steps [kb0, kb1).  Parts start on chunk boundaries and each holds at least one chunk.
+struct Work {
+  Tile tl;
+  int kb0, kb1, tail, part;
+};
+
+template <bool SPLIT>
+__device__ __forceinline__ Work decode_work(int u, const Bars* bars, const KParams& p, int nkb) {
+  Work w;
+  int t = u;
+  w.tail = -1;
+  w.part = 0;
+  w.kb0 = 0;
+  w.kb1 = nkb;
+  if constexpr (SPLIT) {
+    if (u >= p.dp_units) {
+      const int v = u - p.dp_units;
+      w.tail = v / p.split;
+      w.part = v - w.tail * p.split;
+      t = p.dp_units + w.tail;
+      const int nch = (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
+      w.kb0 = CHUNK_STEPS * (w.part * nch / p.split);
+      w.kb1 = min(nkb, CHUNK_STEPS * ((w.part + 1) * nch / p.split));
+    }
+  }
+  w.tl = decode_tile(t, bars, p.E, p.seg, p.rows);
+  return w;
+}
 
 // Whether the pair tile starting at row0 can run single pass (warp-wide, all lanes agree).
 // Every partial sum of the fp32 accumulation is an integer bounded by sum_k |a_k| |w_k|, so
@@ -322,6 +364,7 @@ __device__ __forceinline__ bool tile_single_pass(const KParams& p, const Tile& t
   return (uint64_t)(uint32_t)mq * (uint64_t)(uint32_t)mw < (1ull << 48);
 }
 
+template <bool SPLIT>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(NUM_THREADS, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB, const KParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -380,17 +423,19 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   tc_fence_after();
   const uint32_t tmem = bars->tmem_base;
   const int tiles = bars->tiles_total;
+  const int units = SPLIT ? p.dp_units + (tiles - p.dp_units) * p.split : tiles;
 
   if (warp == 0) {
     // ---------------------------------------------------------------- TMA producer (each CTA)
     if (lane == 0) {
       uint32_t nb = 0, na = 0;  // weight / activation copies issued
       bool ok = true;
-      for (int t = pair; t < tiles && ok; t += npairs) {
-        const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
+      for (int t = pair; t < units && ok; t += npairs) {
+        const Work wk = decode_work<SPLIT>(t, bars, p, nkb);
+        const Tile& tl = wk.tl;
         const int32_t arow = (int32_t)(tl.row0 + BM_CTA * rank);
         const int32_t brow = (int32_t)((int64_t)tl.e * p.N + tl.n0 + BN_CTA * rank);
-        for (int kb = 0; kb < nkb; ++kb) {
+        for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           const uint32_t sa = na % SA, pha = (na / SA) & 1;
           if (!wait_bar(&bars->empty_a[sa], pha ^ 1, bars, p.status)) { ok = false; break; }
           mbar_expect_tx(&bars->full_a[sa], A16);
@@ -419,11 +464,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       uint32_t it = 0, nbuf = 0;
       uint32_t acq0 = 0u, acq1 = 0u;  // acquisitions of buffer 0 / 1 so far
       bool ok = true;
-      for (int t = pair; t < tiles && ok; t += npairs) {
-        const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
-        const bool single = tile_single_pass(p, tl, lane);
+      for (int t = pair; t < units && ok; t += npairs) {
+        const Work wk = decode_work<SPLIT>(t, bars, p, nkb);
+        const bool single = tile_single_pass(p, wk.tl, lane);
         if (lane == 0) {
-          const int spc = single ? nkb : CHUNK_STEPS;
+          const int spc = single ? wk.kb1 - wk.kb0 : CHUNK_STEPS;
           uint32_t b = 0;
           if (single) {
             b = nbuf;
@@ -432,8 +477,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!wait_bar(&bars->accempty[1], (acq1 & 1) ^ 1, bars, p.status)) ok = false;
             ++acq1;
           }
-          for (int kb = 0; kb < nkb && ok; ++kb, ++it) {
-            if (kb % spc == 0) {
+          for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb, ++it) {
+            const int kr = kb - wk.kb0;  // step within this work item
+            if (kr % spc == 0) {
               const uint32_t a = b ? acq1 : acq0;
               if (!wait_bar(&bars->accempty[b], (a & 1) ^ 1, bars, p.status)) { ok = false; break; }
               if (b) ++acq1; else ++acq0;
@@ -448,10 +494,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
             for (int kk = 0; kk < BK / 16; ++kk)
               mma_f16_pair(tmem + b * BN, desc_sw128(abase + kk * 32), desc_sw128(bbase + kk * 32),
-                           (kb % spc != 0 || kk != 0) ? 1u : 0u);
+                           (kr % spc != 0 || kk != 0) ? 1u : 0u);
             mma_commit_pair(&bars->empty_a[sa]);
             mma_commit_pair(&bars->empty16[sb]);
-            if (kb % spc == spc - 1 || kb == nkb - 1) mma_commit_pair(&bars->accfull[b]);
+            if (kr % spc == spc - 1 || kb == wk.kb1 - 1) mma_commit_pair(&bars->accfull[b]);
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -477,8 +523,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint32_t it = 0;  // global step counter (same sequence as the producer and the MMA)
     uint32_t use = 0; // how many steps this warp has converted
     bool ok = true;
-    for (int t = pair; t < tiles && ok; t += npairs) {
-      for (int kb = 0; kb < nkb; ++kb, ++it) {
+    for (int t = pair; t < units && ok; t += npairs) {
+      const Work wk = decode_work<SPLIT>(t, bars, p, nkb);
+      for (int kb = wk.kb0; kb < wk.kb1; ++kb, ++it) {
         if ((int)(it % CONV_WARPS) != cw) continue;
         const uint32_t ph = use & 1;
         ++use;
@@ -532,10 +579,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint32_t nbuf = 0;
     uint32_t filled0 = 0u, filled1 = 0u;  // fills of buffer 0 / 1 consumed so far
     bool ok = true;
-    for (int t = pair; t < tiles && ok; t += npairs) {
-      const Tile tl = decode_tile(t, bars, p.E, p.seg, p.rows);
+    for (int t = pair; t < units && ok; t += npairs) {
+      const Work wk = decode_work<SPLIT>(t, bars, p, nkb);
+      const Tile& tl = wk.tl;
       const bool single = tile_single_pass(p, tl, lane);
-      const int64_t m = tl.row0 + BM_CTA * rank + q * 32 + lane;
+      const int rloc = BM_CTA * (int)rank + q * 32 + lane;  // row within the pair tile
+      const int64_t m = tl.row0 + rloc;
       const bool row_ok = m < tl.row_end;
       EpiParams ep = p.ep;
       if (ep.w_mode == W8A8_W_CHANNEL) ep.s_w = p.ep.s_w + (int64_t)tl.e * p.N;
@@ -543,7 +592,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       const int zpm = row_ok ? epi_row_zp(ep, m) : 0;
       const int64_t nb = tl.n0 + h * 128;
       __nv_bfloat16* yrow = p.y + (row_ok ? m : 0) * p.N;
-      const int nch = single ? 1 : (nkb + CHUNK_STEPS - 1) / CHUNK_STEPS;
+      const int nch = single ? 1 : (wk.kb1 - wk.kb0 + CHUNK_STEPS - 1) / CHUNK_STEPS;
       const uint32_t b = single ? nbuf : 0u;
       if (single) nbuf ^= 1u;
       // Single-pass tiles: every fp32 accumulator is the exact integer (|acc| <= 2^24), which is
@@ -553,7 +602,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
       // so one fma rounds the exact difference once, as the integer path does (rows with
       // |zp| >= 2^24, which bf16 inputs never produce, take the integer form).
       const bool dyn_asym = ep.act_mode == W8A8_ACT_DYN_TOKEN_ASYM;
-      const bool direct = single && (ep.act_mode == W8A8_ACT_DYN_TOKEN_SYM ||
+      const bool direct = single && wk.tail < 0 && (ep.act_mode == W8A8_ACT_DYN_TOKEN_SYM ||
                                      ep.act_mode == W8A8_ACT_STATIC_TENSOR_SYM || dyn_asym);
       const bool zp_exact = zpm > -16777216 && zpm < 16777216;
       const float zpf = (float)zpm;
@@ -659,6 +708,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           }
           if (!last) {
             tmem_st32(lanebase + BN + g * 32, v);
+          } else if (SPLIT && wk.tail >= 0) {
+            if (row_ok) {  // this part's int32 sums; the reduce kernel applies the epilogue
+              int4* dst = reinterpret_cast<int4*>(
+                  p.partials + ((size_t)(wk.tail * p.split + wk.part) * BM + rloc) * BN + h * 128 + g * 32);
+#pragma unroll
+              for (int j = 0; j < 8; ++j) __stcg(dst + j, make_int4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]));
+            }
           } else if (row_ok) {
             const int64_t n0 = nb + g * 32;
             if (((p.N & 7) == 0) && n0 + 32 <= p.N) {
@@ -748,6 +804,55 @@ to_gemm_ready_kernel(const int8_t* __restrict__ a, int64_t K, __half* __restrict
   }
 }
 
+// The split tiles of a split launch: add each output's K parts and apply the epilogue.
+// Block b covers 8 rows of split tile b / (BM / 8); thread (row, 8-column group).
+__global__ void __launch_bounds__(256)
+split_reduce_kernel(const int32_t* __restrict__ partials, int dp_units, int split, int64_t rows, int64_t N,
+                    const EpiParams ep, __nv_bfloat16* __restrict__ y) {
+  const int tt = blockIdx.x / (BM / 8);
+  const int r = (blockIdx.x % (BM / 8)) * 8 + (threadIdx.x >> 5);
+  const int c = (threadIdx.x & 31) * 8;
+  const int64_t t = dp_units + tt;
+  const int64_t ntm = (rows + BM - 1) / BM;
+  const int64_t m = (t % ntm) * BM + r;
+  const int64_t n0 = (t / ntm) * BN + c;
+  if (m >= rows || n0 >= N) return;
+  const int32_t* src = partials + ((size_t)tt * split * BM + r) * BN + c;
+  int32_t v[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) v[i] = 0;
+  for (int s = 0; s < split; ++s) {
+    const int4 a = __ldcg(reinterpret_cast<const int4*>(src + (size_t)s * BM * BN));
+    const int4 b = __ldcg(reinterpret_cast<const int4*>(src + (size_t)s * BM * BN + 4));
+    v[0] += a.x;
+    v[1] += a.y;
+    v[2] += a.z;
+    v[3] += a.w;
+    v[4] += b.x;
+    v[5] += b.y;
+    v[6] += b.z;
+    v[7] += b.w;
+  }
+  const float sx = epi_row_scale(ep, m);
+  const int zpm = epi_row_zp(ep, m);
+  __nv_bfloat16* yrow = y + m * N;
+  if (((N & 7) == 0) && n0 + 8 <= N) {
+    float f[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) f[i] = epi_apply(ep, v[i], sx, zpm, n0 + i);
+    uint4 o;
+    o.x = pack_bf16x2(f[0], f[1]);
+    o.y = pack_bf16x2(f[2], f[3]);
+    o.z = pack_bf16x2(f[4], f[5]);
+    o.w = pack_bf16x2(f[6], f[7]);
+    *reinterpret_cast<uint4*>(yrow + n0) = o;
+  } else {
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+      if (n0 + i < N) yrow[n0 + i] = __float2bfloat16_rn(epi_apply(ep, v[i], sx, zpm, n0 + i));
+  }
+}
+
 }  // namespace tc
 
 // ------------------------------------------------------------------ host side
@@ -781,6 +886,57 @@ static bool make_map(CUtensorMap* m, CUtensorMapDataType dt, int esize, const vo
 
 int gemm_tc_max_segments() { return tc::MAX_SEG; }
 
+namespace {
+
+// Work decomposition of a dense launch on `pairs_max` CTA pairs.  Only launches with fewer
+// tiles than two waves split: the tiles past the first full wave (all of them when there is
+// none) are cut into `split` parts, as many as fill the idle pairs, at most one per chunk.
+struct SplitPlan {
+  int64_t units;     // work items
+  int dp_units;      // whole tiles (first)
+  int split;         // parts per remaining tile (1: no split)
+  int64_t tail;      // split tiles
+  size_t partial_bytes;
+};
+
+SplitPlan plan_dense(int64_t rows, int64_t N, int64_t K, int64_t pairs_max) {
+  SplitPlan s{};
+  const int64_t tiles = ((rows + tc::BM - 1) / tc::BM) * ((N + tc::BN - 1) / tc::BN);
+  s.units = tiles;
+  s.split = 1;
+  if (pairs_max < 1 || tiles >= 2 * pairs_max) return s;
+  const int64_t nch = ((K + tc::BK - 1) / tc::BK + tc::CHUNK_STEPS - 1) / tc::CHUNK_STEPS;
+  const int64_t full = tiles >= pairs_max ? pairs_max : 0;
+  const int64_t tail = tiles - full;
+  int64_t f = pairs_max / tail;
+  if (f > nch) f = nch;
+  if (f < 2) return s;
+  s.split = (int)f;
+  s.dp_units = (int)full;
+  s.tail = tail;
+  s.units = full + tail * f;
+  s.partial_bytes = (size_t)tail * (size_t)f * tc::BM * tc::BN * sizeof(int32_t);
+  return s;
+}
+
+int sm_count(int dev) {
+  static thread_local int s_dev = -1, s_sms = 0;
+  if (s_dev != dev) {
+    if (cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    s_dev = dev;
+  }
+  return s_sms;
+}
+
+}  // namespace
+
+size_t gemm_split_bytes(int64_t rows, int64_t N, int64_t K) {
+  int dev = 0;
+  if (rows <= 0 || N <= 0 || K <= 0 || cudaGetDevice(&dev) != cudaSuccess) return 0;
+  const SplitPlan s = plan_dense(rows, N, K, sm_count(dev) / 2);
+  return s.split > 1 ? s.partial_bytes : 0;
+}
+
 cudaError_t to_gemm_ready(const int8_t* a, int64_t rows, int64_t K, void* a16, int32_t* norms, cudaStream_t st) {
   if (rows == 0) return cudaSuccess;
   tc::to_gemm_ready_kernel<<<(unsigned)rows, 256, 0, st>>>(a, K, static_cast<__half*>(a16), norms);
@@ -795,14 +951,17 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   static thread_local int s_attr_dev = -1;
-  static thread_local int s_sms = 0;
   if (s_attr_dev != dev) {
-    e = cudaFuncSetAttribute(tc::gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)tc::SMEM_BYTES);
+    e = cudaFuncSetAttribute(tc::gemm_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
+    e = cudaFuncSetAttribute(tc::gemm_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             (int)tc::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     s_attr_dev = dev;
   }
+  const int64_t max_pairs = sm_count(dev) / 2;
+  if (max_pairs < 1) return cudaErrorNotSupported;
   CUtensorMap ma, mb;
   if (!make_map(&ma, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, g.a16, g.rows, g.K, tc::BM_CTA,
                 CU_TENSOR_MAP_SWIZZLE_128B))
@@ -832,11 +991,28 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   p.ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
   p.y = static_cast<__nv_bfloat16*>(g.y);
   p.status = g.status;
+  p.dp_units = 0;
+  p.split = 1;
+  p.partials = nullptr;
   const int64_t nt_n = (g.N + tc::BN - 1) / tc::BN;
+  if (!g.seg && g.split_ws) {
+    const SplitPlan s = plan_dense(g.rows, g.N, g.K, max_pairs);
+    if (s.split > 1 && g.split_bytes >= s.partial_bytes) {
+      p.dp_units = s.dp_units;
+      p.split = s.split;
+      p.partials = static_cast<int32_t*>(g.split_ws);
+      const int pairs = (int)(s.units < max_pairs ? s.units : max_pairs);
+      tc::gemm_tc_kernel<true><<<2 * pairs, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
+      e = cudaGetLastError();
+      if (e != cudaSuccess) return e;
+      tc::split_reduce_kernel<<<(unsigned)(s.tail * (tc::BM / 8)), 256, 0, st>>>(p.partials, s.dp_units, s.split,
+                                                                                 g.rows, g.N, p.ep, p.y);
+      return cudaGetLastError();
+    }
+  }
   const int64_t tiles_ub = g.seg ? ((g.rows + tc::BM - 1) / tc::BM + g.E) * nt_n : ((g.rows + tc::BM - 1) / tc::BM) * nt_n;
-  const int64_t max_pairs = s_sms / 2;
   const int pairs = (int)(tiles_ub < max_pairs ? tiles_ub : max_pairs);
-  tc::gemm_tc_kernel<<<2 * pairs, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
+  tc::gemm_tc_kernel<false><<<2 * pairs, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
   return cudaGetLastError();
 }
 

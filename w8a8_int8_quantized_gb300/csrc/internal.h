@@ -84,6 +84,8 @@ struct GemmArgs {
   const void* bias;     // [N] or nullptr
   void* y;              // [rows, N] bf16
   int32_t* status;
+  void* split_ws;       // optional scratch that lets an under-filled dense launch split along K
+  size_t split_bytes;
 };
 
 // gemm_small.cu: mma.sync s8 weight-streaming kernel (small M)
@@ -97,5 +99,8 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st);
 // int8 codes -> fp16 codes + row L1 norms (K % 16 == 0, 16-byte aligned rows)
 cudaError_t to_gemm_ready(const int8_t* a, int64_t rows, int64_t K, void* a16, int32_t* norms, cudaStream_t st);
 int gemm_tc_max_segments();
+// scratch a dense tcgen05 launch of this shape uses to split along K on the current device
+// (0: the launch does not split)
+size_t gemm_split_bytes(int64_t rows, int64_t N, int64_t K);
 
 }  // namespace w8a8

@@ -21,6 +21,8 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
   requant_word   fp8block_to_int8_rowwise_batched over 8 x [3000, 1500] (rows on 4-byte words)
   max_scale      w8a8_requantize_max_scale on a fused q/k/v weight [4096+1024+1024, 4096]
   asym_linear    w8a8_linear, dynamic asymmetric, M=N=K=4096, with the weight's sums of squares
+  split          w8a8_linear at M=128 on the down projection (N=4096, K=14336) with the K-split
+                 scratch: 16 tiles in 4 parts each, then the reduce kernel
 
 Every case uses a few GB of device memory at most, so a profiler capture of one launch
 stays small.
@@ -139,6 +141,13 @@ def case_fn(name):
         ws = torch.empty(w8.linear_workspace_size(4096, 4096, "dyn_asym"), dtype=torch.uint8, device=dev)
         y = torch.empty(4096, 4096, dtype=torch.bfloat16, device=dev)
         return lambda: w8.linear(x, wq, sw, act_mode="dyn_asym", azp_adj=adj, w_sumsq=wsq, workspace=ws, out=y)
+    if name == "split":
+        x = wl.llama_activations(128, 14336, seed=22).to(dev)
+        wq = torch.randint(-127, 128, (4096, 14336), dtype=torch.int8, device=dev, generator=_gen(23))
+        sw = torch.rand(4096, device=dev, generator=_gen(24)).mul_(1e-3)
+        ws = torch.empty(w8.linear_workspace_size(128, 14336, "dyn_sym", 4096), dtype=torch.uint8, device=dev)
+        y = torch.empty(128, 4096, dtype=torch.bfloat16, device=dev)
+        return lambda: w8.linear(x, wq, sw, workspace=ws, out=y)
     raise SystemExit(f"unknown case {name}")
 
 
