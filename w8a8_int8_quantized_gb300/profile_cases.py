@@ -6,7 +6,9 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
   quant          w8a8_quantize_act, dynamic symmetric, M=8192, K=4096
   quant_packed   w8a8_quantize_act_packed, dynamic symmetric, M=8192, K=4096
   quant_asym     w8a8_quantize_act, dynamic asymmetric, M=8192, K=4096
+  quant_asym_mean  the same on nonzero-mean rows N(0.5, 1) (many exact rounding ties)
   wquant         w8a8_quantize_weight (+ azp_adj), N=28672, K=4096
+  wquant_o       the same on the o-projection weight, N=K=4096
   requant        fp8block_to_int8_rowwise_batched over 8 x [6144, 4096]
   gemm           w8a8_scaled_mm_packed, M=4096, N=28672, K=4096 (Llama-like activations, as the
                  bench: 1% outlier channels, so every tile runs the single fp32 pass)
@@ -47,6 +49,12 @@ def _bf16(shape, std, seed):
 
 def case_fn(name):
     dev = "cuda"
+    if name == "quant_asym_mean":
+        x = torch.randn(8192, 4096, device=dev, generator=_gen(1)).add_(0.5).to(torch.bfloat16)
+        return lambda: w8.quantize_act(x, "dyn_asym")
+    if name == "wquant_o":
+        w = _bf16((4096, 4096), 0.02, 2)
+        return lambda: w8.quantize_weight(w, with_azp_adj=True)
     if name in ("quant", "quant_packed", "quant_asym"):
         x = _bf16((8192, 4096), 1.0, 1)
         if name == "quant":
