@@ -404,6 +404,49 @@ def test_linear_split_k(act, M, N, K, acts):
         assert torch.equal(y.view(torch.int16), y_split.view(torch.int16))
 
 
+@pytest.mark.parametrize("case", ["ragged_k_one_step_part", "ragged_n_scalar_stores", "static_sym_tensor_scale",
+                                  "scaled_mm_dyn_asym"])
+def test_split_k_edges(case):
+    """Edges of the K split: a last part of one 64-wide step with a ragged K tail (M = 5 on the
+    tensor-core engine, K = 3088: 49 steps in parts of 16/16/16/1), an output width that is
+    not a multiple of 8 (the reduce kernel's scalar stores), a per-tensor weight scale
+    without bias, and w8a8_scaled_mm with per-row zero points.  Bit-exact against the oracle
+    and against the unsplit call."""
+    if case == "ragged_k_one_step_part":
+        M, N, K, act, w_mode, bias = 5, 520, 3088, "dyn_sym", w8.W_CHANNEL, True
+        w8.set_gemm_engine(1)
+    elif case == "ragged_n_scalar_stores":
+        M, N, K, act, w_mode, bias = 200, 777, 2048, "dyn_sym", w8.W_CHANNEL, True
+    elif case == "static_sym_tensor_scale":
+        M, N, K, act, w_mode, bias = 96, 1000, 4096, "static_sym", w8.W_TENSOR, False
+    else:
+        M, N, K, act, w_mode, bias = 64, 768, 5120, "dyn_asym", w8.W_CHANNEL, True
+    assert w8.splitk_workspace_size(M, N, K) > 0
+    d = _gemm_case(M, N, K, seed=M + N, act=act, bias=bias, w_mode=w_mode)
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    b = d["b"].to(DEV) if bias else None
+    bb = wl.bits(d["b"]) if bias else None
+    extra = w8.splitk_workspace_size(M, N, K)
+    if case == "scaled_mm_dyn_asym":
+        xq, sx, zp = w8.quantize_act(d["x"].to(DEV), "dyn_asym")
+        adj = w8.azp_adj(wq)
+        base = w8.lib().w8a8_scaled_mm_workspace_size(M, K)
+        run = lambda ws: w8.scaled_mm(xq, wq, sx, sw, "dyn_asym", zp=zp, azp_adj=adj, bias=b, workspace=ws)
+        r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=bb, mode="dyn_asym")
+    else:
+        sc, z = oracle.static_scale_from_tensor(d["x"].float().numpy())
+        kw = {"input_scale": torch.tensor([sc], dtype=torch.float32, device=DEV)} if act == "static_sym" else {}
+        base = w8.linear_workspace_size(M, K, act)
+        run = lambda ws: w8.linear(d["x"].to(DEV), wq, sw, act_mode=act, bias=b, w_mode=w_mode, workspace=ws, **kw)
+        r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=bb, mode=act, input_scale=sc)
+    y_split = run(torch.full((base + extra,), 0x5A, dtype=torch.uint8, device=DEV))
+    y_plain = run(torch.empty(base, dtype=torch.uint8, device=DEV))
+    torch.cuda.synchronize()
+    check_bf16(y_split, r["y_bits"], r["y32"])
+    assert torch.equal(y_plain.view(torch.int16), y_split.view(torch.int16))
+
+
 @pytest.mark.parametrize("w_mode", [w8.W_CHANNEL, w8.W_TENSOR])
 def test_scaled_mm_split_k_extremes(w_mode):
     """acc = +-128*127*K at K = 14336 through split parts (2 tiles in 14 one-chunk parts),
