@@ -109,6 +109,17 @@ def sum_over_ranks(pg, v):
     return float(t.item())
 
 
+def bench_config(world):
+    """The workload both arms run (the reference arm's bounded sample is stated in its
+    cpu_baseline, not here)."""
+    from w8a8_int8_quantized_gb300 import workloads as wl
+    return {"workload": "llama3-8b-decoder-linears", "M": M_TOKENS,
+            "shapes": [[n, N, K] for n, N, K in wl.llama_shapes()],
+            "act": "dynamic per-token symmetric int8", "weight": "per-channel symmetric int8",
+            "l2": "flushed between steps (256 MiB write outside the timed events)",
+            "parallelism": f"replicas x{world} (independent batches)"}
+
+
 def step_ops(M=M_TOKENS):
     from w8a8_int8_quantized_gb300 import workloads as wl
     return sum(2.0 * M * N * K for _, N, K in wl.llama_shapes())
@@ -240,6 +251,7 @@ def run_ours(args, world, rank, pg):
     quant_ms = 0.0
     gemm_flops = 0.0
     quant_bytes = 0.0
+    quant_alg_bytes = 0.0
     per_layer = {}
     for L in layers:
         gq = sum(a.elapsed_time(b) for a, b, _ in L["ev"])
@@ -249,6 +261,7 @@ def run_ours(args, world, rank, pg):
         gemm_ms += gg
         gemm_flops += 2.0 * M_TOKENS * L["N"] * L["K"] * n
         quant_bytes += (M_TOKENS * L["K"] * 4 + M_TOKENS * 8) * n   # bf16 in, fp16 codes out, scale + norm
+        quant_alg_bytes += (M_TOKENS * L["K"] * 3 + M_TOKENS * 4) * n  # bf16 in, int8 codes out, scale
         per_layer[L["name"]] = {
             "N": L["N"], "K": L["K"],
             "gemm_us": round(gg / n * 1e3, 2), "quant_us": round(gq / n * 1e3, 2),
@@ -283,16 +296,20 @@ def run_ours(args, world, rank, pg):
         "metric": METRIC, "value": round(value, 2), "unit": "TOPS", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(ms_total / args.steps, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded; random-init weights)",
-        "config": {"workload": "llama3-8b-decoder-linears", "M": M_TOKENS,
-                   "shapes": [[n, N, K] for n, N, K in wl.llama_shapes()],
-                   "act": "dynamic per-token symmetric int8", "weight": "per-channel symmetric int8",
-                   "l2": "flushed between steps (256 MiB write outside the timed events)",
-                   "parallelism": f"replicas x{world} (independent batches)"},
+        "config": bench_config(world),
         "e2e": e2e,
         "gpu_launches": 2 * len(layers) * args.steps,
         "roofline": roofline,
-        "kernels": {"quantize_act_gbs": round(quant_gbs, 1), "quantize_act_frac_hbm": round(quant_gbs / float(
-            peaks.get("hbm_gbs", 6800.0)), 4), "per_layer": per_layer},
+        "kernels": {
+            # the in-step quantizer writes the GEMM's fp16 operand (4 B per element moved);
+            # the algorithmic figure counts the int8 rule's 3 B per element + 4 B per row
+            "quantize_act_gbs": round(quant_gbs, 1),
+            "quantize_act_frac_hbm": round(quant_gbs / float(peaks.get("hbm_gbs", 6800.0)), 4),
+            "quantize_act_bytes_counted": "4 B/elem (bf16 in, fp16 codes out) + 8 B/row",
+            "quantize_act_algorithmic_gbs": round(quant_alg_bytes / (quant_ms * 1e-3) / 1e9, 1),
+            "quantize_act_algorithmic_frac_hbm": round(quant_alg_bytes / (quant_ms * 1e-3) / 1e9 / float(
+                peaks.get("hbm_gbs", 6800.0)), 4),
+            "per_layer": per_layer},
         "clocks": clk,
         "wall_s": round(wall, 3),
     }
@@ -492,33 +509,31 @@ def components(w8, wl, peaks):
                                                   w_sumsq=wsq))
             out["linear_static_asym_M4096_4096x4096"] = {"us": round(ms * 1e3, 2),
                                                          "TOPS": round(2 * M * 4096 * 4096 / (ms * 1e-3) / 1e12, 1)}
-    # small-M (weight streaming) linears on the gate_up shape
-    wq = torch.randint(-127, 128, (28672, 4096), dtype=torch.int8, device=dev)
-    sw = torch.rand(28672, device=dev)
-    for M in (1, 16, 128, 1024):
-        x = wl.llama_activations(M, 4096, seed=4).to(dev)
-        ws = torch.empty(max(w8.linear_workspace_size(M, 4096, "dyn_sym", 28672), 16), dtype=torch.uint8, device=dev)
-        yb = torch.empty(M, 28672, dtype=torch.bfloat16, device=dev)
-        f0 = _time_launches(lambda: flush.zero_())
-        ms = _time_launches(lambda: (flush.zero_(), w8.linear(x, wq, sw, workspace=ws, out=yb))) - f0
-        wbytes = 28672 * 4096
-        out[f"linear_M{M}_28672x4096"] = {"us": round(ms * 1e3, 2),
-                                          "TOPS": round(2 * M * 28672 * 4096 / (ms * 1e-3) / 1e12, 2),
-                                          "weight_GBps": round(wbytes / (ms * 1e-3) / 1e9, 1),
-                                          "frac_hbm": round(wbytes / (ms * 1e-3) / 1e9 / hbm, 3)}
-    # a few hundred tokens on the down projection: 16 tiles, split along K over the idle pairs
-    wq = torch.randint(-127, 128, (4096, 14336), dtype=torch.int8, device=dev)
-    sw = torch.rand(4096, device=dev)
-    for M in (128, 256):
-        x = wl.llama_activations(M, 14336, seed=5).to(dev)
-        ws = torch.empty(w8.linear_workspace_size(M, 14336, "dyn_sym", 4096), dtype=torch.uint8, device=dev)
-        yb = torch.empty(M, 4096, dtype=torch.bfloat16, device=dev)
-        f0 = _time_launches(lambda: flush.zero_())
-        ms = _time_launches(lambda: (flush.zero_(), w8.linear(x, wq, sw, workspace=ws, out=yb))) - f0
-        out[f"linear_M{M}_4096x14336_split_k"] = {"us": round(ms * 1e3, 2),
-                                                  "TOPS": round(2 * M * 4096 * 14336 / (ms * 1e-3) / 1e12, 1),
-                                                  "frac_tensor": round(2 * M * 4096 * 14336 / (ms * 1e-3) / 1e12 / tf,
-                                                                       3)}
+    # the whole Llama-3-8B grid: every linear at M in {1, 16, 128, 1024, 8192} (M = 4096 is the
+    # headline step), quantizer + GEMM through w8a8_linear with the K-split scratch, L2
+    # flushed before each launch (its own time subtracted).  M <= 16 streams the weight
+    # (fraction of HBM over weight + activation + output bytes); larger M is tensor-bound
+    # (fraction of the bf16 peak the fp16 products run at).
+    f0 = _time_launches(lambda: flush.zero_())
+    for name, N, K in wl.llama_shapes():
+        wq = torch.randint(-127, 128, (N, K), dtype=torch.int8, device=dev)
+        sw = torch.rand(N, device=dev).mul_(1e-3)
+        for M in (1, 16, 128, 1024, 8192):
+            x = wl.llama_activations(M, K, seed=4).to(dev)
+            ws = torch.empty(max(w8.linear_workspace_size(M, K, "dyn_sym", N), 16), dtype=torch.uint8, device=dev)
+            yb = torch.empty(M, N, dtype=torch.bfloat16, device=dev)
+            ms = _time_launches(lambda: (flush.zero_(), w8.linear(x, wq, sw, workspace=ws, out=yb)), reps=5) - f0
+            tops = 2 * M * N * K / (ms * 1e-3) / 1e12
+            e = {"us": round(ms * 1e3, 2), "TOPS": round(tops, 2)}
+            if M <= 16:
+                b = N * K + M * K * 2 + M * N * 2 + N * 4
+                e["GBps"] = round(b / (ms * 1e-3) / 1e9, 1)
+                e["frac_hbm"] = round(b / (ms * 1e-3) / 1e9 / hbm, 3)
+            else:
+                e["frac_tensor"] = round(tops / tf, 3)
+            out[f"linear_{name}_{N}x{K}_M{M}"] = e
+            del x, ws, yb
+        del wq, sw
     # S9 MoE layer (4096 tokens, 32 experts, top-4)
     md = moe_device_inputs(w8, wl)
     ms = _time_launches(lambda: w8.moe_forward(*md["args"]), reps=5)
@@ -594,8 +609,7 @@ def run_reference(args, world, rank):
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt / args.steps * 1e3, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "int8",
         "data": "synthetic (seeded; random-init weights)",
-        "config": {"workload": "llama3-8b-decoder-linears", "M": M_TOKENS,
-                   "shapes": [[n, N, K] for n, N, K in wl.llama_shapes()]},
+        "config": bench_config(world),
         "cpu_baseline": {"value": round(value, 6), "unit": "TOPS", "cores": cores, "kind": "oracle",
                          "sample": f"{sample_rows} of {M_TOKENS} token rows per layer, all four layers, per step"},
         "e2e": {"value": round(value, 6), "unit": "TOPS", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},

@@ -382,7 +382,10 @@ w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void
  *   Limit: roundup(M*K*2, 256) + roundup(M*8, 256) <= 36 MiB (e.g. M*K up to 4096 x 4096);
  *   larger problems return W8A8_ERR_WORKSPACE before any launch.
  *   The first call on each device looks up the buffer's device address (no allocation) and
- *   caches it; make that first call before any stream capture.
+ *   caches it with the CUDA context it was found in; make that first call before any stream
+ *   capture.  A call under another context (a non-primary context, or the new primary
+ *   context after cudaDeviceReset) looks the address up again, and that call too must come
+ *   before any capture.
  *   All calls on a device share the one buffer, which keeps the last call's contents; every
  *   call rewrites all of it that it reads, so nothing needs clearing.  Calls whose work
  *   overlaps on the same GPU (e.g. issued to two streams at once) race on the buffer.

@@ -100,3 +100,19 @@ def test_host_side_argument_checks_need_no_gpu(libpath):
     assert lib.fp8block_to_int8_rowwise_batched_adj(0, None, None, None, None, None, None, None, None, None) == 0
     assert lib.w8a8_set_gemm_engine(5) == 1
     assert lib.w8a8_set_gemm_engine(0) == 0
+
+
+def test_noalloc_applies_the_scaled_mm_checks(libpath):
+    """w8a8_scaled_mm_noalloc rejects exactly what w8a8_scaled_mm rejects, before any CUDA
+    call: here an odd bias pointer (bf16 bias must be 2-byte aligned), a missing azp_adj, a K
+    that is not a multiple of 16, and then its own limit (staged codes beyond its buffer)."""
+    lib = _binding.lib()
+    p = ctypes.c_void_p(256)
+    odd = ctypes.c_void_p(257)
+    f = lib.w8a8_scaled_mm_noalloc
+    assert f(p, p, 4, 4, 16, 0, p, None, None, 0, p, odd, p, None, None) == 3
+    assert f(p, p, 4, 4, 16, 1, p, p, None, 0, p, None, p, None, None) == 1
+    assert f(p, p, 4, 4, 24, 0, p, None, None, 0, p, None, p, None, None) == 3
+    g = lib.w8a8_scaled_mm_packed
+    assert g(p, p, 4, 4, 16, 0, p, None, None, 0, p, None, odd, p, None, None) == 3
+    assert f(p, p, 8192, 16, 4096, 0, p, None, None, 0, p, None, p, None, None) == 7

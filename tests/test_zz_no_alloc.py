@@ -85,3 +85,21 @@ def test_noalloc_rejects_problems_beyond_its_buffer():
     rc = lib.w8a8_scaled_mm_noalloc(_ptr(xq), _ptr(wq), M, N, K, 0, _ptr(sx), None, None, 0, _ptr(sw), None,
                                     _ptr(y), None, stream)
     assert rc == 7  # W8A8_ERR_WORKSPACE
+
+
+def test_noalloc_rejects_a_misaligned_bias():
+    """The bf16 bias must be 2-byte aligned, as for w8a8_scaled_mm: an odd pointer is refused
+    before anything is launched."""
+    lib = w8.lib()
+    stream = P(torch.cuda.current_stream().cuda_stream)
+    M, N, K = 32, 64, 256
+    xq = torch.zeros((M, K), dtype=torch.int8, device=DEV)
+    wq = torch.zeros((N, K), dtype=torch.int8, device=DEV)
+    sx = torch.ones(M, dtype=torch.float32, device=DEV)
+    sw = torch.ones(N, dtype=torch.float32, device=DEV)
+    bias = torch.zeros(N + 1, dtype=torch.bfloat16, device=DEV)
+    y = torch.empty((M, N), dtype=torch.bfloat16, device=DEV)
+    odd = P(bias.data_ptr() + 1)
+    rc = lib.w8a8_scaled_mm_noalloc(_ptr(xq), _ptr(wq), M, N, K, 0, _ptr(sx), None, None, 0, _ptr(sw), odd,
+                                    _ptr(y), None, stream)
+    assert rc == 3  # W8A8_ERR_MISALIGNED

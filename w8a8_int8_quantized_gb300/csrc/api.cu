@@ -18,22 +18,6 @@ bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p
 
 w8a8_status cuda_status(cudaError_t e) { return e == cudaSuccess ? W8A8_OK : W8A8_ERR_CUDA; }
 
-// Only compute capability 10.3 (GB300, sm_103a) runs the kernels built here.
-w8a8_status check_device() {
-  int dev = -1;
-  if (cudaGetDevice(&dev) != cudaSuccess) return W8A8_ERR_CUDA;
-  static thread_local int cached_dev = -2;
-  static thread_local w8a8_status cached = W8A8_OK;
-  if (dev == cached_dev) return cached;
-  int major = 0, minor = 0;
-  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return W8A8_ERR_CUDA;
-  cached = (major == 10 && minor == 3) ? W8A8_OK : W8A8_ERR_UNSUPPORTED;
-  cached_dev = dev;
-  return cached;
-}
-
 bool valid_act_mode(int m) { return m >= W8A8_ACT_DYN_TOKEN_SYM && m <= W8A8_ACT_STATIC_TENSOR_ASYM; }
 bool valid_w_mode(int m) { return m == W8A8_W_CHANNEL || m == W8A8_W_TENSOR; }
 
@@ -62,6 +46,27 @@ w8a8_status run_gemm(GemmArgs g, cudaStream_t st, void* ws, bool small, bool a_i
   return cuda_status(e);
 }
 
+}  // namespace
+
+namespace w8a8 {
+
+// Only compute capability 10.3 (GB300, sm_103a) runs the kernels built here.
+w8a8_status check_device() {
+  int dev = -1;
+  if (cudaGetDevice(&dev) != cudaSuccess) return W8A8_ERR_CUDA;
+  static thread_local int cached_dev = -2;
+  static thread_local w8a8_status cached = W8A8_OK;
+  if (dev == cached_dev) return cached;
+  int major = 0, minor = 0;
+  if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
+    return W8A8_ERR_CUDA;
+  cached = (major == 10 && minor == 3) ? W8A8_OK : W8A8_ERR_UNSUPPORTED;
+  cached_dev = dev;
+  return cached;
+}
+
+// Argument checks of the dense GEMM entry points (every one of them applies the same rules).
 w8a8_status check_scaled_mm_args(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
                                  int act_mode, const float* s_x, const int32_t* zp, const int32_t* azp_adj,
                                  int w_mode, const float* s_w, const void* bias, const void* y) {
@@ -77,7 +82,7 @@ w8a8_status check_scaled_mm_args(const int8_t* xq, const int8_t* wq, int64_t M, 
   return W8A8_OK;
 }
 
-}  // namespace
+}  // namespace w8a8
 
 extern "C" {
 

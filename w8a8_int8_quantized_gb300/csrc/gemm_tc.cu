@@ -80,9 +80,9 @@ constexpr int EPI_WARPS = 8;
 
 struct __align__(8) Bars {
   uint64_t full_a[SA];     // activation tile landed (TMA tx)
-  uint64_t empty_a[SA];    // MMAs reading the activation slot finished (multicast commit)
+  uint64_t stepdone[SA];   // the MMAs of step it (it % SA) finished: frees its activation slot and
+                           // its converted weight slot (one multicast commit per step)
   uint64_t full16[SB];     // both CTAs' operands of the step ready (leader only; 2 arrivals)
-  uint64_t empty16[SB];    // MMAs reading the converted weight slot finished (multicast commit)
   uint64_t full8[S8];      // int8 weight tile landed (TMA tx)
   uint64_t empty8[S8];     // converter done reading the int8 tile
   uint64_t accfull[2];     // accumulator buffer ready (multicast commit)
@@ -384,11 +384,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
   if (threadIdx.x == 0) {
     for (int i = 0; i < SA; ++i) {
       mbar_init(&bars->full_a[i], 1);
-      mbar_init(&bars->empty_a[i], 1);
+      mbar_init(&bars->stepdone[i], 1);
     }
     for (int i = 0; i < SB; ++i) {
       mbar_init(&bars->full16[i], 2);
-      mbar_init(&bars->empty16[i], 1);
     }
     for (int i = 0; i < S8; ++i) {
       mbar_init(&bars->full8[i], 1);
@@ -437,7 +436,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         const int32_t brow = (int32_t)((int64_t)tl.e * p.N + tl.n0 + BN_CTA * rank);
         for (int kb = wk.kb0; kb < wk.kb1; ++kb) {
           const uint32_t sa = na % SA, pha = (na / SA) & 1;
-          if (!wait_bar(&bars->empty_a[sa], pha ^ 1, bars, p.status)) { ok = false; break; }
+          if (!wait_bar(&bars->stepdone[sa], pha ^ 1, bars, p.status)) { ok = false; break; }
           mbar_expect_tx(&bars->full_a[sa], A16);
           tma_load_2d(ringA + sa * A16, &tmA, kb * BK, arow, &bars->full_a[sa]);
           ++na;
@@ -460,15 +459,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     // epilogue overlaps the following tile's MMAs).  A chunked tile takes both: buffer 0
     // receives each 1024-K chunk, buffer 1 is the epilogue's int32 running sum.  Every
     // acquisition of a buffer waits for the epilogue's release of the previous one.
+    // The issuing thread is on the critical path (a cta_group::2 MMA costs ~45 cycles to issue
+    // and a commit ~44): the loop keeps its ring positions as counters, builds descriptors by
+    // adding offsets to precomputed bases, and commits once per step.
     if (rank == 0) {
-      uint32_t it = 0, nbuf = 0;
+      uint32_t nbuf = 0;
       uint32_t acq0 = 0u, acq1 = 0u;  // acquisitions of buffer 0 / 1 so far
+      uint32_t sa = 0, sb = 0, phb = 0;  // next step: activation slot, weight slot and its phase
+      const uint64_t adesc0 = desc_sw128(su32(ringA)), bdesc0 = desc_sw128(su32(ringB16));
       bool ok = true;
       for (int t = pair; t < units && ok; t += npairs) {
         const Work wk = decode_work<SPLIT>(t, bars, p, nkb);
         const bool single = tile_single_pass(p, wk.tl, lane);
         if (lane == 0) {
-          const int spc = single ? wk.kb1 - wk.kb0 : CHUNK_STEPS;
+          const int nsteps = wk.kb1 - wk.kb0;
+          const int spc = single ? nsteps : CHUNK_STEPS;
           uint32_t b = 0;
           if (single) {
             b = nbuf;
@@ -477,27 +482,30 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (!wait_bar(&bars->accempty[1], (acq1 & 1) ^ 1, bars, p.status)) ok = false;
             ++acq1;
           }
-          for (int kb = wk.kb0; kb < wk.kb1 && ok; ++kb, ++it) {
-            const int kr = kb - wk.kb0;  // step within this work item
-            if (kr % spc == 0) {
+          const uint32_t dcol = tmem + b * BN;
+          int kc = 0;  // step within the current chunk (the whole item when single)
+          for (int kr = 0; kr < nsteps && ok; ++kr) {
+            if (kc == 0) {
               const uint32_t a = b ? acq1 : acq0;
               if (!wait_bar(&bars->accempty[b], (a & 1) ^ 1, bars, p.status)) { ok = false; break; }
               if (b) ++acq1; else ++acq0;
               tc_fence_after();
             }
-            const uint32_t sb = it % SB, phb = (it / SB) & 1;
             if (!wait_bar(&bars->full16[sb], phb, bars, p.status)) { ok = false; break; }
             tc_fence_after();
-            const uint32_t sa = it % SA;
-            const uint32_t abase = su32(ringA + sa * A16);
-            const uint32_t bbase = su32(ringB16 + sb * B16);
-#pragma unroll
-            for (int kk = 0; kk < BK / 16; ++kk)
-              mma_f16_pair(tmem + b * BN, desc_sw128(abase + kk * 32), desc_sw128(bbase + kk * 32),
-                           (kr % spc != 0 || kk != 0) ? 1u : 0u);
-            mma_commit_pair(&bars->empty_a[sa]);
-            mma_commit_pair(&bars->empty16[sb]);
-            if (kr % spc == spc - 1 || kb == wk.kb1 - 1) mma_commit_pair(&bars->accfull[b]);
+            const uint64_t ad = adesc0 + (uint64_t)(sa * (A16 >> 4));
+            const uint64_t bd = bdesc0 + (uint64_t)(sb * (B16 >> 4));
+            mma_f16_pair(dcol, ad, bd, kc != 0 ? 1u : 0u);
+            mma_f16_pair(dcol, ad + 2, bd + 2, 1u);
+            mma_f16_pair(dcol, ad + 4, bd + 4, 1u);
+            mma_f16_pair(dcol, ad + 6, bd + 6, 1u);
+            mma_commit_pair(&bars->stepdone[sa]);
+            if (++kc == spc || kr == nsteps - 1) {
+              mma_commit_pair(&bars->accfull[b]);
+              kc = 0;
+            }
+            if (++sa == SA) sa = 0;
+            if (++sb == SB) { sb = 0; phb ^= 1u; }
           }
         }
         ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -531,7 +539,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ++use;
         // every lane waits; the outcome is made warp-uniform so the warp stays converged
         if (!__all_sync(0xffffffffu, wait_bar(&bars->full8[cw], ph, bars, p.status))) { ok = false; break; }
-        if (!__all_sync(0xffffffffu, wait_bar(&bars->empty16[cw], ph ^ 1, bars, p.status))) { ok = false; break; }
+        // the slot's previous use, step it - SB, must be finished
+        if (it >= (uint32_t)SB) {
+          const uint32_t j = it - SB;
+          if (!__all_sync(0xffffffffu, wait_bar(&bars->stepdone[j % SA], (j / SA) & 1, bars, p.status))) {
+            ok = false;
+            break;
+          }
+        }
         // 512 units of 16 int8 (128 rows x 4): 16 per lane, in 4 batches
 #pragma unroll
         for (int bt = 0; bt < 4; ++bt) {

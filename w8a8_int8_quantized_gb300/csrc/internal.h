@@ -88,6 +88,13 @@ struct GemmArgs {
   size_t split_bytes;
 };
 
+// api.cu: the device check every entry point runs, and the argument checks of the dense GEMM
+// entry points (w8a8_scaled_mm, w8a8_scaled_mm_packed, w8a8_scaled_mm_noalloc)
+w8a8_status check_device();
+w8a8_status check_scaled_mm_args(const int8_t* xq, const int8_t* wq, int64_t M, int64_t N, int64_t K,
+                                 int act_mode, const float* s_x, const int32_t* zp, const int32_t* azp_adj,
+                                 int w_mode, const float* s_w, const void* bias, const void* y);
+
 // gemm_small.cu: mma.sync s8 weight-streaming kernel (small M)
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st);
 // Dynamic per-token symmetric decode (at most 8 bf16 rows x) with the quantizer fused into the

@@ -15,6 +15,9 @@
 // Each call writes every byte it later reads (the fp16 codes of all M rows and their norms)
 // before the GEMM kernel reads them, so nothing needs clearing between calls.  Calls whose
 // work overlaps on the same GPU (for example on two streams at once) race on the buffer.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -28,24 +31,53 @@ constexpr int kMaxDevices = 64;
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoallocScratchBytes];
 
 std::mutex g_noalloc_mu;
+// Per device: the context the address was looked up in, and the address.
+CUcontext g_noalloc_ctx[kMaxDevices] = {};
 void* g_noalloc_addr[kMaxDevices] = {};
 
 size_t round256(size_t v) { return (v + 255) & ~(size_t)255; }
 
+PFN_cuCtxGetCurrent_v4000 ctx_getter() {
+  static PFN_cuCtxGetCurrent_v4000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(f);
+  });
+  return fn;
+}
+
+CUcontext current_ctx() {
+  CUcontext c = nullptr;
+  auto fn = ctx_getter();
+  if (fn && fn(&c) != CUDA_SUCCESS) c = nullptr;
+  return c;
+}
+
 // Device address of the scratch array on the current device.  In host code the array's
-// name is only a host-side handle, so the address is asked from the runtime once per
-// device (with that device current) and cached.
+// name is only a host-side handle, so the address is asked from the runtime (with the
+// device current) and cached per device.  The cache remembers the CUDA context it was
+// looked up in and asks again when the current context differs (another context on the
+// device, or a new primary context after cudaDeviceReset), so a stale address of an
+// unloaded module is never handed to a kernel.
 w8a8_status scratch_on_current_device(void** out) {
   int dev = -1;
   if (cudaGetDevice(&dev) != cudaSuccess) return W8A8_ERR_CUDA;
   if (dev < 0 || dev >= kMaxDevices) return W8A8_ERR_UNSUPPORTED;
   std::lock_guard<std::mutex> lock(g_noalloc_mu);
-  if (!g_noalloc_addr[dev]) {
-    void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return W8A8_ERR_CUDA;
-    g_noalloc_addr[dev] = p;
+  const CUcontext before = current_ctx();
+  if (g_noalloc_addr[dev] && before && before == g_noalloc_ctx[dev]) {
+    *out = g_noalloc_addr[dev];
+    return W8A8_OK;
   }
-  *out = g_noalloc_addr[dev];
+  void* p = nullptr;
+  if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || !p) return W8A8_ERR_CUDA;
+  g_noalloc_ctx[dev] = current_ctx();  // the lookup made the device's context current
+  g_noalloc_addr[dev] = p;
+  *out = p;
   return W8A8_OK;
 }
 
@@ -55,27 +87,17 @@ extern "C" w8a8_status w8a8_scaled_mm_noalloc(const int8_t* xq, const int8_t* wq
                                               int act_mode, const float* s_x, const int32_t* zp,
                                               const int32_t* azp_adj, int w_mode, const float* s_w,
                                               const void* bias, void* y, int32_t* dev_status, cudaStream_t stream) {
-  if (M < 0 || N < 0 || K < 1 || K > 131072) return W8A8_ERR_INVALID_ARG;
-  if (act_mode < W8A8_ACT_DYN_TOKEN_SYM || act_mode > W8A8_ACT_STATIC_TENSOR_ASYM) return W8A8_ERR_INVALID_ARG;
-  if (w_mode != W8A8_W_CHANNEL && w_mode != W8A8_W_TENSOR) return W8A8_ERR_INVALID_ARG;
-  if (K % 16 != 0) return W8A8_ERR_MISALIGNED;
-  if (M == 0 || N == 0) return W8A8_OK;
-  if (!xq || !wq || !s_x || !s_w || !y) return W8A8_ERR_INVALID_ARG;
-  if (act_mode == W8A8_ACT_DYN_TOKEN_ASYM && (!zp || !azp_adj)) return W8A8_ERR_INVALID_ARG;
-  if (act_mode == W8A8_ACT_STATIC_TENSOR_ASYM && !azp_adj) return W8A8_ERR_INVALID_ARG;
-  if (((reinterpret_cast<uintptr_t>(xq) | reinterpret_cast<uintptr_t>(wq) | reinterpret_cast<uintptr_t>(y)) & 15) != 0)
-    return W8A8_ERR_MISALIGNED;
+  // the same checks as w8a8_scaled_mm (shapes, modes, null pointers, 16-byte operands,
+  // 2-byte bias), then the one limit of this entry point: the staged codes must fit
+  w8a8_status s = w8a8::check_scaled_mm_args(xq, wq, M, N, K, act_mode, s_x, zp, azp_adj, w_mode, s_w, bias, y);
+  if (s != W8A8_OK || M == 0 || N == 0) return s;
   const size_t codes_bytes = round256((size_t)M * (size_t)K * 2);
   // codes, then the row L1 norms and sums of squares (2 * M int32) that the conversion writes
   if (codes_bytes + round256((size_t)M * 8) > kNoallocScratchBytes) return W8A8_ERR_WORKSPACE;
-  int dev = -1, major = 0, minor = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess)
-    return W8A8_ERR_CUDA;
-  if (major != 10 || minor != 3) return W8A8_ERR_UNSUPPORTED;
+  s = w8a8::check_device();
+  if (s != W8A8_OK) return s;
   void* scratch = nullptr;
-  w8a8_status s = scratch_on_current_device(&scratch);
+  s = scratch_on_current_device(&scratch);
   if (s != W8A8_OK) return s;
   uint8_t* base = static_cast<uint8_t*>(scratch);
   int32_t* norms = reinterpret_cast<int32_t*>(base + codes_bytes);
