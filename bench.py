@@ -28,7 +28,20 @@ if HERE not in sys.path:
     sys.path.insert(0, HERE)
 
 METRIC = "W8A8 linear TOPS (quant+GEMM) at Llama-3-8B shapes; % of INT8 tensor peak"
-INT8_MMA_SYNC_TOPS = 150.0  # measured dense rate of the GPU's only INT8 tensor instruction (warp MMA)
+def engine_rate(key, default):
+    """A rate recorded in profiles/engine_rates.md (written from the engine probe's output)."""
+    p = os.path.join(HERE, "profiles", "engine_rates.md")
+    try:
+        for line in open(p):
+            if line.startswith(key + ":"):
+                return float(line.split(":", 1)[1])
+    except (OSError, ValueError):
+        pass
+    return default
+
+
+# measured dense rate of the GPU's only INT8 tensor instruction (warp MMA s8)
+INT8_MMA_SYNC_TOPS = engine_rate("int8_mma_sync_tops", 158.5)
 M_TOKENS = 4096
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 
@@ -282,9 +295,11 @@ def run_ours(args, world, rank, pg):
         "peak_source": f"{peak_src} bf16 burst (fp16 runs at the bf16 rate)",
         "per_launch_flops": "2*M*N*K of each GEMM launch (M=4096)",
         # sm_103a has no tcgen05 integer MMA kind; its one INT8 tensor path, the warp-level
-        # mma.sync.m16n8k32.s8, was probed at this rate on the same GPUs: the int8 products
-        # run instead as exact fp16 products on the tcgen05 tensor cores (peak above)
+        # mma.sync.m16n8k32.s8, was probed at this rate on the same GPUs
+        # (profiles/engine_rates.md): the int8 products run instead as exact fp16 products
+        # on the tcgen05 tensor cores (peak above)
         "int8_mma_sync_tops": INT8_MMA_SYNC_TOPS,
+        "int8_mma_sync_source": "profiles/engine_rates.md (engine_probe.cu)",
         "achieved_over_int8_mma_sync": round(achieved / INT8_MMA_SYNC_TOPS, 2),
     }
     quant_gbs = quant_bytes / (quant_ms * 1e-3) / 1e9

@@ -75,6 +75,20 @@ int w8a8_version(void);
 w8a8_status w8a8_set_gemm_engine(int engine);
 
 /*
+ * w8a8_test_requant_wait_fault -- test hook for the device-side timeout path
+ * ([Kunlun-INT8] 验证: the converter's tests include illegal inputs; this one makes a wait
+ * run out on purpose).  Not for production use; process-wide; off by default.
+ *   wait_limit_ns: limit of the requantizer row ring's bounded waits (100 us .. 2 s; 0
+ *   restores the default 2 s).  extra_tx_bytes (0 .. 4096): bytes that the barrier of the
+ *   first row of the next ring launches expects beyond what the row's bulk copy delivers,
+ *   so that wait cannot complete: the copy itself lands as usual, the wait runs out after
+ *   wait_limit_ns, the kernel records W8A8_ERR_TIMEOUT in dev_status and returns; nothing
+ *   faults or hangs, and the context stays usable.  Call with (0, 0) to switch it off.
+ *   Returns W8A8_ERR_INVALID_ARG for values out of range.
+ */
+w8a8_status w8a8_test_requant_wait_fault(uint32_t extra_tx_bytes, uint64_t wait_limit_ns);
+
+/*
  * w8a8_quantize_act -- activation quantization ([SGLang-CT] item 3, per_token_quant_int8;
  * per-row rule of [Kunlun-INT8] 转换关系; modes of [vLLM-W8A8] 4.1/4.2).
  *   x      bf16 [M, K] with row stride ldx (elements, ldx >= K).

@@ -470,8 +470,9 @@ def moe_forward(x_bits, topk_ids, topk_w, w13_q, s13, w2_q, s2, rows=None):
     ([Kunlun-INT8]: per-token dynamic symmetric INT8 activations).
     rows: optional token indices to evaluate (others left zero) so that large
     cases can be sampled.
-    Returns dict(y_bits [T, H], h_bits [R, 2I], out_bits [R, H]) where h/out are
-    in sorted-row order (zero for rows not evaluated).
+    Returns dict(y_bits [T, H], y32 [T, H] (the float32 sums before the bf16 rounding),
+    h_bits [R, 2I], out_bits [R, H]) where h/out are in sorted-row order (zero for rows
+    not evaluated).
     """
     x = bf16_bits_to_f32(x_bits)
     T, H = x.shape
@@ -508,4 +509,4 @@ def moe_forward(x_bits, topk_ids, topk_w, w13_q, s13, w2_q, s2, rows=None):
             acc = (acc + (F32(topk_w[t, j]) * o).astype(F32)).astype(F32)
         y[t] = acc
     y_bits = f32_to_bf16_bits(y)
-    return dict(y_bits=y_bits, h_bits=h_bits, out_bits=out_bits, seg=seg, tok=tok, slot=slot)
+    return dict(y_bits=y_bits, y32=y, h_bits=h_bits, out_bits=out_bits, seg=seg, tok=tok, slot=slot)

@@ -33,6 +33,7 @@ SIGNATURES = {
     "w8a8_status_string": (ctypes.c_char_p, [_I]),
     "w8a8_version": (_I, []),
     "w8a8_set_gemm_engine": (_I, [_I]),
+    "w8a8_test_requant_wait_fault": (_I, [ctypes.c_uint32, ctypes.c_uint64]),
     "w8a8_quantize_act": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
     "w8a8_scaled_mm_workspace_size": (_SZ, [_I64, _I64]),
     "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),

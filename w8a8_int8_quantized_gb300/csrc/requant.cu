@@ -11,6 +11,8 @@
 // through a by-value descriptor table, optionally writing each row's code sum (azp_adj).
 // Also here: the requantization of a fused weight's per-tensor partitions to their largest
 // scale ("[SGLang] W4A8, W8A8, W4A4", item 7, requantize_with_max_scale).
+#include <atomic>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -181,8 +183,18 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
                "l"(src), "r"(bytes), "r"(bar)
                : "memory");
 }
-// waits for the phase with the given parity; false after 2 s
-__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
+// Bounded waits of the row ring: the limit (2 s) and, for tests of the timeout path only, a
+// number of bytes that the first row's barrier of the launch expects beyond what its bulk
+// copy delivers, so that its wait cannot complete (set by w8a8_test_requant_wait_fault; both
+// off by default).
+struct RingWait {
+  uint64_t limit_ns;
+  uint32_t extra_tx;
+  uint32_t pad;
+};
+
+// waits for the phase with the given parity; false once `limit_ns` has passed
+__device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
   uint64_t t0;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t0));
   for (;;) {
@@ -194,7 +206,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
     if (ok) return true;
     uint64_t t;
     asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    if (t - t0 > 2000000000ull) return false;
+    if (t - t0 > limit_ns) return false;
   }
 }
 
@@ -204,7 +216,7 @@ __device__ __forceinline__ bool bar_wait(uint32_t bar, uint32_t parity) {
 // warps compute.  slot >= the largest K of the batch, a multiple of 128.
 template <int WARPS, bool ADJ>
 __global__ void __launch_bounds__(WARPS * 32, 1024 / (WARPS * 32))
-requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
+requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st, const RingWait rw) {
   extern __shared__ __align__(128) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* ring = smem + (size_t)warp * slot;
@@ -219,6 +231,10 @@ requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
     asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
     const ReqMat& m0 = find_mat(b, gw);
+    // (the test hook's extra bytes go to the launch's first row only; the copy itself
+    // completes as usual)
+    if (gw == 0 && rw.extra_tx)
+      asm volatile("mbarrier.expect_tx.relaxed.cta.shared::cta.b64 [%0], %1;\n" ::"r"(sbar), "r"(rw.extra_tx) : "memory");
     bulk_load(sring, m0.w + (gw - m0.row0) * (int64_t)m0.K, (uint32_t)m0.K, sbar);
   }
   __syncwarp();
@@ -227,7 +243,7 @@ requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st) {
     const ReqMat& mt = find_mat(b, grow);
     const int64_t i = grow - mt.row0;
     const int K = mt.K, nv = K / 16, nbc = (K + 127) / 128;
-    if (!__all_sync(0xffffffffu, bar_wait(sbar, phase))) {
+    if (!__all_sync(0xffffffffu, bar_wait(sbar, phase, rw.limit_ns))) {
       if (lane == 0) report_status(st, W8A8_ERR_TIMEOUT);
       return;
     }
@@ -320,6 +336,17 @@ static size_t ring_smem(int warps, int slot) {
   return (size_t)warps * slot + (size_t)warps * (slot / 128) * 4 + (size_t)warps * 8;
 }
 
+static std::atomic<uint64_t> g_ring_limit_ns{2000000000ull};
+static std::atomic<uint32_t> g_ring_extra_tx{0u};
+
+static RingWait ring_wait() {
+  RingWait w;
+  w.limit_ns = g_ring_limit_ns.load(std::memory_order_relaxed);
+  w.extra_tx = g_ring_extra_tx.load(std::memory_order_relaxed);
+  w.pad = 0;
+  return w;
+}
+
 template <int WARPS, bool ADJ>
 static cudaError_t launch_ring(const ReqBatch& b, int slot, int32_t* st, cudaStream_t stream) {
   static thread_local int s_dev = -1, s_sms = 0;
@@ -345,7 +372,8 @@ static cudaError_t launch_ring(const ReqBatch& b, int slot, int32_t* st, cudaStr
   if (per_sm < 1) per_sm = 1;
   const int64_t need = (b.total_rows + WARPS - 1) / WARPS;
   const int64_t cap = (int64_t)s_sms * per_sm;
-  requant_ring_kernel<WARPS, ADJ><<<(unsigned)(need < cap ? need : cap), WARPS * 32, smem, stream>>>(b, slot, st);
+  requant_ring_kernel<WARPS, ADJ><<<(unsigned)(need < cap ? need : cap), WARPS * 32, smem, stream>>>(b, slot, st,
+                                                                                                  ring_wait());
   return cudaGetLastError();
 }
 
@@ -671,3 +699,11 @@ int requant_path(const uint8_t* w, const int8_t* q, int64_t K) {
 }
 
 }  // namespace w8a8
+
+extern "C" w8a8_status w8a8_test_requant_wait_fault(uint32_t extra_tx_bytes, uint64_t wait_limit_ns) {
+  if (extra_tx_bytes > 4096 || (wait_limit_ns != 0 && (wait_limit_ns < 100000ull || wait_limit_ns > 2000000000ull)))
+    return W8A8_ERR_INVALID_ARG;
+  w8a8::g_ring_extra_tx.store(extra_tx_bytes, std::memory_order_relaxed);
+  w8a8::g_ring_limit_ns.store(wait_limit_ns ? wait_limit_ns : 2000000000ull, std::memory_order_relaxed);
+  return W8A8_OK;
+}
