@@ -140,7 +140,10 @@ def step_ops(M=M_TOKENS):
 
 # --------------------------------------------------------------------------- clocks
 class ClockSampler:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    """nvidia-smi samples every 200 ms.  Started (and given time to come up) before the
+    warm-up, because its start-up stalled GPU work for tens of milliseconds when it began with
+    the timed region; only samples stamped inside the timed window are reported."""
+    FIELDS = ("timestamp,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -148,6 +151,7 @@ class ClockSampler:
         self.proc = None
         self.gpu = gpu_index
         self.out = None
+        self.window = None
 
     def start(self):
         try:
@@ -155,8 +159,13 @@ class ClockSampler:
             self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
                                           "--format=csv,noheader,nounits", "-lms", "200"],
                                          stdout=self.out, stderr=subprocess.DEVNULL)
+            time.sleep(1.0)
         except Exception:
             self.proc = None
+
+    def mark(self, t0, t1):
+        """The timed window, as time.time() values."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -169,21 +178,40 @@ class ClockSampler:
         self.out.seek(0)
         rows = [r.strip().split(",") for r in self.out.read().strip().splitlines() if r.strip()]
         self.out.close()
-        sm, smax, reasons = [], 0.0, set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for r in rows:
+        import datetime
+
+        def in_window(r):
+            if self.window is None:
+                return True
             try:
-                sm.append(float(r[1]))
-                smax = max(smax, float(r[2]))
-                for nm, v in zip(names, r[5:9]):
-                    if "Active" in v and "Not" not in v:
-                        reasons.add(nm)
+                ts = datetime.datetime.strptime(r[0].strip(), "%Y/%m/%d %H:%M:%S.%f").timestamp()
             except (ValueError, IndexError):
-                continue
+                return False
+            return self.window[0] - 0.2 <= ts <= self.window[1] + 0.2
+
+        def summarize(sel):
+            sm, smax, reasons = [], 0.0, set()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for r in sel:
+                try:
+                    sm.append(float(r[1]))
+                    smax = max(smax, float(r[2]))
+                    for nm, v in zip(names, r[5:9]):
+                        if "Active" in v and "Not" not in v:
+                            reasons.add(nm)
+                except (ValueError, IndexError):
+                    continue
+            return sm, smax, reasons
+
+        sm, smax, reasons = summarize([r for r in rows if in_window(r)])
+        scope = "timed window"
+        if not sm:  # no sample stamped inside a short window: report the whole loaded run
+            sm, smax, reasons = summarize(rows)
+            scope = "warm-up and timed region"
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": smax, "reasons": sorted(reasons),
-                "samples": len(sm)}
+                "samples": len(sm), "scope": scope}
 
 
 # --------------------------------------------------------------------------- our arm
@@ -232,15 +260,16 @@ def run_ours(args, world, rank, pg):
             if rc:
                 raise RuntimeError("library call failed")
 
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
     for _ in range(args.warmup):
         step(False)
         flush.zero_()
     torch.cuda.synchronize()
     barrier(pg)
     torch.cuda.synchronize()
-    clocks = ClockSampler(torch.cuda.current_device())
-    clocks.start()
     wall0 = time.perf_counter()
+    tw0 = time.time()
     step_events = []
     for _ in range(args.steps):
         flush.zero_()           # L2 flush between steps, outside the timed events
@@ -252,6 +281,7 @@ def run_ours(args, world, rank, pg):
         step_events.append((s0, s1))
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
+    clocks.mark(tw0, time.time())
     clk = clocks.stop()
     barrier(pg)
     torch.cuda.synchronize()

@@ -75,6 +75,20 @@ int w8a8_version(void);
 w8a8_status w8a8_set_gemm_engine(int engine);
 
 /*
+ * Bounds-checked build.  Built with -DW8A8_DEBUG (libw8a8_debug.so, `build.py --debug`),
+ * every kernel checks the index invariants of its global-memory accesses (row within the
+ * rows, column block within K or N, segment within E, partial tile within the split
+ * scratch); a violated one records a site code in a caller-provided device int32 (the
+ * first code wins, 0 = none) and skips that access instead of trapping.  No counterpart on
+ * the pages: it is a test instrument.
+ *   w8a8_debug_set_error_word: registers the device word (device pointer, or NULL to stop
+ *   recording); W8A8_ERR_UNSUPPORTED in the release build.  w8a8_debug_build: 1 in the
+ *   bounds-checked build, 0 otherwise.
+ */
+w8a8_status w8a8_debug_set_error_word(int32_t* word);
+int w8a8_debug_build(void);
+
+/*
  * w8a8_test_requant_wait_fault -- test hook for the device-side timeout path
  * ([Kunlun-INT8] 验证: the converter's tests include illegal inputs; this one makes a wait
  * run out on purpose).  Not for production use; process-wide; off by default.

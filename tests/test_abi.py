@@ -100,6 +100,9 @@ def test_host_side_argument_checks_need_no_gpu(libpath):
     assert lib.fp8block_to_int8_rowwise_batched_adj(0, None, None, None, None, None, None, None, None, None) == 0
     assert lib.w8a8_set_gemm_engine(5) == 1
     assert lib.w8a8_set_gemm_engine(0) == 0
+    # the release build is not the bounds-checked one
+    assert lib.w8a8_debug_build() == 0
+    assert lib.w8a8_debug_set_error_word(None) == 2
     # the timeout test hook: values out of range are refused, (0, 0) switches it off
     assert lib.w8a8_test_requant_wait_fault(8192, 0) == 1
     assert lib.w8a8_test_requant_wait_fault(16, 10) == 1

@@ -34,6 +34,8 @@ SIGNATURES = {
     "w8a8_version": (_I, []),
     "w8a8_set_gemm_engine": (_I, [_I]),
     "w8a8_test_requant_wait_fault": (_I, [ctypes.c_uint32, ctypes.c_uint64]),
+    "w8a8_debug_set_error_word": (_I, [_P]),
+    "w8a8_debug_build": (_I, []),
     "w8a8_quantize_act": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
     "w8a8_scaled_mm_workspace_size": (_SZ, [_I64, _I64]),
     "w8a8_scaled_mm": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
@@ -72,6 +74,17 @@ class W8A8Error(RuntimeError):
         self.code = code
 
 
+def load_library(path):
+    """Load a build of the library (libw8a8.so, or the bounds-checked libw8a8_debug.so) with
+    the C signatures declared."""
+    L = ctypes.CDLL(path)
+    for name, (res, args) in SIGNATURES.items():
+        f = getattr(L, name)
+        f.restype = res
+        f.argtypes = args
+    return L
+
+
 def lib():
     """Load libw8a8.so (raises if it is not built or cannot be loaded)."""
     global _lib
@@ -79,13 +92,27 @@ def lib():
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"{LIB_PATH} is missing: build it with "
                                "`python -m w8a8_int8_quantized_gb300.build`")
-        L = ctypes.CDLL(LIB_PATH)
-        for name, (res, args) in SIGNATURES.items():
-            f = getattr(L, name)
-            f.restype = res
-            f.argtypes = args
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
+
+
+class using_library:
+    """Context manager: every call of this module goes to library `L` (for example the
+    bounds-checked build) until the block ends."""
+
+    def __init__(self, L):
+        self.L = L
+
+    def __enter__(self):
+        global _lib
+        self.prev = lib()
+        _lib = self.L
+        return self.L
+
+    def __exit__(self, *exc):
+        global _lib
+        _lib = self.prev
+        return False
 
 
 def _ptr(t):

@@ -3,7 +3,10 @@
 Each .cu under csrc/ is compiled in parallel with nvcc (one -gencode, -lineinfo, -O3,
 IEEE division: no fast-math), then linked into a shared library next to this file.
 Runs on a machine without a GPU (nvcc cross-compiles).  Usage:
-    python -m w8a8_int8_quantized_gb300.build [--force]
+    python -m w8a8_int8_quantized_gb300.build [--force] [--debug]
+--debug builds libw8a8_debug.so instead: the same sources with -DW8A8_DEBUG, whose kernels
+check the index invariants of their global-memory accesses and report a violated one in a
+registered error word (w8a8_debug_set_error_word) instead of trapping.
 """
 
 import concurrent.futures as cf
@@ -18,6 +21,8 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libw8a8.so")
+BUILD_DEBUG = os.path.join(HERE, "_build_debug")
+LIB_DEBUG = os.path.join(HERE, "libw8a8_debug.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2",
@@ -42,24 +47,26 @@ def _deps():
     return files
 
 
-def up_to_date():
-    if not os.path.exists(LIB):
+def up_to_date(lib=LIB):
+    if not os.path.exists(lib):
         return False
-    t = os.path.getmtime(LIB)
+    t = os.path.getmtime(lib)
     return all(os.path.getmtime(f) <= t for f in _deps())
 
 
-def build(force=False, verbose=False):
-    """Compile and link libw8a8.so; returns its path."""
-    if not force and up_to_date():
-        return LIB
+def build(force=False, verbose=False, debug=False):
+    """Compile and link libw8a8.so (or, with debug, libw8a8_debug.so); returns its path."""
+    lib, bdir = (LIB_DEBUG, BUILD_DEBUG) if debug else (LIB, BUILD)
+    if not force and up_to_date(lib):
+        return lib
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
+    os.makedirs(bdir, exist_ok=True)
     srcs = sources()
+    extra = ["-DW8A8_DEBUG"] if debug else []
 
     def compile_one(src):
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
-        cmd = [nvcc, *ARCH, *FLAGS, "-c", src, "-o", obj]
+        obj = os.path.join(bdir, os.path.basename(src)[:-3] + ".o")
+        cmd = [nvcc, *ARCH, *FLAGS, *extra, "-c", src, "-o", obj]
         if verbose:
             cmd.insert(1, "-Xptxas=-v")
         r = subprocess.run(cmd, capture_output=True, text=True)
@@ -73,14 +80,14 @@ def build(force=False, verbose=False):
         for _, err in results:
             sys.stderr.write(err)
     objs = [o for o, _ in results]
-    tmp = LIB + ".tmp"
+    tmp = lib + ".tmp"
     cmd = [nvcc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv))
+    print(build(force="--force" in sys.argv, verbose="-v" in sys.argv, debug="--debug" in sys.argv))

@@ -102,6 +102,27 @@ const char* w8a8_status_string(int s) {
 
 int w8a8_version(void) { return 100; }
 
+w8a8_status w8a8_debug_set_error_word(int32_t* word) {
+#ifdef W8A8_DEBUG
+  if (debug_register_quant(word) != cudaSuccess || debug_register_requant(word) != cudaSuccess ||
+      debug_register_gemm_tc(word) != cudaSuccess || debug_register_gemm_small(word) != cudaSuccess ||
+      debug_register_moe_route(word) != cudaSuccess)
+    return W8A8_ERR_CUDA;
+  return W8A8_OK;
+#else
+  (void)word;
+  return W8A8_ERR_UNSUPPORTED;
+#endif
+}
+
+int w8a8_debug_build(void) {
+#ifdef W8A8_DEBUG
+  return 1;
+#else
+  return 0;
+#endif
+}
+
 w8a8_status w8a8_set_gemm_engine(int engine) {
   if (engine < 0 || engine > 2) return W8A8_ERR_INVALID_ARG;
   g_engine = engine;

@@ -263,6 +263,31 @@ __device__ __forceinline__ float epi_apply(const EpiParams& p, int32_t acc, floa
   return y;
 }
 
+// ---------------------------------------------------------------------------
+// Bounds-checked build (-DW8A8_DEBUG, libw8a8_debug.so): W8A8_DOK(cond, site) guards a
+// global-memory access whose index the kernel itself computed.  When the invariant fails it
+// records `site` in the error word registered with w8a8_debug_set_error_word (first code
+// wins) and the access is skipped, so a broken index never reaches memory and never traps.
+// In the release build it is the constant true and compiles away.
+// ---------------------------------------------------------------------------
+#ifdef W8A8_DEBUG
+static __device__ int32_t* g_w8a8_debug_word = nullptr;
+__device__ __forceinline__ bool w8a8_dok(bool ok, int site) {
+  if (!ok) {
+    int32_t* w = g_w8a8_debug_word;
+    if (w) atomicCAS(w, 0, site);
+  }
+  return ok;
+}
+#define W8A8_DOK(cond, site) ::w8a8::w8a8_dok((cond), (site))
+// this translation unit's copy of the error-word pointer (called from its register function)
+static inline cudaError_t w8a8_debug_register_here(int32_t* word) {
+  return cudaMemcpyToSymbol(g_w8a8_debug_word, &word, sizeof(word));
+}
+#else
+#define W8A8_DOK(cond, site) true
+#endif
+
 // Record a device-side condition: the first non-zero code wins.
 __device__ __forceinline__ void report_status(int32_t* st, int code) {
   if (st) atomicCAS(st, 0, code);

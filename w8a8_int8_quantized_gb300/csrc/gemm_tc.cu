@@ -279,6 +279,7 @@ __device__ __forceinline__ Tile decode_tile(int t, const Bars* bars, int E, cons
   r.row0 = s0 + (int64_t)(local % ntm) * BM;
   r.row_end = s1;
   r.n0 = (int64_t)(local / ntm) * BN;
+  (void)W8A8_DOK(lo >= 0 && lo < E && r.row0 < r.row_end && r.row_end <= rows, 301);
   return r;
 }
 
@@ -699,12 +700,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 o.y = pack_bf16x2(f[2], f[3]);
                 o.z = pack_bf16x2(f[4], f[5]);
                 o.w = pack_bf16x2(f[6], f[7]);
-                *reinterpret_cast<uint4*>(yrow + n0 + 8 * j) = o;
+                if (W8A8_DOK(m < p.rows && n0 + 8 * j + 8 <= p.N, 302)) *reinterpret_cast<uint4*>(yrow + n0 + 8 * j) = o;
               }
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (n0 + i < p.N)
+                if (n0 + i < p.N && W8A8_DOK(m < p.rows, 303))
                   yrow[n0 + i] = __float2bfloat16_rn(epi_apply(ep, (int32_t)__uint_as_float(r[i]), sx, zpm, n0 + i));
             }
             continue;
@@ -724,7 +725,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
           if (!last) {
             tmem_st32(lanebase + BN + g * 32, v);
           } else if (SPLIT && wk.tail >= 0) {
-            if (row_ok) {  // this part's int32 sums; the reduce kernel applies the epilogue
+            if (row_ok && W8A8_DOK(wk.part < p.split && rloc < BM && wk.tail >= 0, 304)) {  // this part's int32 sums; the reduce kernel applies the epilogue
               int4* dst = reinterpret_cast<int4*>(
                   p.partials + ((size_t)(wk.tail * p.split + wk.part) * BM + rloc) * BN + h * 128 + g * 32);
 #pragma unroll
@@ -743,12 +744,13 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 o.y = pack_bf16x2(f[2], f[3]);
                 o.z = pack_bf16x2(f[4], f[5]);
                 o.w = pack_bf16x2(f[6], f[7]);
-                *reinterpret_cast<uint4*>(yrow + n0 + 8 * j) = o;
+                if (W8A8_DOK(m < p.rows && n0 + 8 * j + 8 <= p.N, 305)) *reinterpret_cast<uint4*>(yrow + n0 + 8 * j) = o;
               }
             } else {
 #pragma unroll
               for (int i = 0; i < 32; ++i)
-                if (n0 + i < p.N) yrow[n0 + i] = __float2bfloat16_rn(epi_apply(ep, v[i], sx, zpm, n0 + i));
+                if (n0 + i < p.N && W8A8_DOK(m < p.rows, 306))
+                  yrow[n0 + i] = __float2bfloat16_rn(epi_apply(ep, v[i], sx, zpm, n0 + i));
             }
           }
         }
@@ -832,6 +834,7 @@ split_reduce_kernel(const int32_t* __restrict__ partials, int dp_units, int spli
   const int64_t m = (t % ntm) * BM + r;
   const int64_t n0 = (t / ntm) * BN + c;
   if (m >= rows || n0 >= N) return;
+  if (!W8A8_DOK(r < BM && c + 8 <= BN, 307)) return;
   const int32_t* src = partials + ((size_t)tt * split * BM + r) * BN + c;
   int32_t v[8];
 #pragma unroll
@@ -1030,5 +1033,9 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   tc::gemm_tc_kernel<false><<<2 * pairs, tc::NUM_THREADS, tc::SMEM_BYTES, st>>>(ma, mb, p);
   return cudaGetLastError();
 }
+
+#ifdef W8A8_DEBUG
+cudaError_t debug_register_gemm_tc(int32_t* word) { return w8a8_debug_register_here(word); }
+#endif
 
 }  // namespace w8a8

@@ -95,6 +95,15 @@ w8a8_status check_scaled_mm_args(const int8_t* xq, const int8_t* wq, int64_t M, 
                                  int act_mode, const float* s_x, const int32_t* zp, const int32_t* azp_adj,
                                  int w_mode, const float* s_w, const void* bias, const void* y);
 
+#ifdef W8A8_DEBUG
+// bounds-checked build: each translation unit's copy of the error-word pointer
+cudaError_t debug_register_quant(int32_t* word);
+cudaError_t debug_register_requant(int32_t* word);
+cudaError_t debug_register_gemm_tc(int32_t* word);
+cudaError_t debug_register_gemm_small(int32_t* word);
+cudaError_t debug_register_moe_route(int32_t* word);
+#endif
+
 // gemm_small.cu: mma.sync s8 weight-streaming kernel (small M)
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st);
 // Dynamic per-token symmetric decode (at most 8 bf16 rows x) with the quantizer fused into the

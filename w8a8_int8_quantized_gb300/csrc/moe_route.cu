@@ -202,4 +202,8 @@ cudaError_t moe_route(const float* logits, int64_t T, int E, int topk, int32_t* 
   return cudaGetLastError();
 }
 
+#ifdef W8A8_DEBUG
+cudaError_t debug_register_moe_route(int32_t* word) { return w8a8_debug_register_here(word); }
+#endif
+
 }  // namespace w8a8

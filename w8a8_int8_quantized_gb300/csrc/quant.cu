@@ -141,7 +141,7 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int idx = threadIdx.x + i * THREADS;
-      if (idx < nvec) dst[i] = ldg_stream(xr + idx);
+      if (idx < nvec && W8A8_DOK(r < rows && src >= 0, 101)) dst[i] = ldg_stream(xr + idx);
     }
   };
   auto finish_sums = [&](int b, int64_t r) {
@@ -152,6 +152,7 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       if (F16) a += sh_abs[b][i];
       if (SQ) q2 += sh_sq[b][i];
     }
+    if (!W8A8_DOK(r < rows, 104)) return;
     if (SUM) sum_out[r] = s;
     if (F16) norm_out[r] = a;         // L1 norm of the codes
     if (SQ) norm_out[rows + r] = q2;  // sum of their squares, right after the rows' L1 norms
@@ -274,13 +275,13 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
           uint4 o;
           i8x4_to_f16x4(w0, o.x, o.y);
           i8x4_to_f16x4(w1, o.z, o.w);
-          reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
+          if (W8A8_DOK(row < rows && (int64_t)(idx + 1) * 8 <= K, 102)) reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
         } else {
-          reinterpret_cast<uint2*>(q + row * K)[idx] = make_uint2(w0, w1);
+          if (W8A8_DOK(row < rows && (int64_t)(idx + 1) * 8 <= K, 102)) reinterpret_cast<uint2*>(q + row * K)[idx] = make_uint2(w0, w1);
         }
       }
     }
-    if (threadIdx.x == 0) {
+    if (threadIdx.x == 0 && W8A8_DOK(row < rows, 103)) {
       if (DYN) scale[row] = rq.s;
       if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
     }
@@ -355,6 +356,7 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
   int qsum = 0, qabs = 0, qsq = 0;
   for (int64_t k = threadIdx.x; k < K; k += THREADS) {
     const int c = apply_rq(rq, __bfloat162float(xr[k]));
+    if (!W8A8_DOK(src >= 0 && k < K, 105)) continue;
     if (q16) q16[row * K + k] = __int2half_rn(c);
     else q[row * K + k] = (int8_t)c;
     qsum += c;
@@ -656,5 +658,9 @@ cudaError_t moe_combine(const void* out, const int64_t* row_of, const float* tw,
                                                   static_cast<__nv_bfloat16*>(y));
   return cudaGetLastError();
 }
+
+#ifdef W8A8_DEBUG
+cudaError_t debug_register_quant(int32_t* word) { return w8a8_debug_register_here(word); }
+#endif
 
 }  // namespace w8a8

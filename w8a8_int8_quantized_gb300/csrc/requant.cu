@@ -262,14 +262,14 @@ requant_ring_kernel(const __grid_constant__ ReqBatch b, int slot, int32_t* st, c
 #pragma unroll 2
       for (int idx = lane; idx < nv; idx += 32) {
         const uint4 o = requant_group(rowv[idx], cb[idx >> 3], srow + (idx >> 3), s);
-        qr[idx] = o;
+        if (W8A8_DOK(i < mt.N && (int64_t)(idx + 1) * 16 <= K, 201)) qr[idx] = o;
         if (ADJ && mt.adj) qsum = sum4_i8(o.w, sum4_i8(o.z, sum4_i8(o.y, sum4_i8(o.x, qsum))));
       }
     } else {
       for (int idx = lane; idx < nv; idx += 32) qr[idx] = make_uint4(0u, 0u, 0u, 0u);
     }
     if (ADJ && mt.adj) qsum = warp_sum_i(qsum);
-    if (lane == 0) {
+    if (lane == 0 && W8A8_DOK(i >= 0 && i < mt.N, 202)) {
       mt.s[i] = s;
       if (ADJ && mt.adj) mt.adj[i] = qsum;
       if (bad) report_status(st, W8A8_ERR_BAD_SCALE);
@@ -697,6 +697,10 @@ int requant_path(const uint8_t* w, const int8_t* q, int64_t K) {
   if (K % 4 == 0 && K <= kReqWordMaxK && (a & 3) == 0) return 2;
   return 0;
 }
+
+#ifdef W8A8_DEBUG
+cudaError_t debug_register_requant(int32_t* word) { return w8a8_debug_register_here(word); }
+#endif
 
 }  // namespace w8a8
 
