@@ -468,7 +468,22 @@ def components(w8, wl, peaks):
     hbm = float(peaks.get("hbm_gbs", 6800.0))
     tf = float(peaks.get("bf16_tflops", 1900.0))
     out = {}
-    flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_buf = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
+    flush_words = flush_buf.view(torch.int32)
+
+    class _Flush:
+        """L2 flush before each component launch: a 256 MiB write, then a read of the same
+        buffer, so the write's dirty lines are written back before the measured kernel
+        instead of during it (a short kernel would otherwise be charged up to ~129 MB of
+        write-back that is not its own).  Its own time is subtracted."""
+
+        @staticmethod
+        def zero_():
+            flush_buf.zero_()
+            flush_words.sum()
+
+    flush = _Flush()
+    out["flush"] = "256 MiB write + read of the same buffer before each launch, its time subtracted"
     # S1 / S2 quantizers at M = 8192
     for K in (4096, 14336):
         x = wl.llama_activations(8192, K, seed=5).to(dev)

@@ -973,6 +973,33 @@ def test_decode_linear_fused_single_row(kind, N, K):
     check_bf16(y, r["y_bits"], r["y32"])
 
 
+@pytest.mark.parametrize("kind", ["nonzero_mean", "zero", "stress0", "stress1", "stress2", "stress3", "stress4",
+                                  "stress5", "stress6", "stress7"])
+@pytest.mark.parametrize("N,K", [(520, 4112), (300, 64), (1000, 11200)])
+def test_decode_linear_fused_asym_single_row(kind, N, K):
+    """A single token row with dynamic asymmetric quantization ([vLLM-W8A8] 4.1; the zero
+    point enters the epilogue through azp_adj, [SGLang-CT] item 4) takes the fused quantizer +
+    small-M GEMM: bit-exact against the oracle and against the two-launch path (stand-alone
+    quantizer, then the GEMM) for rows far from zero, constant rows (hi == lo: the symmetric
+    fallback), rows of two values, tiny magnitudes, exact ties and an all-zero row."""
+    d = _gemm_case(1, N, K, seed=3 * K + N, act="dyn_asym")
+    x = d["x"].clone()
+    if kind == "zero":
+        x[0] = 0
+    elif kind.startswith("stress"):
+        x[0] = _asym_stress_rows(K)[int(kind[-1])]
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    adj = w8.azp_adj(wq)
+    b = d["b"].to(DEV)
+    y = w8.linear(x.to(DEV), wq, sw, act_mode="dyn_asym", azp_adj=adj, bias=b)
+    xq, sx, zp = w8.quantize_act(x.to(DEV), "dyn_asym")
+    y2 = w8.scaled_mm(xq, wq, sx, sw, "dyn_asym", zp=zp, azp_adj=adj, bias=b)
+    r = oracle.w8a8_linear(wl.bits(x), d["rq"], d["rs"], bias_bits=wl.bits(d["b"]), mode="dyn_asym")
+    check_bf16(y, r["y_bits"], r["y32"])
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+
+
 @pytest.mark.parametrize("bias", [True, False])
 def test_decode_linear_fused_tensor_scale(bias):
     """The fused single-row path with a per-tensor weight scale, with and without bias."""

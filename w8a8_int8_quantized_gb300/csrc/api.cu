@@ -218,8 +218,10 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
   w8a8_status s = check_device();
   if (s != W8A8_OK) return s;
   const bool small = use_small_engine(M, true);
-  if (small && act_mode == W8A8_ACT_DYN_TOKEN_SYM && gemm_small_m_fused_ok(M, K) && aligned(x, 16) && ldx % 8 == 0) {
-    // decode: the quantizer runs inside the small-M GEMM (no separate launch)
+  if (small && (act_mode == W8A8_ACT_DYN_TOKEN_SYM || act_mode == W8A8_ACT_DYN_TOKEN_ASYM) &&
+      gemm_small_m_fused_ok(M, K) && aligned(x, 16) && ldx % 8 == 0) {
+    // decode: the per-token quantizer (symmetric, or affine with zp * azp_adj in the
+    // epilogue) runs inside the small-M GEMM (no separate launch)
     GemmArgs g{};
     g.w = wq;
     g.rows = M;
@@ -228,6 +230,7 @@ w8a8_status w8a8_linear(const void* x, int64_t M, int64_t K, int64_t ldx, int ac
     g.E = 1;
     g.act_mode = act_mode;
     g.w_mode = w_mode;
+    g.azp = azp_adj;
     g.s_w = s_w;
     g.bias = bias;
     g.y = y;

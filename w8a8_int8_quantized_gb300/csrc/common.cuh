@@ -134,6 +134,43 @@ __device__ __forceinline__ void quant_row_group_x2(const float* x, float s, floa
   }
 }
 
+// The per-token row rule: scale (and zero point) of one row from its statistics.  Symmetric:
+// s = absmax / 127 (a zero row gets s = 1).  Affine: s = (hi - lo) / 255, zp = rint(-128 - lo / s)
+// (int32, unclamped); a constant row (hi == lo) falls back to the symmetric rule with zp = 0.
+// Shared by the stand-alone quantizers and the quantizer fused into the decode GEMM, so both
+// produce the same codes.
+struct RowQuant {
+  float s;
+  int zp;
+  int affine;
+};
+
+__device__ __forceinline__ RowQuant row_quant_sym(float absmax) {
+  RowQuant r;
+  r.s = (absmax == 0.f) ? 1.f : __fdiv_rn(absmax, 127.f);
+  r.zp = 0;
+  r.affine = 0;
+  return r;
+}
+
+__device__ __forceinline__ RowQuant row_quant_asym(float lo, float hi) {
+  RowQuant r;
+  if (hi == lo) {
+    r.s = (hi == 0.f) ? 1.f : __fdiv_rn(fabsf(hi), 127.f);
+    r.zp = 0;
+    r.affine = 0;
+  } else {
+    r.s = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
+    r.zp = __float2int_rn(__fsub_rn(-128.f, __fdiv_rn(lo, r.s)));
+    r.affine = 1;
+  }
+  return r;
+}
+
+__device__ __forceinline__ int apply_rq(const RowQuant& r, float x) {
+  return r.affine ? quant_asym(x, r.s, r.zp) : quant_sym(x, r.s);
+}
+
 // four int32 values saturated to [-128, 127] and packed into one word, byte 0 = a
 __device__ __forceinline__ uint32_t pack4_i8_sat(int a, int b, int c, int d) {
   uint32_t hi, w;

@@ -258,13 +258,16 @@ gemm_small_m_xs_kernel(const int8_t* __restrict__ xq, const int8_t* __restrict__
 // takes the separate quantizer launch and its int8 round trip through memory off a decode
 // step.  The first round of weight loads is issued before the quantization so that it
 // overlaps the row reads.
+template <int MODE>
 __global__ void __launch_bounds__(kSmWarps * 32)
 gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const int8_t* __restrict__ wq,
                        int64_t rows, int64_t N, int64_t K, EpiParams ep, __nv_bfloat16* __restrict__ y) {
+  constexpr bool ASYM = MODE == W8A8_ACT_DYN_TOKEN_ASYM;
   extern __shared__ __align__(16) uint8_t xs[];
   __shared__ int red[kSmWarps][16][17];
-  __shared__ float sh_amax[kSmWarps][8];
-  __shared__ float sh_s[8], sh_r[8];
+  __shared__ float sh_amax[kSmWarps][8], sh_hi[kSmWarps][8];
+  __shared__ float sh_s[8], sh_r[8], sh_thr[8];
+  __shared__ int sh_zp[8];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, tq = lane & 3;
   const int nr = (int)rows;  // <= 8
@@ -292,38 +295,76 @@ gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const i
     load_round(blockIdx.x, warp, wa);
     preloaded = true;
   }
-  // row absmax (exact: a max of exact values), one CTA reduction for all rows
-  float am[8];
+  // row statistics (exact: max / min of exact values), one CTA reduction for all rows:
+  // absmax for the symmetric rule, min and max for the affine one
+  float am[8], ah[8];
 #pragma unroll
   for (int r = 0; r < 8; ++r) {
-    am[r] = 0.f;
+    am[r] = ASYM ? __int_as_float(0x7f800000) : 0.f;
+    ah[r] = __int_as_float(0xff800000);
     if (r < nr) {
       const uint4* xr = reinterpret_cast<const uint4*>(x + r * ldx);
       for (int c = threadIdx.x; c < nvec; c += kSmWarps * 32) {
         const uint4 v = __ldg(xr + c);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-        for (int k = 0; k < 4; ++k) am[r] = fmaxf(am[r], fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+        for (int k = 0; k < 4; ++k) {
+          if (ASYM) {
+            am[r] = fminf(am[r], fminf(bf16_lo(w[k]), bf16_hi(w[k])));
+            ah[r] = fmaxf(ah[r], fmaxf(bf16_lo(w[k]), bf16_hi(w[k])));
+          } else {
+            am[r] = fmaxf(am[r], fmaxf(fabsf(bf16_lo(w[k])), fabsf(bf16_hi(w[k]))));
+          }
+        }
       }
     }
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) am[r] = fmaxf(am[r], __shfl_xor_sync(0xffffffffu, am[r], o));
+    for (int o = 16; o > 0; o >>= 1) {
+      if (ASYM) {
+        am[r] = fminf(am[r], __shfl_xor_sync(0xffffffffu, am[r], o));
+        ah[r] = fmaxf(ah[r], __shfl_xor_sync(0xffffffffu, ah[r], o));
+      } else {
+        am[r] = fmaxf(am[r], __shfl_xor_sync(0xffffffffu, am[r], o));
+      }
+    }
   }
   if (lane == 0) {
 #pragma unroll
-    for (int r = 0; r < 8; ++r) sh_amax[warp][r] = am[r];
+    for (int r = 0; r < 8; ++r) {
+      sh_amax[warp][r] = am[r];
+      if (ASYM) sh_hi[warp][r] = ah[r];
+    }
   }
   __syncthreads();
   if (threadIdx.x < 8) {
-    float a = 0.f;
+    RowQuant rq;
+    float lo = 0.f, hi = 0.f;
+    if (ASYM) {
+      lo = sh_amax[0][threadIdx.x];
+      hi = sh_hi[0][threadIdx.x];
 #pragma unroll
-    for (int w = 0; w < kSmWarps; ++w) a = fmaxf(a, sh_amax[w][threadIdx.x]);
-    const float sc = (a == 0.f) ? 1.f : __fdiv_rn(a, 127.f);
-    sh_s[threadIdx.x] = sc;
-    sh_r[threadIdx.x] = __frcp_rn(sc);
+      for (int w = 1; w < kSmWarps; ++w) {
+        lo = fminf(lo, sh_amax[w][threadIdx.x]);
+        hi = fmaxf(hi, sh_hi[w][threadIdx.x]);
+      }
+      rq = row_quant_asym(lo, hi);
+    } else {
+      float a = 0.f;
+#pragma unroll
+      for (int w = 0; w < kSmWarps; ++w) a = fmaxf(a, sh_amax[w][threadIdx.x]);
+      rq = row_quant_sym(a);
+    }
+    const float rc = __frcp_rn(rq.s);
+    sh_s[threadIdx.x] = rq.s;
+    sh_r[threadIdx.x] = rc;
+    sh_zp[threadIdx.x] = rq.zp;
+    // the stand-alone affine quantizer's margin of its division-free fast path
+    sh_thr[threadIdx.x] = ASYM ? __fsub_rd(0.5f, __fmul_rn(__fmul_rn(fmaxf(fabsf(lo), fabsf(hi)), rc), 0x1p-21f)) : 0.f;
   }
   __syncthreads();
-  // codes into the shared-memory copy (|x| <= absmax: every code within +-127)
+  // codes into the shared-memory copy, by the stand-alone quantizer's rules (symmetric:
+  // |x| <= absmax, every code within +-127; affine: zero point folded into the rounding,
+  // saturated to [-128, 127])
   for (int r = 0; r < nr; ++r) {
     const float sc = sh_s[r], rc = sh_r[r];
     const uint4* xr = reinterpret_cast<const uint4*>(x + r * ldx);
@@ -336,10 +377,17 @@ gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const i
         f[2 * k] = bf16_lo(w[k]);
         f[2 * k + 1] = bf16_hi(w[k]);
       }
-      uint32_t b[8];
-      quant_row_group_x2<8>(f, sc, rc, b);
-      *reinterpret_cast<uint2*>(xs + r * ld + (int64_t)c * 8) =
-          make_uint2(pack4_i8_prmt(b[0], b[1], b[2], b[3]), pack4_i8_prmt(b[4], b[5], b[6], b[7]));
+      uint2 packed;
+      if (ASYM) {
+        uint32_t o2[2];
+        quant_row_group_affine_x2<8>(f, sc, rc, sh_zp[r], sh_thr[r], o2);
+        packed = make_uint2(o2[0], o2[1]);
+      } else {
+        uint32_t b[8];
+        quant_row_group_x2<8>(f, sc, rc, b);
+        packed = make_uint2(pack4_i8_prmt(b[0], b[1], b[2], b[3]), pack4_i8_prmt(b[4], b[5], b[6], b[7]));
+      }
+      *reinterpret_cast<uint2*>(xs + r * ld + (int64_t)c * 8) = packed;
     }
   }
   __syncthreads();
@@ -377,7 +425,8 @@ gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const i
       int sum = 0;
 #pragma unroll
       for (int w = 0; w < kSmWarps; ++w) sum += red[w][ch][tok];
-      if (W8A8_DOK(tok < rows, 403)) y[tok * N + n] = __float2bfloat16_rn(epi_apply(ep, sum, sh_s[tok], 0, n));
+      if (W8A8_DOK(tok < rows, 403))
+        y[tok * N + n] = __float2bfloat16_rn(epi_apply(ep, sum, sh_s[tok], ASYM ? sh_zp[tok] : 0, n));
     }
     __syncthreads();  // red is rewritten by the next block
   }
@@ -386,12 +435,15 @@ gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const i
 bool gemm_small_m_fused_ok(int64_t rows, int64_t K) { return rows == 1 && xs_stride(K) <= 96 * 1024; }
 
 cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cudaStream_t st) {
+  const bool asym = g.act_mode == W8A8_ACT_DYN_TOKEN_ASYM;
+  if (!asym && g.act_mode != W8A8_ACT_DYN_TOKEN_SYM) return cudaErrorInvalidValue;
+  if (asym && !g.azp) return cudaErrorInvalidValue;
   EpiParams ep;
-  ep.act_mode = W8A8_ACT_DYN_TOKEN_SYM;
+  ep.act_mode = g.act_mode;
   ep.w_mode = g.w_mode;
   ep.s_x = nullptr;
   ep.zp = nullptr;
-  ep.azp = nullptr;
+  ep.azp = asym ? g.azp : nullptr;
   ep.s_w = g.s_w;
   ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
   static thread_local int s_dev = -1, s_grid = 0;
@@ -399,7 +451,11 @@ cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cu
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev != s_dev) {
-    e = cudaFuncSetAttribute(gemm_small_m_fq_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    e = cudaFuncSetAttribute(gemm_small_m_fq_kernel<W8A8_ACT_DYN_TOKEN_SYM>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
+    if (e != cudaSuccess) return e;
+    e = cudaFuncSetAttribute(gemm_small_m_fq_kernel<W8A8_ACT_DYN_TOKEN_ASYM>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, 96 * 1024);
     if (e != cudaSuccess) return e;
     int sms = 0;
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -410,9 +466,12 @@ cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cu
   const int64_t gx = (g.N + 15) / 16;
   const unsigned grid = (unsigned)(gx < s_grid ? gx : s_grid);
   const size_t xs_bytes = (size_t)(g.rows * xs_stride(g.K));
-  gemm_small_m_fq_kernel<<<grid, kSmWarps * 32, xs_bytes, st>>>(static_cast<const __nv_bfloat16*>(x), ldx, g.w,
-                                                                g.rows, g.N, g.K, ep,
-                                                                static_cast<__nv_bfloat16*>(g.y));
+  if (asym)
+    gemm_small_m_fq_kernel<W8A8_ACT_DYN_TOKEN_ASYM><<<grid, kSmWarps * 32, xs_bytes, st>>>(
+        static_cast<const __nv_bfloat16*>(x), ldx, g.w, g.rows, g.N, g.K, ep, static_cast<__nv_bfloat16*>(g.y));
+  else
+    gemm_small_m_fq_kernel<W8A8_ACT_DYN_TOKEN_SYM><<<grid, kSmWarps * 32, xs_bytes, st>>>(
+        static_cast<const __nv_bfloat16*>(x), ldx, g.w, g.rows, g.N, g.K, ep, static_cast<__nv_bfloat16*>(g.y));
   return cudaGetLastError();
 }
 

@@ -106,8 +106,9 @@ cudaError_t debug_register_moe_route(int32_t* word);
 
 // gemm_small.cu: mma.sync s8 weight-streaming kernel (small M)
 cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st);
-// Dynamic per-token symmetric decode (at most 8 bf16 rows x) with the quantizer fused into the
-// small-M GEMM; g carries the weight side and the output (g.a, g.s_x unused).
+// Dynamic per-token decode (at most 8 bf16 rows x; symmetric, or affine with g.azp the
+// weight's azp_adj) with the quantizer fused into the small-M GEMM; g carries the weight side,
+// the mode and the output (g.a, g.s_x, g.zp unused).
 bool gemm_small_m_fused_ok(int64_t rows, int64_t K);
 cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cudaStream_t st);
 // gemm_tc.cu: tcgen05 kernel; returns cudaErrorNotSupported when it cannot run

@@ -62,38 +62,6 @@ __device__ __forceinline__ int block_reduce_sum_i(int v, int* sh) {
 
 // Scale and zero point of one row from its statistics.  Returns kind: 0 = symmetric
 // rule with scale s, 1 = affine rule with (s, zp).
-struct RowQuant {
-  float s;
-  int zp;
-  int affine;
-};
-
-__device__ __forceinline__ RowQuant row_quant_sym(float absmax) {
-  RowQuant r;
-  r.s = (absmax == 0.f) ? 1.f : __fdiv_rn(absmax, 127.f);
-  r.zp = 0;
-  r.affine = 0;
-  return r;
-}
-
-__device__ __forceinline__ RowQuant row_quant_asym(float lo, float hi) {
-  RowQuant r;
-  if (hi == lo) {
-    r.s = (hi == 0.f) ? 1.f : __fdiv_rn(fabsf(hi), 127.f);
-    r.zp = 0;
-    r.affine = 0;
-  } else {
-    r.s = __fdiv_rn(__fsub_rn(hi, lo), 255.f);
-    r.zp = __float2int_rn(__fsub_rn(-128.f, __fdiv_rn(lo, r.s)));
-    r.affine = 1;
-  }
-  return r;
-}
-
-__device__ __forceinline__ int apply_rq(const RowQuant& r, float x) {
-  return r.affine ? quant_asym(x, r.s, r.zp) : quant_sym(x, r.s);
-}
-
 __device__ __forceinline__ void unpack8(const uint4& v, float* f) {
   f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
   f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
