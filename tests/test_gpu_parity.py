@@ -72,10 +72,29 @@ def test_quantize_act_dyn_asym(M, K):
     np.testing.assert_array_equal(zp.cpu().numpy(), rz)
 
 
+def test_division_free_codes_equal_ieee_quotient_exhaustively():
+    """The symmetric row rule's codes come from a division-free rounding (Markstein's
+    correction step on RN(x * RN(1/s))).  Run on every bf16 absmax a and every bf16 x with
+    |x| <= a (s = RN(a / 127)), the library's own device function gives rint of the IEEE
+    float32 quotient x / s in every case ([Kunlun-INT8] 转换关系: round(W / s)).  The affine
+    rule's division-free codes (window test and exact near-tie decision) are checked the same
+    way over every bf16 value of 65536 row ranges, a quarter of them with exact ties."""
+    from w8a8_int8_quantized_gb300 import quotient_check
+    out = quotient_check.run()
+    r = out["symmetric_rule"]
+    assert r["values"] > 800_000_000
+    assert r["code_mismatches"] == 0
+    a = out["affine_rule"]
+    assert a["values"] > 100_000_000
+    assert a["code_mismatches"] == 0
+    assert a["exact_resolver_mismatches"] == 0
+
+
 def _asym_stress_rows(K):
     """bf16 rows that stress the affine rule's fast path: rows far from zero (|x/s| up to
-    about 2^16), constant rows, rows of two values, tiny magnitudes and rows of exact
-    multiples of a power of two (many exact ties)."""
+    about 2^16), constant rows, rows of two values, tiny magnitudes, rows of exact
+    multiples of a power of two (many exact ties), exact ties under an odd zero point and
+    near-ties under an inexact scale."""
     g = torch.Generator().manual_seed(K)
     rows = [
         1000.0 + torch.randint(0, 8, (K,), generator=g).float() * 4.0,      # bf16 step 4 at 1000
@@ -87,6 +106,31 @@ def _asym_stress_rows(K):
         torch.randn(K, generator=g) * 5.0 + 40.0,
         torch.linspace(-1.0, 1.0, K),
     ]
+    # exact ties with an odd zero point: s = 1/8 exactly (lo = -13/8, hi = lo + 255/8, zp = -115)
+    # and x = (m + 1/2) s
+    r = (torch.randint(-13, 128, (K,), generator=g).float() + 0.5) * 0.125
+    r[0], r[1 % K] = -1.625, 30.25
+    rows.append(r)
+    # lo = -13.6875, hi = 36.25: x = +-1.46875 has RN(x * RN(1/s)) = +-7.5 exactly but
+    # x / s = +-7.4999995, and the exact product x * RN(1/s) lies just above the midpoint below
+    # 7.5, so a multiply-add fused into one rounding and the separately rounded product break
+    # the value different ways
+    r = torch.where(torch.rand(K, generator=g) < 0.5, torch.tensor(1.46875), torch.tensor(-1.46875))
+    r[0], r[1 % K] = -13.6875, 36.25
+    rows.append(r)
+    # near-ties with inexact scales: of every bf16 value in [lo, hi], the 64 whose quotients
+    # x / s lie closest to a half-integer, drawn at random
+    for lo, hi in ((-3.5, 4.5), (-1.0, 7.25), (0.5, 1.5)):
+        s_ = np.float32(np.float32(hi) - np.float32(lo)) / np.float32(255.0)
+        pos = np.arange(0, 0x7F80, dtype=np.uint32) << 16
+        cand = np.concatenate([pos.view(np.float32), (pos | 0x80000000).view(np.float32)])
+        cand = cand[(cand >= lo) & (cand <= hi)]
+        t = cand.astype(np.float64) / np.float64(s_)
+        dist = np.abs(np.abs(t - np.floor(t)) - 0.5)
+        near = torch.from_numpy(cand[np.argsort(dist, kind="stable")[:64]].copy())
+        r = near[torch.randint(0, 64, (K,), generator=g)]
+        r[0], r[1 % K] = lo, hi
+        rows.append(r)
     return torch.stack(rows).to(torch.bfloat16)
 
 

@@ -48,27 +48,6 @@ __device__ __forceinline__ int rint_div_i(float x, float s, float r) {
   return __float2int_rn(fminf(fmaxf(e, -1073741824.0f), 1073741824.0f));
 }
 
-// rint(RN(x / s)) for a value whose approximate quotient t lies near the half-integer
-// h = k + 0.5, without a division in the common case.  The residual x - h*s is formed by one
-// fma, whose sign is exact.  RN(x / s) lands on h itself exactly when |x / s - h| <=
-// ulp(h)/2, i.e. |x - h*s| <= s*ulp(h)/2 =: tau (tau is s scaled by a power of two, so exact;
-// ties at ulp(h)/2 go to h because h = k + 0.5 has a zero last mantissa bit for |h| >= 1.5):
-// then the result is the even one of k, k + 1.  Otherwise RN(x / s) lies strictly on the
-// residual's side of h and less than 1/2 from it, so the result is k or k + 1 by that side.
-// The rounded residual decides both tests unless it equals tau; that case, |h| < 1.5 (where
-// the neighbours of h are not symmetric), and s outside [2^-100, 2^100] use the division.
-// Requires |t - x/s| < 2^-13 and |t| < 2^22.
-__device__ __forceinline__ float rint_quot_near_tie(float x, float s, float t) {
-  const float h = __fadd_rn(rintf(__fsub_rn(t, 0.5f)), 0.5f);
-  if (fabsf(h) >= 1.5f && s >= 0x1p-100f && s <= 0x1p100f) {
-    const float rho = fabsf(__fmaf_rn(-h, s, x));
-    const float tau = __fmul_rn(__fmul_rn(s, __uint_as_float(__float_as_uint(h) & 0x7F800000u)), 0x1p-24f);
-    if (rho < tau) return rintf(h);
-    if (rho > tau) return __fmaf_rn(-h, s, x) > 0.f ? __fadd_rn(h, 0.5f) : __fsub_rn(h, 0.5f);
-  }
-  return rintf(__fdiv_rn(x, s));
-}
-
 // rint_div_i for quotients known to satisfy |x/s| <= 256 (a row divided by its own
 // absmax/127, or anything clamped to int8 range afterwards when it is that small): the
 // margin |t|*2^-20 is then at most 2^-12, used as a constant, and the slow path needs no
@@ -106,31 +85,41 @@ __device__ __forceinline__ uint64_t f2sub(uint64_t a, uint64_t b) {
   return r;
 }
 
-// quant_row_group on packed float32 pairs (N even): half the float instructions.
+__device__ __forceinline__ uint64_t f2fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+
+// The symmetric row rule's codes rint(RN(x / s)) for N values (N even), without a division:
+// q0 = RN(x * r) with r = RN(1 / s), the remainder x - q0 * s (exact by fma), and one
+// correction q = RN(q0 + (x - q0 * s) * r) (Markstein's correction step, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res. Dev. 34, 1990).
+// q is RN(x / s) or an adjacent float; rint(q) equals rint(RN(x / s)) for every bf16 x with
+// |x| <= a and s = RN(a / 127), a any finite positive bf16 with s in [2^-100, 2^100]: checked
+// exhaustively against the IEEE division (quotient_check.cu, run by the GPU tests).  An exact
+// tie x / s = k + 1/2 gives q = k + 1/2 exactly, which rint breaks to even, so no tie needs
+// detecting.  rint is the addition of 1.5 * 2^23 (|q| <= 128): the integer is the low
+// mantissa bits of the sum, returned here as the sum's bit pattern.  Scales outside that
+// range divide.
 template <int N>
 __device__ __forceinline__ void quant_row_group_x2(const float* x, float s, float r, uint32_t* b) {
-  // |x / s| <= 128 here, so t = RN(x * r) is within 2^-16 of x / s and RN(x / s) within 2^-17:
-  // a t more than 2^-14 from every half-integer rounds like the IEEE quotient
   const uint64_t kMagic = 0x4B4000004B400000ull;  // 1.5*2^23 in both lanes
-  const uint64_t r2 = f2pack(r, r);
-  float emax = 0.f;
-  float e[N];
+  if (s >= 0x1p-100f && s <= 0x1p100f) {
+    const uint64_t r2 = f2pack(r, r), ns2 = f2pack(-s, -s);
 #pragma unroll
-  for (int j = 0; j < N; j += 2) {
-    const uint64_t t = f2mul(f2pack(x[j], x[j + 1]), r2);
-    const uint64_t m = f2add(t, kMagic);
-    float m0, m1;
-    f2unpack(f2sub(t, f2sub(m, kMagic)), e[j], e[j + 1]);
-    f2unpack(m, m0, m1);
-    emax = fmaxf(emax, fmaxf(fabsf(e[j]), fabsf(e[j + 1])));
-    b[j] = __float_as_uint(m0);
-    b[j + 1] = __float_as_uint(m1);
-  }
-  if (!(emax < 0.49993896484375f)) {  // 0.5 - 2^-14: decide the values near a tie exactly
+    for (int j = 0; j < N; j += 2) {
+      const uint64_t x2 = f2pack(x[j], x[j + 1]);
+      const uint64_t q0 = f2mul(x2, r2);
+      const uint64_t q = f2fma(f2fma(q0, ns2, x2), r2, q0);
+      float m0, m1;
+      f2unpack(f2add(q, kMagic), m0, m1);
+      b[j] = __float_as_uint(m0);
+      b[j + 1] = __float_as_uint(m1);
+    }
+  } else {
 #pragma unroll
-    for (int j = 0; j < N; ++j)
-      if (!(fabsf(e[j]) < 0.49993896484375f))
-        b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rint_quot_near_tie(x[j], s, __fmul_rn(x[j], r)));
+    for (int j = 0; j < N; ++j) b[j] = 0x4B400000u + (uint32_t)__float2int_rn(rintf(__fdiv_rn(x[j], s)));
   }
 }
 
@@ -190,38 +179,109 @@ __device__ __forceinline__ int sign_bytes(uint32_t w) {
 __device__ __forceinline__ int sum4_i8(uint32_t w, int acc) { return __dp4a((int)w, 0x01010101, acc); }
 __device__ __forceinline__ int abssum4_i8(uint32_t w, int acc) { return __dp4a((int)w, sign_bytes(w), acc); }
 
-// N values (N % 4 == 0) of a row under the affine rule q = clamp(rint(x / s) + zp, -128, 127),
-// written as N/4 packed words.  t = RN(x * r) with r = RN(1/s) and the zero point folded into
-// the rounding constant (1.5*2^23 + zp, exact for |zp| < 2^22): the low mantissa bits of
-// t + 1.5*2^23 + zp are rint(t) + zp.  thr = 0.5 - (margin of the row): a value whose t lies
-// at least that far inside an integer interval rounds as the IEEE quotient does; the others
-// (and every value when thr <= 0) are decided by the division.
+// ---- affine row rule q = clamp(rint(RN(x / s)) + zp, -128, 127) without dividing.
+//
+// Fast path: m = RN(x * r + (1.5*2^23 + zp)) by one fma (r = RN(1/s)); the low mantissa bits
+// of m are rint(P) + zp with P = x * r the exact product (1.5*2^23 + zp is exact for |zp| <
+// 2^22 and the sum lands where float spacing is 1).  P is within |x / s| * 2^-24 < ulp(x / s)
+// of x / s, so within 1.5 ulps of RN(x / s).  With thr = 0.5 - tmax * 2^-21 (tmax the row's
+// largest |x / s|, the callers' margin of at least four such ulps), every value whose
+// e = RN(P - rint(P)) satisfies |e| < thr has rint(RN(x / s)) = rint(P).  The others lie near
+// a half-integer (rows of bf16 values put a few tenths of a percent of their values there:
+// quotients of short mantissas cluster near half-integers) and are flagged for
+// affine_code_exact.  The packed operations are written as fma so that the compiler has no
+// multiply-add left to fuse: the fast path's code is then reproducible one value at a time
+// (affine_code_fast_one).
+__device__ __forceinline__ bool affine_fast_ok(float s, float thr) {
+  return s >= 0x1p-100f && s <= 0x1p100f && thr > 0.25f;
+}
+
+// N values (N even): codes (unclamped; 0 where the fast path does not apply) and the mask of
+// values that need affine_code_exact
 template <int N>
-__device__ __forceinline__ void quant_row_group_affine_x2(const float* x, float s, float r, int zp, float thr,
-                                                          uint32_t* out) {
+__device__ __forceinline__ uint32_t affine_codes_fast(const float* x, float s, float r, int zp, float thr, int* qv) {
+  if (!affine_fast_ok(s, thr)) {
+#pragma unroll
+    for (int j = 0; j < N; ++j) qv[j] = 0;
+    return (N >= 32) ? 0xFFFFFFFFu : ((1u << N) - 1u);
+  }
   const float mg = __fadd_rn(12582912.0f, (float)zp);
   const uint64_t mg2 = f2pack(mg, mg);
   const uint64_t r2 = f2pack(r, r);
-  float emax = 0.f;
-  int qv[N];
+  uint32_t m = 0;
 #pragma unroll
   for (int j = 0; j < N; j += 2) {
-    const uint64_t t = f2mul(f2pack(x[j], x[j + 1]), r2);
-    const uint64_t m = f2add(t, mg2);
+    const uint64_t x2 = f2pack(x[j], x[j + 1]);
+    const uint64_t mm = f2fma(x2, r2, mg2);
+    const uint64_t e2 = f2fma(x2, r2, f2sub(mg2, mm));  // RN(P - rint(P)); mg - m is exact
     float e0, e1, m0, m1;
-    f2unpack(f2sub(t, f2sub(m, mg2)), e0, e1);
-    f2unpack(m, m0, m1);
-    emax = fmaxf(emax, fmaxf(fabsf(e0), fabsf(e1)));
+    f2unpack(e2, e0, e1);
+    f2unpack(mm, m0, m1);
+    m |= ((fabsf(e0) < thr) ? 0u : (1u << j)) | ((fabsf(e1) < thr) ? 0u : (2u << j));
     qv[j] = __float_as_int(m0) - 0x4B400000;
     qv[j + 1] = __float_as_int(m1) - 0x4B400000;
   }
-  if (!(emax < thr)) {
+  return m;
+}
+
+// the code affine_codes_fast gives one value, clamped as the packing does
+__device__ __forceinline__ int affine_code_fast_one(float x, float s, float r, int zp, float thr) {
+  if (!affine_fast_ok(s, thr)) return 0;
+  const float m = __fmaf_rn(x, r, __fadd_rn(12582912.0f, (float)zp));
+  return min(127, max(-128, __float_as_int(m) - 0x4B400000));
+}
+
+// rint(RN(x / s)) + zp exactly (clamped), for any value; the common case without dividing.
+// With t = RN(x * r) and h the half-integer nearest t: RN(x / s) equals h when |x / s - h| <
+// ulp(h) / 2, is above h when x / s is above h + ulp(h) / 2 and below it symmetrically.  Scaled
+// by s > 0 the test compares D = x - h * s with tau = s * ulp(h) / 2 = s * 2^(exponent of h) *
+// 2^-24, which is exact for s in [2^-100, 2^100].  For |h| >= 1.5 both neighbours of h are
+// ulp(h) away (h is not a power of two); for h = +-1/2 the neighbour toward zero is only
+// ulp(h) / 2 away, but there the even code and the code toward zero are both 0, so the same
+// test decides.  fma(-h, s, x) rounds D once, so |fma| < tau proves |D| < tau (code: h rounded
+// half to even) and |fma| > tau proves |D| > tau (code: h + 1/2 or h - 1/2 by its sign).
+// The same decision is right for a value far from every half-integer (x / s is then within
+// 1/2 of h with the sign of D, as t is).  |fma| == tau (or NaN) and scales or quotients
+// outside the fast path's range divide.
+__device__ __forceinline__ int affine_code_exact(float x, float s, float r, int zp, float thr) {
+  int code;
+  bool divide = !affine_fast_ok(s, thr);
+  if (!divide) {
+    const float mg = __fadd_rn(12582912.0f, (float)zp);
+    const float t = __fmul_rn(x, r);
+    const float k = __fsub_rn(__fadd_rn(t, mg), mg);
+    const float e = __fsub_rn(t, k);
+    const float h = __fadd_rn(k, __uint_as_float((__float_as_uint(e) & 0x80000000u) | 0x3F000000u));
+    const float dd = __fmaf_rn(-h, s, x);
+    const float d = fabsf(dd);
+    const float tau = __fmul_rn(__uint_as_float(__float_as_uint(h) & 0x7F800000u), __fmul_rn(s, 0x1p-24f));
+    const int kd = __float_as_int(__fadd_rn(__fsub_rn(h, 0.5f), mg)) - 0x4B400000;  // h - 1/2 + zp
+    code = kd + ((d < tau) ? ((kd - zp) & 1) : (dd > 0.f ? 1 : 0));
+    divide = !(d < tau || d > tau);
+  }
+  if (divide) {
+    const long long v = (long long)__float2int_rn(rintf(__fdiv_rn(x, s))) + (long long)zp;
+    code = (int)min(127ll, max(-128ll, v));
+  }
+  return min(127, max(-128, code));
+}
+
+// N values (N % 4 == 0) of a row under the affine rule, written as N/4 packed words: the fast
+// path, then each flagged value decided by affine_code_exact.
+template <int N>
+__device__ __forceinline__ void quant_row_group_affine_x2(const float* x, float s, float r, int zp, float thr,
+                                                          uint32_t* out) {
+  int qv[N];
+  uint32_t m = affine_codes_fast<N>(x, s, r, zp, thr, qv);
+  while (m) {  // rare: one value per iteration
+    const int j = __ffs(m) - 1;
+    m &= m - 1;
+    float xj = x[0];
 #pragma unroll
-    for (int j = 0; j < N; ++j) {
-      const float t = __fmul_rn(x[j], r);
-      const float e = __fsub_rn(t, __fsub_rn(__fadd_rn(t, mg), mg));
-      if (!(fabsf(e) < thr)) qv[j] = quant_asym(x[j], s, zp);
-    }
+    for (int i = 1; i < N; ++i) xj = (j == i) ? x[i] : xj;
+    const int v = affine_code_exact(xj, s, r, zp, thr);
+#pragma unroll
+    for (int i = 0; i < N; ++i) qv[i] = (j == i) ? v : qv[i];
   }
 #pragma unroll
   for (int g = 0; g < N / 4; ++g) out[g] = pack4_i8_sat(qv[4 * g], qv[4 * g + 1], qv[4 * g + 2], qv[4 * g + 3]);

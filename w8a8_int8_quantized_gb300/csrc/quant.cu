@@ -205,6 +205,7 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       thr = __fsub_rd(0.5f, __fmul_rn(tmax, 0x1p-21f));
     }
     int qsum = 0, qabs = 0, qsq = 0;
+    uint32_t near = 0;  // affine rule: values (bit 8*i + j) left to the exact decision
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int idx = threadIdx.x + i * THREADS;
@@ -220,11 +221,13 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
           w1 = pack4_i8_prmt(b[4], b[5], b[6], b[7]);
         } else if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
           // |x / s| <= 127 in a degenerate (symmetric-rule) row, so the [-128, 127] saturation
-          // of the packing never differs from the symmetric clamp there
-          uint32_t o2[2];
-          quant_row_group_affine_x2<8>(f, rq.s, r, rq.zp, thr, o2);
-          w0 = o2[0];
-          w1 = o2[1];
+          // of the packing never differs from the symmetric clamp there.  Values near a
+          // half-integer keep the fast path's code here and are corrected after the loop, which
+          // keeps this loop free of branches.
+          int c[8];
+          near |= affine_codes_fast<8>(f, rq.s, r, rq.zp, thr, c) << (8 * i);
+          w0 = pack4_i8_sat(c[0], c[1], c[2], c[3]);
+          w1 = pack4_i8_sat(c[4], c[5], c[6], c[7]);
         } else {
           int c[8];
 #pragma unroll
@@ -247,6 +250,31 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
         } else {
           if (W8A8_DOK(row < rows && (int64_t)(idx + 1) * 8 <= K, 102)) reinterpret_cast<uint2*>(q + row * K)[idx] = make_uint2(w0, w1);
         }
+      }
+    }
+    if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) {
+      // the flagged values (a few per thousand): exact code, stored over the fast path's, and
+      // the row sums moved by the difference
+      while (near) {
+        const int b = __ffs(near) - 1;
+        near &= near - 1;
+        const int i = b >> 3, j = b & 7;
+        uint4 vs = v[0];
+#pragma unroll
+        for (int ii = 1; ii < NV; ++ii) vs = (i == ii) ? v[ii] : vs;
+        const uint32_t wd = (j < 4) ? ((j < 2) ? vs.x : vs.y) : ((j < 6) ? vs.z : vs.w);
+        const float xj = (j & 1) ? bf16_hi(wd) : bf16_lo(wd);
+        const int c0 = affine_code_fast_one(xj, rq.s, r, rq.zp, thr);
+        const int c1 = affine_code_exact(xj, rq.s, r, rq.zp, thr);
+        const int64_t col = (int64_t)(threadIdx.x + i * THREADS) * 8 + j;
+        if (F16) {
+          if (W8A8_DOK(row < rows && col < K, 106)) q16[row * K + col] = __int2half_rn(c1);
+        } else {
+          if (W8A8_DOK(row < rows && col < K, 106)) q[row * K + col] = (int8_t)c1;
+        }
+        if (SUM) qsum += c1 - c0;
+        if (F16) qabs += abs(c1) - abs(c0);
+        if (SQ) qsq += c1 * c1 - c0 * c0;
       }
     }
     if (threadIdx.x == 0 && W8A8_DOK(row < rows, 103)) {
