@@ -114,6 +114,8 @@ w8a8_status w8a8_test_requant_wait_fault(uint32_t extra_tx_bytes, uint64_t wait_
  * Rounding: q = clamp(rint(x / s) (+ zp), lo, hi), IEEE float32 division, ties to even;
  * [lo, hi] = [-127, 127] symmetric, [-128, 127] asymmetric.  All-zero rows give q = 0, s = 1.
  * The static scale must be finite and positive (results are unspecified otherwise).
+ * Activations are expected finite: a row holding NaN or an infinity gets unspecified codes
+ * (saturated to the code range; nothing faults).
  * M == 0 or K == 0 is a no-op returning W8A8_OK.
  */
 w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, int mode,
