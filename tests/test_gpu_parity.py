@@ -281,6 +281,60 @@ def test_scaled_mm_dyn_sym(engine, M, N, K):
     check_bf16(y, r["y_bits"], r["y32"])
 
 
+@pytest.mark.parametrize("act", ["dyn_sym", "dyn_asym", "static_sym", "static_asym"])
+@pytest.mark.parametrize("w_mode", [w8.W_CHANNEL, w8.W_TENSOR])
+@pytest.mark.parametrize("M,N,K", [(1, 520, 4112), (2, 8, 16), (2, 2500, 4096), (2, 300, 14336), (1, 5000, 4096),
+                                   (1, 17, 12304)])
+def test_gemv_rows(act, w_mode, M, N, K):
+    """One or two token rows take the dp4a GEMV (K % 16 == 0): units of 4096 weight bytes
+    with a ragged last one (K = 4112, 12304), K = 16 (one partial unit), weights with fewer
+    rows than warps (N = 8, 17) and more rows than warps (N = 5000), every activation mode
+    through the pre-quantized path; bit-exact against the oracle."""
+    d = _gemm_case(M, N, K, seed=M * 31 + K, act=act, w_mode=w_mode)
+    xs = d["x"].float().numpy()
+    wq = torch.from_numpy(d["rq"]).to(DEV)
+    sw = torch.from_numpy(d["rs"]).to(DEV)
+    bias = d["b"].to(DEV)
+    sc, z = oracle.static_scale_from_tensor(xs)
+    kw = {}
+    if act == "dyn_sym":
+        xq, sx, _ = w8.quantize_act(d["x"].to(DEV), "dyn_sym")
+    elif act == "dyn_asym":
+        xq, sx, zq = w8.quantize_act(d["x"].to(DEV), "dyn_asym")
+        kw = dict(zp=zq, azp_adj=w8.azp_adj(wq))
+    else:
+        sx = torch.tensor([sc], dtype=torch.float32, device=DEV)
+        zt = torch.tensor([z], dtype=torch.int32, device=DEV)
+        xq, _, _ = w8.quantize_act(d["x"].to(DEV), act, scale=sx, zp=zt if act == "static_asym" else None)
+        if act == "static_asym":
+            kw = dict(zp=zt, azp_adj=w8.azp_adj(wq, zt))
+    y = w8.scaled_mm(xq, wq, sx, sw, act, bias=bias, w_mode=w_mode, **kw)
+    r = oracle.w8a8_linear(d["xb"], d["rq"], d["rs"], bias_bits=wl.bits(d["b"]), mode=act,
+                           input_scale=sc, input_zero_point=z)
+    check_bf16(y, r["y_bits"], r["y32"])
+
+
+def test_gemv_extremes_exact():
+    """Largest int32 magnitudes through the GEMV: acc = +-128*127*K at K = 65536 (one row)
+    and 14336 (two rows) must be exact, with the asymmetric epilogue."""
+    for M, K in ((1, 65536), (2, 14336)):
+        N = 40
+        xq = torch.full((M, K), -128, dtype=torch.int8)
+        xq[1::2] = 127
+        wq = torch.full((N, K), 127, dtype=torch.int8)
+        wq[1::2] = -127
+        wq[7, 1000:] = 3
+        sx = torch.full((M,), 1.0, dtype=torch.float32)
+        sw = torch.full((N,), 2.0 ** -24, dtype=torch.float32)
+        zp = torch.arange(M, dtype=torch.int32) - 2
+        adj = torch.from_numpy(oracle.azp_adj(wq.numpy()))
+        y = w8.scaled_mm(xq.to(DEV), wq.to(DEV), sx.to(DEV), sw.to(DEV), "dyn_asym", zp=zp.to(DEV),
+                         azp_adj=adj.to(DEV))
+        acc = oracle.int8_gemm(xq.numpy(), wq.numpy())
+        yb, y32 = oracle.scaled_mm_epilogue(acc, sx.numpy(), sw.numpy(), zp=zp.numpy(), adj=adj.numpy())
+        check_bf16(y, yb, y32)
+
+
 @pytest.mark.parametrize("M,N,K", [(1, 520, 4112), (2, 520, 14336), (1, 520, 30016), (2, 520, 30016),
                                    (5, 5000, 4096), (8, 5000, 11200), (8, 300, 64)])
 def test_decode_rows_staged(M, N, K):

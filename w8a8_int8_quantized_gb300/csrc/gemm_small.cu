@@ -12,8 +12,11 @@
 //                           rows too long to stage);
 //   gemm_small_m_xs_kernel  at most 8 rows staged in shared memory once per persistent CTA,
 //                           eight chunks in flight per thread;
-//   gemm_small_m_fq_kernel  one dynamic-symmetric bf16 row quantized inside the CTA (the
-//                           stand-alone quantizer's exact rule) before the same streaming.
+//   gemm_small_m_fq_kernel  one dynamic bf16 row quantized inside the CTA (the stand-alone
+//                           quantizer's exact rules) before the same streaming;
+//   gemv_kernel             one or two token rows (given codes, or one dynamic bf16 row)
+//                           on dp4a instead of the warp MMA, which would be mostly padding
+//                           (below).
 //
 // K order inside a 64-byte chunk: each thread loads 16 contiguous bytes of a row and
 // feeds them to the MMA as its k-slots; A and B use the same mapping, so the sum over k
@@ -432,6 +435,219 @@ gemm_small_m_fq_kernel(const __nv_bfloat16* __restrict__ x, int64_t ldx, const i
   }
 }
 
+// ---- one or two token rows: a GEMV on dp4a.  The warp MMA above computes 16 x 8 outputs
+// per instruction, so with one token 7/8 of its work is padding, and this GPU's int8 warp
+// MMA rate is low enough (about 158 TOPS) that the padded products take about 70 % of the
+// time the weight takes to stream from HBM.  Here each weight byte costs a quarter of a dp4a
+// per token (exact s8 x s8 -> s32 products, int32 sums below 2^31 for K <= 65536).  A warp
+// owns whole weight rows (rows gw, gw + warps, ...), read in units of 4096 bytes: lane l
+// loads the 16-byte chunks l, l + 32, ... of the unit (each load instruction covers 512
+// contiguous bytes), with the next unit's loads in flight while the current one is summed;
+// the tokens' codes sit in shared memory (zero past K).  One warp reduction per row and
+// token, then the epilogue by lane t for token t.  The codes are either given (XM = 0, up
+// to MT = 2 rows) or computed in every CTA from one bf16 row with the stand-alone
+// quantizer's exact rules (XM = 1 dynamic symmetric, XM = 2 dynamic asymmetric; the first
+// weight unit is in flight meanwhile).
+constexpr int kGvWarps = 8;
+constexpr int kGvKU = 8;                       // 16-byte chunks per lane per unit
+constexpr int kGvUnit = 32 * 16 * kGvKU;       // 4096 weight bytes per unit
+
+__host__ __device__ inline int64_t gemv_xs_bytes(int64_t K) { return (K + kGvUnit - 1) / kGvUnit * kGvUnit; }
+
+template <int XM, int MT>
+__global__ void __launch_bounds__(kGvWarps * 32)
+gemv_kernel(const __nv_bfloat16* __restrict__ x, const int8_t* __restrict__ xq, int64_t M, const int8_t* __restrict__ wq,
+            int64_t N, int64_t K, EpiParams ep, __nv_bfloat16* __restrict__ y) {
+  extern __shared__ __align__(16) uint8_t xs[];
+  __shared__ float sh_a[kGvWarps], sh_b[kGvWarps];
+  __shared__ float sh_s, sh_r, sh_thr;
+  __shared__ int sh_zp;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int64_t tw = (int64_t)gridDim.x * kGvWarps;
+  const int64_t gw = (int64_t)blockIdx.x * kGvWarps + warp;
+  const int64_t nseg = gemv_xs_bytes(K) / kGvUnit;
+  const int64_t units = gw < N ? ((N - gw + tw - 1) / tw) * nseg : 0;
+  uint4 w0[kGvKU], w1[kGvKU];
+  auto load_unit = [&](int64_t u, uint4 (&d)[kGvKU]) {
+    const int64_t n = gw + (u / nseg) * tw, sg = u % nseg;
+    const int8_t* wr = wq + n * K;
+#pragma unroll
+    for (int c = 0; c < kGvKU; ++c) {
+      const int64_t k = (sg * kGvKU + c) * 512 + lane * 16;
+      d[c] = ld16_stream_or_zero(wr + k, k < K && W8A8_DOK(n < N, 404));
+    }
+  };
+  if (units > 0) load_unit(0, w0);
+
+  // the tokens' codes into shared memory ([MT][xs bytes]), zero past K and for tokens >= M
+  const int64_t nx = gemv_xs_bytes(K) / 16;
+  if (XM == 0) {
+    for (int64_t c = threadIdx.x; c < nx * MT; c += kGvWarps * 32) {
+      const int64_t t = c / nx, k = (c - t * nx) * 16;
+      reinterpret_cast<uint4*>(xs)[c] = ld16_or_zero(xq + t * K + k, t < M && k < K);
+    }
+  } else {
+    constexpr bool ASYM = XM == 2;
+    const int64_t nv = K / 8;
+    const uint4* xr = reinterpret_cast<const uint4*>(x);
+    float a = ASYM ? __int_as_float(0x7f800000) : 0.f, b = __int_as_float(0xff800000);
+    for (int64_t c = threadIdx.x; c < nv; c += kGvWarps * 32) {
+      const uint4 v = __ldg(xr + c);
+      const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        if (ASYM) {
+          a = fminf(a, fminf(bf16_lo(wd[k]), bf16_hi(wd[k])));
+          b = fmaxf(b, fmaxf(bf16_lo(wd[k]), bf16_hi(wd[k])));
+        } else {
+          a = fmaxf(a, fmaxf(fabsf(bf16_lo(wd[k])), fabsf(bf16_hi(wd[k]))));
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      if (ASYM) {
+        a = fminf(a, __shfl_xor_sync(0xffffffffu, a, o));
+        b = fmaxf(b, __shfl_xor_sync(0xffffffffu, b, o));
+      } else {
+        a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
+      }
+    }
+    if (lane == 0) {
+      sh_a[warp] = a;
+      sh_b[warp] = b;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      float lo = sh_a[0], hi = sh_b[0];
+#pragma unroll
+      for (int w = 1; w < kGvWarps; ++w) {
+        lo = ASYM ? fminf(lo, sh_a[w]) : fmaxf(lo, sh_a[w]);
+        hi = fmaxf(hi, sh_b[w]);
+      }
+      const RowQuant rq = ASYM ? row_quant_asym(lo, hi) : row_quant_sym(lo);
+      const float rc = __frcp_rn(rq.s);
+      sh_s = rq.s;
+      sh_r = rc;
+      sh_zp = rq.zp;
+      // the stand-alone affine quantizer's margin of its division-free fast path
+      sh_thr = ASYM ? __fsub_rd(0.5f, __fmul_rn(__fmul_rn(fmaxf(fabsf(lo), fabsf(hi)), rc), 0x1p-21f)) : 0.f;
+    }
+    __syncthreads();
+    const float sc = sh_s, rc = sh_r, thr = sh_thr;
+    const int zpv = sh_zp;
+    for (int64_t c = threadIdx.x; c < nx * 2; c += kGvWarps * 32) {
+      uint2 packed = make_uint2(0, 0);
+      if (c < nv) {
+        const uint4 v = __ldg(xr + c);
+        const uint32_t wd[4] = {v.x, v.y, v.z, v.w};
+        float f[8];
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          f[2 * k] = bf16_lo(wd[k]);
+          f[2 * k + 1] = bf16_hi(wd[k]);
+        }
+        if (ASYM) {
+          uint32_t o2[2];
+          quant_row_group_affine_x2<8>(f, sc, rc, zpv, thr, o2);
+          packed = make_uint2(o2[0], o2[1]);
+        } else {
+          uint32_t q8[8];
+          quant_row_group_x2<8>(f, sc, rc, q8);
+          packed = make_uint2(pack4_i8_prmt(q8[0], q8[1], q8[2], q8[3]), pack4_i8_prmt(q8[4], q8[5], q8[6], q8[7]));
+        }
+      }
+      reinterpret_cast<uint2*>(xs)[c] = packed;
+    }
+  }
+  __syncthreads();
+  // row scale and zero point of token `lane` (lane t < M writes token t's outputs)
+  const int tl = lane < MT ? lane : 0;
+  const float sx = XM == 0 ? (tl < M ? epi_row_scale(ep, tl) : 0.f) : sh_s;
+  const int zpm = XM == 0 ? (tl < M ? epi_row_zp(ep, tl) : 0) : (XM == 2 ? sh_zp : 0);
+
+  int acc[MT];
+#pragma unroll
+  for (int t = 0; t < MT; ++t) acc[t] = 0;
+  auto sum_unit = [&](int64_t u, const uint4 (&d)[kGvKU]) {
+    const int64_t sg = u % nseg;
+#pragma unroll
+    for (int c = 0; c < kGvKU; ++c) {
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const uint4 xv = reinterpret_cast<const uint4*>(xs)[t * nx + (sg * kGvKU + c) * 32 + lane];
+        acc[t] = __dp4a((int)d[c].x, (int)xv.x, acc[t]);
+        acc[t] = __dp4a((int)d[c].y, (int)xv.y, acc[t]);
+        acc[t] = __dp4a((int)d[c].z, (int)xv.z, acc[t]);
+        acc[t] = __dp4a((int)d[c].w, (int)xv.w, acc[t]);
+      }
+    }
+    if (sg == nseg - 1) {
+      int mine = 0;
+#pragma unroll
+      for (int t = 0; t < MT; ++t) {
+        const int tot = __reduce_add_sync(0xffffffffu, acc[t]);
+        mine = (lane == t) ? tot : mine;
+        acc[t] = 0;
+      }
+      const int64_t n = gw + (u / nseg) * tw;
+      if (lane < MT && lane < M && W8A8_DOK(n < N, 405))
+        y[lane * N + n] = __float2bfloat16_rn(epi_apply(ep, mine, sx, zpm, n));
+    }
+  };
+  for (int64_t u = 0; u < units; u += 2) {
+    if (u + 1 < units) load_unit(u + 1, w1);
+    sum_unit(u, w0);
+    if (u + 2 < units) load_unit(u + 2, w0);
+    if (u + 1 < units) sum_unit(u + 1, w1);
+  }
+}
+
+// up to 2 token rows: the dp4a work grows with the tokens (a quarter instruction per weight
+// byte and token) while the padded warp MMA costs the same up to 8; measured against the
+// staged MMA kernel, 2 rows gain (28672 x 4096: 29.6 -> 26.9 us) and 3-4 rows lose on long
+// rows (4096 x 14336 at 4 rows: 20.2 -> 26.5 us), so those stay there
+constexpr int kGvMaxRows = 2;
+bool gemv_ok(int64_t rows, int64_t K) {
+  return rows >= 1 && rows <= kGvMaxRows && K > 0 && K % 16 == 0 && K <= 65536;
+}
+
+// x: the bf16 row (xm 1/2, one row) or null; g.a: the int8 codes (xm 0)
+static cudaError_t gemv(int xm, const void* x, const GemmArgs& g, const EpiParams& ep, cudaStream_t st) {
+  static thread_local int s_dev = -1, s_sms = 0;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev != s_dev) {
+    const int big = 64 * 1024;
+    e = cudaFuncSetAttribute(gemv_kernel<0, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<0, 2>, cudaFuncAttributeMaxDynamicSharedMemorySize, 2 * big);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<1, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(gemv_kernel<2, 1>, cudaFuncAttributeMaxDynamicSharedMemorySize, big);
+    if (e == cudaSuccess) e = cudaDeviceGetAttribute(&s_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    s_dev = dev;
+  }
+  const int mt = g.rows <= 1 ? 1 : 2;
+  const size_t xs_bytes = (size_t)gemv_xs_bytes(g.K) * (size_t)mt;
+  // two CTAs per SM at most (registers, and the codes' shared memory); no more CTAs than
+  // 8-row groups of the weight
+  const int64_t want = (g.N + kGvWarps - 1) / kGvWarps;
+  const int64_t cap = (xs_bytes <= 100 * 1024 ? 2 : 1) * (int64_t)s_sms;
+  const unsigned grid = (unsigned)(want < cap ? want : cap);
+  __nv_bfloat16* y = static_cast<__nv_bfloat16*>(g.y);
+  const __nv_bfloat16* xb = static_cast<const __nv_bfloat16*>(x);
+  if (xm == 1)
+    gemv_kernel<1, 1><<<grid, kGvWarps * 32, xs_bytes, st>>>(xb, nullptr, 1, g.w, g.N, g.K, ep, y);
+  else if (xm == 2)
+    gemv_kernel<2, 1><<<grid, kGvWarps * 32, xs_bytes, st>>>(xb, nullptr, 1, g.w, g.N, g.K, ep, y);
+  else if (mt == 1)
+    gemv_kernel<0, 1><<<grid, kGvWarps * 32, xs_bytes, st>>>(nullptr, g.a, g.rows, g.w, g.N, g.K, ep, y);
+  else
+    gemv_kernel<0, 2><<<grid, kGvWarps * 32, xs_bytes, st>>>(nullptr, g.a, g.rows, g.w, g.N, g.K, ep, y);
+  return cudaGetLastError();
+}
+
 bool gemm_small_m_fused_ok(int64_t rows, int64_t K) { return rows == 1 && xs_stride(K) <= 96 * 1024; }
 
 cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cudaStream_t st) {
@@ -463,6 +679,8 @@ cudaError_t gemm_small_m_fused(const void* x, int64_t ldx, const GemmArgs& g, cu
     s_grid = 2 * sms;
     s_dev = dev;
   }
+  if (g.rows == 1 && gemv_ok(1, g.K) && (reinterpret_cast<uintptr_t>(g.w) & 15) == 0)
+    return gemv(asym ? 2 : 1, x, g, ep, st);
   const int64_t gx = (g.N + 15) / 16;
   const unsigned grid = (unsigned)(gx < s_grid ? gx : s_grid);
   const size_t xs_bytes = (size_t)(g.rows * xs_stride(g.K));
@@ -484,6 +702,9 @@ cudaError_t gemm_small_m(const GemmArgs& g, cudaStream_t st) {
   ep.azp = g.azp;
   ep.s_w = g.s_w;
   ep.bias = static_cast<const __nv_bfloat16*>(g.bias);
+  if (!g.seg && gemv_ok(g.rows, g.K) && (reinterpret_cast<uintptr_t>(g.w) & 15) == 0 &&
+      (reinterpret_cast<uintptr_t>(g.a) & 15) == 0)
+    return gemv(0, nullptr, g, ep, st);
   const int64_t gx = (g.N + 15) / 16;
   {
     const int64_t xs_bytes = g.rows * xs_stride(g.K);

@@ -16,6 +16,8 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
   gemm_chunked   M=4096, N=28672, K=4096 with N(0,1) activations: many rows' L1 norms exceed
                  2^17, so their tiles run the 1024-K chunked mode
   small          w8a8_linear at M=16 (warp-MMA engine), N=28672, K=4096
+  decode1_o      w8a8_linear on one bf16 token row (quantizer fused into the small-M GEMM), N=K=4096
+  decode1_qkv    the same with N=6144
   decode8        w8a8_scaled_mm on 8 quantized token rows (staged small-M kernel), N=28672, K=4096
   moe            the MoE layer: 4096 tokens, 32 experts, top-4
   moe_routed     the same layer behind w8a8_moe_route (router logits in, every step on the GPU)
@@ -90,6 +92,14 @@ def case_fn(name):
         sw = torch.rand(28672, device=dev, generator=_gen(9)).mul_(1e-3)
         ws = torch.empty(w8.linear_workspace_size(16, 4096), dtype=torch.uint8, device=dev)
         y = torch.empty(16, 28672, dtype=torch.bfloat16, device=dev)
+        return lambda: w8.linear(x, wq, sw, workspace=ws, out=y)
+    if name in ("decode1_o", "decode1_qkv"):
+        N = 4096 if name == "decode1_o" else 6144
+        x = _bf16((1, 4096), 1.0, 25)
+        wq = torch.randint(-127, 128, (N, 4096), dtype=torch.int8, device=dev, generator=_gen(26))
+        sw = torch.rand(N, device=dev, generator=_gen(27)).mul_(1e-3)
+        ws = torch.empty(w8.linear_workspace_size(1, 4096), dtype=torch.uint8, device=dev)
+        y = torch.empty(1, N, dtype=torch.bfloat16, device=dev)
         return lambda: w8.linear(x, wq, sw, workspace=ws, out=y)
     if name == "decode8":
         xq = torch.randint(-127, 128, (8, 4096), dtype=torch.int8, device=dev, generator=_gen(18))
