@@ -540,6 +540,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ++use;
         // every lane waits; the outcome is made warp-uniform so the warp stays converged
         if (!__all_sync(0xffffffffu, wait_bar(&bars->full8[cw], ph, bars, p.status))) { ok = false; break; }
+        // 512 units of 16 int8 (128 rows x 4): 16 per lane, in two batches of 8 loads each.
+        // The compiler cannot move loads of the int8 slot above stores into the fp16 slot,
+        // so every batch costs a shared-memory latency: few, large batches, and the first
+        // issued before the wait for the fp16 slot, whose latency then hides it.
+        uint4 v[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const int u = lane + 32 * i;
+          v[i] = *reinterpret_cast<const uint4*>(src + (u >> 2) * 64 + (u & 3) * 16);
+        }
         // the slot's previous use, step it - SB, must be finished
         if (it >= (uint32_t)SB) {
           const uint32_t j = it - SB;
@@ -548,18 +558,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             break;
           }
         }
-        // 512 units of 16 int8 (128 rows x 4): 16 per lane, in 4 batches
 #pragma unroll
-        for (int bt = 0; bt < 4; ++bt) {
-          uint4 v[4];
+        for (int bt = 0; bt < 2; ++bt) {
+          if (bt == 1) {
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int u = lane + 32 * (4 * bt + i);
-            v[i] = *reinterpret_cast<const uint4*>(src + (u >> 2) * 64 + (u & 3) * 16);
+            for (int i = 0; i < 8; ++i) {
+              const int u = lane + 32 * (8 + i);
+              v[i] = *reinterpret_cast<const uint4*>(src + (u >> 2) * 64 + (u & 3) * 16);
+            }
           }
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const int u = lane + 32 * (4 * bt + i);
+          for (int i = 0; i < 8; ++i) {
+            const int u = lane + 32 * (8 * bt + i);
             const int r = u >> 2, sgm = u & 3;
             uint32_t o[8];
             i8x4_to_f16x4(v[i].x, o[0], o[1]);
