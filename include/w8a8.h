@@ -400,6 +400,22 @@ w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void
                                        float* s_g, cudaStream_t stream);
 
 /*
+ * w8a8_moe_quantize_scatter_packed -- the packed result of w8a8_moe_quantize_gather_packed,
+ * computed the other way round ([SGLang-CT] MoE INT8 scheme: per-token dynamic symmetric
+ * activations of the expert GEMMs): each token row x[t] is quantized once and its codes,
+ * L1 norm and scale are written to the routed rows row_of[t, j], j < topk, instead of
+ * quantizing every routed row from its token.
+ *   x bf16 [T, K] (row stride ldx; 16-byte aligned rows);  row_of int64 [T, topk] (device;
+ *   the w8a8_moe_route output: distinct rows in [0, R));  packed: R rows of the packed
+ *   activation format;  s_x float [R].  K % 16 == 0, K <= 16384, 1 <= topk <= 32.
+ *   Routed rows that no (t, j) names are left untouched.  Returns W8A8_ERR_MISALIGNED for
+ *   unaligned x, row_of or packed, W8A8_ERR_INVALID_ARG for sizes out of range.
+ */
+w8a8_status w8a8_moe_quantize_scatter_packed(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                             const int64_t* row_of, int topk, int64_t R, void* packed,
+                                             float* s_x, cudaStream_t stream);
+
+/*
  * w8a8_scaled_mm_noalloc -- w8a8_scaled_mm without a workspace, for callers that cannot
  * allocate device memory (a host runtime that owns only the tensors it passes in and has no
  * allocator to lend, or a latency-critical path where cudaMalloc's possible device-wide

@@ -953,6 +953,32 @@ def test_moe_route(T, E, k, kind):
     np.testing.assert_allclose(w.cpu().numpy(), rw, rtol=1e-5, atol=0)
 
 
+@pytest.mark.parametrize("T,K,topk,E", [(4096, 4096, 4, 32), (37, 1040, 3, 5), (1, 16, 1, 1), (300, 14336, 8, 64)])
+def test_moe_quantize_scatter_matches_gather(T, K, topk, E):
+    """Each token quantized once and written to its routed rows gives the packed buffer
+    (fp16 codes, L1 norms) and scales of quantizing every routed row from its token, bit for
+    bit, and both equal the oracle's per-token quantization of the gathered rows."""
+    g = torch.Generator().manual_seed(T + K)
+    x = wl.llama_activations(T, K, seed=T * 3 + K)
+    ids = torch.stack([torch.randperm(E, generator=g)[:topk] for _ in range(T)]).reshape(-1)
+    order = torch.argsort(ids, stable=True)
+    row_index = order // topk
+    row_of = torch.empty(T * topk, dtype=torch.int64)
+    row_of[order] = torch.arange(T * topk)
+    xd = x.to(DEV)
+    ga = w8.moe_quantize_gather_packed(xd, row_index.to(DEV))
+    sa = w8.moe_quantize_scatter_packed(xd, row_of.view(T, topk).to(DEV))
+    torch.cuda.synchronize()
+    R = T * topk
+    assert torch.equal(ga.buf[: R * K * 2], sa.buf[: R * K * 2])
+    assert torch.equal(ga.norms(), sa.norms())
+    assert torch.equal(ga.scale, sa.scale)
+    rq, rs = oracle.quantize_act_dynamic_symmetric(x.float().numpy()[row_index.numpy()])
+    np.testing.assert_array_equal(sa.codes().float().cpu().numpy().astype(np.int8), rq)
+    np.testing.assert_array_equal(sa.scale.cpu().numpy(), rs)
+    np.testing.assert_array_equal(sa.norms().cpu().numpy(), np.abs(rq.astype(np.int64)).sum(1))
+
+
 def test_moe_route_feeds_moe_forward():
     """The routed outputs drive the MoE layer end to end: the same result as the oracle layer
     given the oracle's routing (the weights within the routing tolerance)."""

@@ -17,6 +17,7 @@ from ._binding import (  # noqa: F401
     act_packed_size,
     grouped_mm_packed,
     moe_quantize_gather_packed,
+    moe_quantize_scatter_packed,
     quantize_act_packed,
     scaled_mm_packed,
     silu_mul_quant_packed,

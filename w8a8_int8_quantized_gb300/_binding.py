@@ -61,6 +61,7 @@ SIGNATURES = {
     "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
     "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_gather_packed": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
+    "w8a8_moe_quantize_scatter_packed": (_I, [_P, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P]),
     "w8a8_silu_mul_quant_packed": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_scaled_mm_noalloc": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P]),
 }
@@ -481,6 +482,21 @@ def moe_quantize_gather_packed(x, row_index, buf=None):
     return PackedActivations(pk, R, K, s)
 
 
+def moe_quantize_scatter_packed(x, row_of, R=None, buf=None):
+    """Each token row quantized once, its codes written to the routed rows row_of[t, j]."""
+    _need(x, torch.bfloat16, "x", 2)
+    _need(row_of, torch.int64, "row_of", 2)
+    T, K = x.shape
+    topk = row_of.shape[1]
+    R = T * topk if R is None else R
+    pk = _packed_buf(R, K, x.device, buf)
+    s = torch.empty(R, dtype=torch.float32, device=x.device)
+    _check("w8a8_moe_quantize_scatter_packed",
+           lib().w8a8_moe_quantize_scatter_packed(_ptr(x), T, K, K, _ptr(row_of), topk, R, _ptr(pk), _ptr(s),
+                                                  _stream()))
+    return PackedActivations(pk, R, K, s)
+
+
 def silu_mul_quant_packed(h, buf=None):
     _need(h, torch.bfloat16, "h", 2)
     R, twoI = h.shape
@@ -498,10 +514,11 @@ def moe_forward(x, row_index, seg_offsets, row_of, topk_w, w13, s13, w2, s2):
     x bf16 [T, H]; row_index int64 [R] (token of each sorted row); seg_offsets int64 [E+1];
     row_of int64 [T, k] (sorted row of each (token, slot)); topk_w float32 [T, k];
     w13 int8 [E, 2I, H] with s13 [E, 2I]; w2 int8 [E, H, I] with s2 [E, H].
-    Five launches: gather-quantize, expert GEMM 1, SiLU*up + quantize, expert GEMM 2, combine.
+    Five launches: quantize (each token once, written to its routed rows), expert GEMM 1,
+    SiLU*up + quantize, expert GEMM 2, combine.
     Returns (y [T, H], h [R, 2I], out [R, H]).
     """
-    xa = moe_quantize_gather_packed(x, row_index)
+    xa = moe_quantize_scatter_packed(x, row_of.reshape(x.shape[0], -1), row_index.numel())
     h = grouped_mm_packed(xa, w13, s13, seg_offsets)
     ga = silu_mul_quant_packed(h)
     o = grouped_mm_packed(ga, w2, s2, seg_offsets)

@@ -588,6 +588,22 @@ w8a8_status w8a8_moe_quantize_gather_packed(const void* x, int64_t T, int64_t K,
                                 norms, stream));
 }
 
+w8a8_status w8a8_moe_quantize_scatter_packed(const void* x, int64_t T, int64_t K, int64_t ldx,
+                                             const int64_t* row_of, int topk, int64_t R, void* packed, float* s_x,
+                                             cudaStream_t stream) {
+  if (T < 0 || K < 0 || R < 0 || R > 0x7FFFFFFF || T > 0x7FFFFFFF || topk < 1 || topk > 32 || K > 16384)
+    return W8A8_ERR_INVALID_ARG;
+  if (T == 0 || K == 0 || R == 0) return W8A8_OK;
+  if (!x || !row_of || !packed || !s_x || ldx < K) return W8A8_ERR_INVALID_ARG;
+  if (K % 16 != 0 || ldx % 8 != 0 || !aligned(x, 16) || !aligned(row_of, 8) || !aligned(packed, 256))
+    return W8A8_ERR_MISALIGNED;
+  w8a8_status st = check_device();
+  if (st != W8A8_OK) return st;
+  uint8_t* pk = static_cast<uint8_t*>(packed);
+  int32_t* norms = reinterpret_cast<int32_t*>(pk + a256((size_t)R * (size_t)K * 2));
+  return cuda_status(quant_rows_scatter_packed(x, T, K, ldx, row_of, topk, R, pk, s_x, norms, stream));
+}
+
 w8a8_status w8a8_silu_mul_quant_packed(const void* h, int64_t R, int64_t I, void* packed, float* s_g,
                                        cudaStream_t stream) {
   if (R < 0 || I < 0 || R > 0x7FFFFFFF) return W8A8_ERR_INVALID_ARG;

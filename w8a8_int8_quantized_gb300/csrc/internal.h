@@ -13,6 +13,9 @@ struct EpiParams;
 // quant.cu
 // q_i8: int8 codes [rows, K] or nullptr; q_f16: the same codes as fp16 [rows, K] (the GEMM-ready
 // activation format) or nullptr; norm_out: sum_k |q| per row (with q_f16); sum_out: sum_k q.
+cudaError_t quant_rows_scatter_packed(const void* x, int64_t T, int64_t K, int64_t ldx, const int64_t* row_of,
+                                      int topk, int64_t R, void* q_f16, float* scale, int32_t* norm_out,
+                                      cudaStream_t st);
 cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t ldx,
                        const int64_t* row_index, int8_t* q_i8, void* q_f16, float* scale, int32_t* zp,
                        int32_t* sum_out, int32_t* norm_out, cudaStream_t st);

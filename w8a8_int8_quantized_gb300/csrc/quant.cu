@@ -81,12 +81,20 @@ __device__ __forceinline__ uint4 ldg_stream(const uint4* p) {
 // MODE: w8a8_act_mode.  row_index: optional gather (MoE), sum_out: optional per-row sum
 // of q (weight azp_adj).
 // ---------------------------------------------------------------------------
-template <int MODE, int THREADS, int NV, bool F16, bool SUM>
+// Scatter of the output rows (MoE): input row t is written to output rows
+// row_of[t * topk + j], j < topk, of the out_rows rows of the output.
+struct RowScatter {
+  const int64_t* row_of;
+  int topk;
+  int64_t out_rows;
+};
+
+template <int MODE, int THREADS, int NV, bool F16, bool SUM, bool SC = false>
 __global__ void __launch_bounds__(THREADS, THREADS >= 512 ? 2 : 0)
 quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int64_t ldx,
                const int64_t* __restrict__ row_index, int8_t* __restrict__ q, __half* __restrict__ q16,
                float* __restrict__ scale, int32_t* __restrict__ zp, int32_t* __restrict__ sum_out,
-               int32_t* __restrict__ norm_out) {
+               int32_t* __restrict__ norm_out, const RowScatter sc) {
   constexpr int W = THREADS / 32;
   constexpr bool DYN = (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM);
   // row sums of squares of the codes (the GEMM's Cauchy-Schwarz test) for the affine modes only
@@ -121,6 +129,13 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
       if (SQ) q2 += sh_sq[b][i];
     }
     if (!W8A8_DOK(r < rows, 104)) return;
+    if constexpr (SC) {
+      for (int j = 0; j < sc.topk; ++j) {
+        const int64_t d = sc.row_of[r * sc.topk + j];
+        if (W8A8_DOK(d >= 0 && d < sc.out_rows, 107)) norm_out[d] = a;  // L1 norm of the codes
+      }
+      return;
+    }
     if (SUM) sum_out[r] = s;
     if (F16) norm_out[r] = a;         // L1 norm of the codes
     if (SQ) norm_out[rows + r] = q2;  // sum of their squares, right after the rows' L1 norms
@@ -246,7 +261,15 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
           uint4 o;
           i8x4_to_f16x4(w0, o.x, o.y);
           i8x4_to_f16x4(w1, o.z, o.w);
-          if (W8A8_DOK(row < rows && (int64_t)(idx + 1) * 8 <= K, 102)) reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
+          if constexpr (SC) {
+            for (int j = 0; j < sc.topk; ++j) {
+              const int64_t d = __ldg(sc.row_of + row * sc.topk + j);
+              if (W8A8_DOK(d >= 0 && d < sc.out_rows && (int64_t)(idx + 1) * 8 <= K, 108))
+                reinterpret_cast<uint4*>(q16 + d * K)[idx] = o;
+            }
+          } else {
+            if (W8A8_DOK(row < rows && (int64_t)(idx + 1) * 8 <= K, 102)) reinterpret_cast<uint4*>(q16 + row * K)[idx] = o;
+          }
         } else {
           if (W8A8_DOK(row < rows && (int64_t)(idx + 1) * 8 <= K, 102)) reinterpret_cast<uint2*>(q + row * K)[idx] = make_uint2(w0, w1);
         }
@@ -277,7 +300,12 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
         if (SQ) qsq += c1 * c1 - c0 * c0;
       }
     }
-    if (threadIdx.x == 0 && W8A8_DOK(row < rows, 103)) {
+    if constexpr (SC) {
+      if (threadIdx.x < sc.topk) {
+        const int64_t d = sc.row_of[row * sc.topk + threadIdx.x];
+        if (W8A8_DOK(row < rows && d >= 0 && d < sc.out_rows, 109)) scale[d] = rq.s;
+      }
+    } else if (threadIdx.x == 0 && W8A8_DOK(row < rows, 103)) {
       if (DYN) scale[row] = rq.s;
       if (MODE == W8A8_ACT_DYN_TOKEN_ASYM) zp[row] = rq.zp;
     }
@@ -375,32 +403,32 @@ quant_rows_generic(const __nv_bfloat16* __restrict__ x, int64_t K, int64_t ldx,
   }
 }
 
-template <int MODE, int THREADS, int NV, bool F16, bool SUM>
+template <int MODE, int THREADS, int NV, bool F16, bool SUM, bool SC = false>
 static void launch_vec(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* row_index,
                        int8_t* q, __half* q16, float* scale, int32_t* zp, int32_t* sum_out, int32_t* norm_out,
-                       cudaStream_t st) {
-  auto kern = quant_rows_vec<MODE, THREADS, NV, F16, SUM>;
+                       cudaStream_t st, const RowScatter& sc = RowScatter{nullptr, 0, 0}) {
+  auto kern = quant_rows_vec<MODE, THREADS, NV, F16, SUM, SC>;
   static thread_local unsigned cached = 0;  // per instantiation: CTAs that fill the GPU once
   if (cached == 0) cached = persistent_grid(kern, THREADS, (int64_t)1 << 40);
   const unsigned grid = (unsigned)(rows < (int64_t)cached ? rows : (int64_t)cached);
-  kern<<<grid, THREADS, 0, st>>>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out);
+  kern<<<grid, THREADS, 0, st>>>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, sc);
 }
 
-template <int MODE, bool F16, bool SUM>
+template <int MODE, bool F16, bool SUM, bool SC = false>
 static void launch_vec_k(const __nv_bfloat16* x, int64_t rows, int64_t K, int64_t ldx, const int64_t* row_index,
                          int8_t* q, __half* q16, float* scale, int32_t* zp, int32_t* sum_out, int32_t* norm_out,
-                         cudaStream_t st) {
+                         cudaStream_t st, const RowScatter& sc = RowScatter{nullptr, 0, 0}) {
   // Rows are latency-bound at these sizes (one CTA-wide reduction per row), so short rows get
   // small CTAs and many rows in flight per SM; about 16-32 values per thread.
   const int64_t nvec = K / 8;
   if (nvec <= 128 * 2)
-    launch_vec<MODE, 128, 2, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+    launch_vec<MODE, 128, 2, F16, SUM, SC>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st, sc);
   else if (nvec <= 128 * 4)
-    launch_vec<MODE, 128, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+    launch_vec<MODE, 128, 4, F16, SUM, SC>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st, sc);
   else if (nvec <= 256 * 4)
-    launch_vec<MODE, 256, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+    launch_vec<MODE, 256, 4, F16, SUM, SC>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st, sc);
   else
-    launch_vec<MODE, 512, 4, F16, SUM>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st);
+    launch_vec<MODE, 512, 4, F16, SUM, SC>(x, rows, K, ldx, row_index, q, q16, scale, zp, sum_out, norm_out, st, sc);
 }
 
 template <int MODE>
@@ -441,6 +469,18 @@ cudaError_t quant_rows(int mode, const void* x, int64_t rows, int64_t K, int64_t
       return launch_quant_rows<W8A8_ACT_STATIC_TENSOR_ASYM>(xb, rows, K, ldx, row_index, q, qh, scale, zp,
                                                             sum_out, norm_out, st);
   }
+}
+
+// MoE: each token row quantized once (dynamic symmetric, packed fp16 codes) and written to
+// its topk expert-sorted rows.  K % 8 == 0, 16-byte aligned rows, K <= 16384.
+cudaError_t quant_rows_scatter_packed(const void* x, int64_t T, int64_t K, int64_t ldx, const int64_t* row_of,
+                                      int topk, int64_t R, void* q_f16, float* scale, int32_t* norm_out,
+                                      cudaStream_t st) {
+  const RowScatter sc{row_of, topk, R};
+  launch_vec_k<W8A8_ACT_DYN_TOKEN_SYM, true, false, true>(static_cast<const __nv_bfloat16*>(x), T, K, ldx, nullptr,
+                                                          nullptr, static_cast<__half*>(q_f16), scale, nullptr,
+                                                          nullptr, norm_out, st, sc);
+  return cudaGetLastError();
 }
 
 // ---------------------------------------------------------------------------
