@@ -326,13 +326,16 @@ w8a8_status w8a8_requantize_max_scale(int8_t* wq, int64_t N, int64_t K, const fl
  *   y bf16 [R, N].  R is seg[E]; max_rows is a host-side upper bound on R used to size the
  *   launch and the workspace (pass R when known).  workspace: at least
  *   w8a8_grouped_mm_workspace_size(max_rows, K) bytes, 256-byte aligned.  E <= 1024.
+ *   w_sumsq: int32 [E, N] row sums of squares of the expert weights (w8a8_weight_sumsq over
+ *   the E*N rows), or NULL; when given, tiles whose activation rows fail the L1 exactness
+ *   test may still run in one pass by the Cauchy-Schwarz test (see w8a8_scaled_mm).
  *   Requirements as for w8a8_scaled_mm.
  */
 size_t w8a8_grouped_mm_workspace_size(int64_t max_rows, int64_t K);
 w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int8_t* w,
-                            const float* s_w, const int64_t* seg_offsets, int E, int64_t max_rows,
-                            int64_t N, int64_t K, void* y, void* workspace, size_t workspace_bytes,
-                            int32_t* dev_status, cudaStream_t stream);
+                            const float* s_w, const int32_t* w_sumsq, const int64_t* seg_offsets,
+                            int E, int64_t max_rows, int64_t N, int64_t K, void* y, void* workspace,
+                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
 /*
  * w8a8_moe_quantize_gather -- per-token symmetric quantization of x rows taken in expert-
@@ -385,11 +388,11 @@ w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t 
                                   const int32_t* w_sumsq, const void* bias, void* y,
                                   int32_t* dev_status, cudaStream_t stream);
 
-/* w8a8_grouped_mm reading packed activations. */
+/* w8a8_grouped_mm reading packed activations (max_rows: the rows the packed buffer holds). */
 w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const int8_t* w,
-                                   const float* s_w, const int64_t* seg_offsets, int E,
-                                   int64_t max_rows, int64_t N, int64_t K, void* y,
-                                   int32_t* dev_status, cudaStream_t stream);
+                                   const float* s_w, const int32_t* w_sumsq,
+                                   const int64_t* seg_offsets, int E, int64_t max_rows, int64_t N,
+                                   int64_t K, void* y, int32_t* dev_status, cudaStream_t stream);
 
 /* w8a8_moe_quantize_gather / w8a8_silu_mul_quant writing packed activations
  * (packed holds R rows; for the SiLU glue K is I). */

@@ -839,6 +839,32 @@ def test_moe_small_full_compare(engine):
     check_bf16(y, r["y_bits"], r["y32"], exact=False)
 
 
+def test_moe_weight_squares_exact():
+    """With the expert weights' sums of squares, grouped tiles whose activation rows fail the
+    L1 test (every 37th token made nearly constant in magnitude, so its codes are near +-127)
+    may run one pass by the Cauchy-Schwarz test (weights indexed by expert): the expert GEMMs'
+    outputs equal the runs without squares and the oracle, bit for bit."""
+    T, H, E, k, inter = 512, 4096, 8, 2, 256
+    d, dev, tok, seg = _moe_setup(T, H, E, k, inter, seed=9)
+    x = d["x"].float()
+    x[::37] = torch.where(x[::37] >= 0, 1.0, -1.0) * (1.0 + 0.01 * torch.rand(x[::37].shape,
+                                                      generator=torch.Generator().manual_seed(3)))
+    x = x.to(torch.bfloat16)
+    xd = x.to(DEV)
+    w13sq = w8.weight_sumsq(dev["w13"].reshape(E * 2 * inter, H)).view(E, 2 * inter)
+    w2sq = w8.weight_sumsq(dev["w2"].reshape(E * H, inter)).view(E, H)
+    args = (xd, dev["row_index"], dev["seg"], dev["row_of"], dev["topk_w"], dev["w13"], dev["s13"], dev["w2"],
+            dev["s2"])
+    y1, h1, o1 = w8.moe_forward(*args)
+    y2, h2, o2 = w8.moe_forward(*args, w13_sumsq=w13sq, w2_sumsq=w2sq)
+    assert torch.equal(h1, h2) and torch.equal(o1, o2) and torch.equal(y1, y2)
+    r = oracle.moe_forward(wl.bits(x), d["topk_ids"].numpy(), d["topk_w"].numpy(),
+                           dev["w13"].cpu().numpy(), dev["s13"].cpu().numpy(), dev["w2"].cpu().numpy(),
+                           dev["s2"].cpu().numpy())
+    np.testing.assert_array_equal(npbits(h2), r["h_bits"])
+    check_bf16(y2, r["y_bits"], r["y32"], exact=False)
+
+
 def test_moe_full_config_sampled():
     T, H, E, k, inter = 4096, 4096, 32, 4, 1408
     d, dev, tok, seg = _moe_setup(T, H, E, k, inter, seed=0)

@@ -52,14 +52,14 @@ SIGNATURES = {
     "w8a8_moe_route_workspace_size": (_SZ, [_I64, _I, _I]),
     "w8a8_moe_route": (_I, [_P, _I64, _I, _I, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "w8a8_grouped_mm_workspace_size": (_SZ, [_I64, _I64]),
-    "w8a8_grouped_mm": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _SZ, _P, _P]),
+    "w8a8_grouped_mm": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _SZ, _P, _P]),
     "w8a8_moe_quantize_gather": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     "w8a8_silu_mul_quant": (_I, [_P, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_combine": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _P]),
     "w8a8_act_packed_size": (_SZ, [_I64, _I64]),
     "w8a8_quantize_act_packed": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
     "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
-    "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
+    "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_gather_packed": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_scatter_packed": (_I, [_P, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P]),
     "w8a8_silu_mul_quant_packed": (_I, [_P, _I64, _I64, _P, _P, _P]),
@@ -348,8 +348,9 @@ def requantize_max_scale(wq, scales, logical_widths, status=None):
     return s_max
 
 
-def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None, workspace=None):
-    """Per-segment W8A8 GEMMs: rows [seg[e], seg[e+1]) use expert e's weight."""
+def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None, workspace=None, w_sumsq=None):
+    """Per-segment W8A8 GEMMs: rows [seg[e], seg[e+1]) use expert e's weight.  w_sumsq: int32
+    [E, N] row sums of squares of the expert weights (enables the Cauchy-Schwarz test)."""
     _need(xq_sorted, torch.int8, "xq_sorted", 2)
     _need(w, torch.int8, "w", 3)
     _need(seg_offsets, torch.int64, "seg_offsets", 1)
@@ -360,8 +361,8 @@ def grouped_mm(xq_sorted, s_x, w, s_w, seg_offsets, out=None, status=None, works
     if out is None:
         out = torch.empty((R, N), dtype=torch.bfloat16, device=w.device)
     ws = _workspace(lib().w8a8_grouped_mm_workspace_size(R, K), w.device, workspace)
-    code = lib().w8a8_grouped_mm(_ptr(xq_sorted), _ptr(s_x), _ptr(w), _ptr(s_w), _ptr(seg_offsets), E, R, N, K,
-                                 _ptr(out), _ptr(ws), ws.numel(), _ptr(status), _stream())
+    code = lib().w8a8_grouped_mm(_ptr(xq_sorted), _ptr(s_x), _ptr(w), _ptr(s_w), _ptr(w_sumsq), _ptr(seg_offsets), E,
+                                 R, N, K, _ptr(out), _ptr(ws), ws.numel(), _ptr(status), _stream())
     _check("w8a8_grouped_mm", code)
     return out
 
@@ -459,13 +460,13 @@ def scaled_mm_packed(pa, wq, s_w, act_mode="dyn_sym", azp_adj=None, w_mode=W_CHA
     return out
 
 
-def grouped_mm_packed(pa, w, s_w, seg_offsets, out=None, status=None):
+def grouped_mm_packed(pa, w, s_w, seg_offsets, out=None, status=None, w_sumsq=None):
     _need(w, torch.int8, "w", 3)
     E, N, K = w.shape
     if out is None:
         out = torch.empty((pa.M, N), dtype=torch.bfloat16, device=w.device)
-    code = lib().w8a8_grouped_mm_packed(_ptr(pa.buf), _ptr(pa.scale), _ptr(w), _ptr(s_w), _ptr(seg_offsets), E,
-                                        pa.M, N, K, _ptr(out), _ptr(status), _stream())
+    code = lib().w8a8_grouped_mm_packed(_ptr(pa.buf), _ptr(pa.scale), _ptr(w), _ptr(s_w), _ptr(w_sumsq),
+                                        _ptr(seg_offsets), E, pa.M, N, K, _ptr(out), _ptr(status), _stream())
     _check("w8a8_grouped_mm_packed", code)
     return out
 
@@ -508,18 +509,20 @@ def silu_mul_quant_packed(h, buf=None):
     return PackedActivations(pk, R, inter, s)
 
 
-def moe_forward(x, row_index, seg_offsets, row_of, topk_w, w13, s13, w2, s2):
+def moe_forward(x, row_index, seg_offsets, row_of, topk_w, w13, s13, w2, s2, w13_sumsq=None, w2_sumsq=None):
     """MoE layer with W8A8 expert GEMMs over token-sorted segments (routing given).
 
     x bf16 [T, H]; row_index int64 [R] (token of each sorted row); seg_offsets int64 [E+1];
     row_of int64 [T, k] (sorted row of each (token, slot)); topk_w float32 [T, k];
-    w13 int8 [E, 2I, H] with s13 [E, 2I]; w2 int8 [E, H, I] with s2 [E, H].
+    w13 int8 [E, 2I, H] with s13 [E, 2I]; w2 int8 [E, H, I] with s2 [E, H]; optional row sums
+    of squares of the expert weights (int32 [E, 2I] and [E, H], weight_sumsq) for the GEMMs'
+    Cauchy-Schwarz exactness test.
     Five launches: quantize (each token once, written to its routed rows), expert GEMM 1,
     SiLU*up + quantize, expert GEMM 2, combine.
     Returns (y [T, H], h [R, 2I], out [R, H]).
     """
     xa = moe_quantize_scatter_packed(x, row_of.reshape(x.shape[0], -1), row_index.numel())
-    h = grouped_mm_packed(xa, w13, s13, seg_offsets)
+    h = grouped_mm_packed(xa, w13, s13, seg_offsets, w_sumsq=w13_sumsq)
     ga = silu_mul_quant_packed(h)
-    o = grouped_mm_packed(ga, w2, s2, seg_offsets)
+    o = grouped_mm_packed(ga, w2, s2, seg_offsets, w_sumsq=w2_sumsq)
     return moe_combine(o, row_of, topk_w), h, o

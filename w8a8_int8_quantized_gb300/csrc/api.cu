@@ -428,14 +428,16 @@ size_t w8a8_grouped_mm_workspace_size(int64_t R, int64_t K) {
 }
 
 w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int8_t* w, const float* s_w,
-                            const int64_t* seg_offsets, int E, int64_t max_rows, int64_t N, int64_t K, void* y,
-                            void* workspace, size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream) {
+                            const int32_t* w_sumsq, const int64_t* seg_offsets, int E, int64_t max_rows, int64_t N,
+                            int64_t K, void* y, void* workspace, size_t workspace_bytes, int32_t* dev_status,
+                            cudaStream_t stream) {
   if (E < 1 || E > gemm_tc_max_segments() || max_rows < 0 || N < 0 || K < 1 || K > kMaxK)
     return W8A8_ERR_INVALID_ARG;
   if (K % 16 != 0) return W8A8_ERR_MISALIGNED;
   if (max_rows == 0 || N == 0) return W8A8_OK;
   if (!xq_sorted || !s_x || !w || !s_w || !seg_offsets || !y) return W8A8_ERR_INVALID_ARG;
-  if (!aligned(xq_sorted, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(seg_offsets, 8))
+  if (!aligned(xq_sorted, 16) || !aligned(w, 16) || !aligned(y, 16) || !aligned(seg_offsets, 8) ||
+      !aligned(w_sumsq, 4))
     return W8A8_ERR_MISALIGNED;
   const bool small = use_small_engine(max_rows, false);
   if (!small && (!workspace || workspace_bytes < ready_bytes(max_rows, K))) return W8A8_ERR_WORKSPACE;
@@ -456,6 +458,7 @@ w8a8_status w8a8_grouped_mm(const int8_t* xq_sorted, const float* s_x, const int
   g.zp = nullptr;
   g.azp = nullptr;
   g.s_w = s_w;
+  g.wsq = w_sumsq;
   g.bias = nullptr;
   g.y = y;
   g.status = dev_status;
@@ -546,14 +549,15 @@ w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t 
 }
 
 w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const int8_t* w, const float* s_w,
-                                   const int64_t* seg_offsets, int E, int64_t max_rows, int64_t N, int64_t K,
-                                   void* y, int32_t* dev_status, cudaStream_t stream) {
+                                   const int32_t* w_sumsq, const int64_t* seg_offsets, int E, int64_t max_rows,
+                                   int64_t N, int64_t K, void* y, int32_t* dev_status, cudaStream_t stream) {
   if (E < 1 || E > gemm_tc_max_segments() || max_rows < 0 || N < 0 || K < 1 || K > kMaxK)
     return W8A8_ERR_INVALID_ARG;
   if (K % 16 != 0) return W8A8_ERR_MISALIGNED;
   if (max_rows == 0 || N == 0) return W8A8_OK;
   if (!packed || !s_x || !w || !s_w || !seg_offsets || !y) return W8A8_ERR_INVALID_ARG;
-  if (!aligned(packed, 256) || !aligned(w, 16) || !aligned(y, 16) || !aligned(seg_offsets, 8))
+  if (!aligned(packed, 256) || !aligned(w, 16) || !aligned(y, 16) || !aligned(seg_offsets, 8) ||
+      !aligned(w_sumsq, 4))
     return W8A8_ERR_MISALIGNED;
   w8a8_status st = check_device();
   if (st != W8A8_OK) return st;
@@ -568,6 +572,7 @@ w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const i
   g.w_mode = W8A8_W_CHANNEL;
   g.s_x = s_x;
   g.s_w = s_w;
+  g.wsq = w_sumsq;
   g.y = y;
   g.status = dev_status;
   return run_gemm(g, stream, const_cast<void*>(packed), false, true);

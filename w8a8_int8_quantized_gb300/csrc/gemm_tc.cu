@@ -332,8 +332,9 @@ __device__ __forceinline__ Work decode_work(int u, const Bars* bars, const KPara
 // Whether the pair tile starting at row0 can run single pass (warp-wide, all lanes agree).
 // Every partial sum of the fp32 accumulation is an integer bounded by sum_k |a_k| |w_k|, so
 // the pass is exact when that bound stays below 2^24.  Two bounds: 127 * (row L1 norm), i.e.
-// a norm below 2^17; or, when the row and weight sums of squares are known (asymmetric
-// activations with the weight's squares given), Cauchy-Schwarz: ||a||_2 ||w||_2 < 2^24,
+// a norm below 2^17; or, when the weight's sums of squares are given (the activation format
+// always carries the rows'; grouped weights are indexed by expert), Cauchy-Schwarz:
+// ||a||_2 ||w||_2 < 2^24,
 // tested exactly as max_rows(sum a^2) * max_cols(sum w^2) < 2^48 in 64-bit integers.  The
 // second is only evaluated when the first fails.
 __device__ __forceinline__ bool tile_single_pass(const KParams& p, const Tile& tl, int lane) {
@@ -355,7 +356,7 @@ __device__ __forceinline__ bool tile_single_pass(const KParams& p, const Tile& t
 #pragma unroll
   for (int j = 0; j < BN / 32; ++j) {
     const int64_t n = tl.n0 + lane + 32 * j;
-    if (n < p.N) mw = max(mw, p.wsq[n]);
+    if (n < p.N) mw = max(mw, p.wsq[(int64_t)tl.e * p.N + n]);
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -1004,11 +1005,10 @@ cudaError_t gemm_tcgen05(const GemmArgs& g, cudaStream_t st) {
   p.E = g.E;
   p.seg = g.seg;
   p.norms = g.norms;
-  // the squares follow the L1 norms in the activation format, written for the asymmetric
-  // modes (whose affine codes usually fail the L1 test); dense GEMMs only
-  const bool asym = g.act_mode == W8A8_ACT_DYN_TOKEN_ASYM || g.act_mode == W8A8_ACT_STATIC_TENSOR_ASYM;
-  p.asq = (!g.seg && g.wsq && asym) ? g.norms + g.rows : nullptr;
-  p.wsq = p.asq ? g.wsq : nullptr;
+  // the squares follow the L1 norms in the activation format (every producer writes them);
+  // with the weight's squares given, tiles that fail the L1 test try Cauchy-Schwarz
+  p.asq = g.wsq ? g.norms + g.rows : nullptr;
+  p.wsq = g.wsq;
   p.az_small = 127 * g.K < (int64_t(1) << 22) ? 1 : 0;
   p.ep.act_mode = g.act_mode;
   p.ep.w_mode = g.w_mode;

@@ -97,8 +97,8 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
                int32_t* __restrict__ norm_out, const RowScatter sc) {
   constexpr int W = THREADS / 32;
   constexpr bool DYN = (MODE == W8A8_ACT_DYN_TOKEN_SYM || MODE == W8A8_ACT_DYN_TOKEN_ASYM);
-  // row sums of squares of the codes (the GEMM's Cauchy-Schwarz test) for the affine modes only
-  constexpr bool SQ = F16 && (MODE == W8A8_ACT_DYN_TOKEN_ASYM || MODE == W8A8_ACT_STATIC_TENSOR_ASYM);
+  // row sums of squares of the codes (the GEMM's Cauchy-Schwarz test) with every packed output
+  constexpr bool SQ = F16;
   // One CTA barrier per row: per-warp partials go to a double-buffered shared array, so a
   // warp may start writing row k+1's partials while slower warps still read row k's; the
   // row sums of row k (SUM / F16) are completed behind row k+1's barrier.
@@ -132,7 +132,10 @@ quant_rows_vec(const __nv_bfloat16* __restrict__ x, int64_t rows, int64_t K, int
     if constexpr (SC) {
       for (int j = 0; j < sc.topk; ++j) {
         const int64_t d = sc.row_of[r * sc.topk + j];
-        if (W8A8_DOK(d >= 0 && d < sc.out_rows, 107)) norm_out[d] = a;  // L1 norm of the codes
+        if (W8A8_DOK(d >= 0 && d < sc.out_rows, 107)) {
+          norm_out[d] = a;                  // L1 norm of the codes
+          norm_out[sc.out_rows + d] = q2;   // sum of their squares
+        }
       }
       return;
     }
@@ -535,10 +538,21 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t rows, int64_t
                       __half* __restrict__ g16, int32_t* __restrict__ norm_out, float* __restrict__ sg) {
   constexpr int W = THREADS / 32;
   __shared__ float sh_a[2][W];
-  __shared__ int sh_abs[2][W];
+  __shared__ int sh_abs[2][W], sh_sq[2][W];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nvec = (int)(I / 8);
   uint4 ng[NV], nu[NV];
+  // packed output: row L1 norms [rows] then sums of squares [rows] of the codes
+  auto finish = [&](int b, int64_t r) {
+    int t = 0, t2 = 0;
+#pragma unroll
+    for (int i = 0; i < W; ++i) {
+      t += sh_abs[b][i];
+      t2 += sh_sq[b][i];
+    }
+    norm_out[r] = t;
+    norm_out[rows + r] = t2;
+  };
   auto load_row = [&](int64_t r) {
     const uint4* gate = reinterpret_cast<const uint4*>(h + r * 2 * I);
     const uint4* up = reinterpret_cast<const uint4*>(h + r * 2 * I + I);
@@ -578,18 +592,13 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t rows, int64_t
     for (int o = 16; o > 0; o >>= 1) a = fmaxf(a, __shfl_xor_sync(0xffffffffu, a, o));
     if (lane == 0) sh_a[buf][warp] = a;
     __syncthreads();
-    if (F16 && threadIdx.x == 0 && prev >= 0) {
-      int t = 0;
-#pragma unroll
-      for (int i = 0; i < W; ++i) t += sh_abs[buf ^ 1][i];
-      norm_out[prev] = t;
-    }
+    if (F16 && threadIdx.x == 0 && prev >= 0) finish(buf ^ 1, prev);
     a = sh_a[buf][0];
 #pragma unroll
     for (int i = 1; i < W; ++i) a = fmaxf(a, sh_a[buf][i]);
     const RowQuant rq = row_quant_sym(a);
     const float rcp = __frcp_rn(rq.s);
-    int qabs = 0;
+    int qabs = 0, qsq = 0;
 #pragma unroll
     for (int i = 0; i < NV; ++i) {
       const int idx = threadIdx.x + i * THREADS;
@@ -600,6 +609,7 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t rows, int64_t
         const uint32_t w1 = pack4_i8_prmt(b[4], b[5], b[6], b[7]);
         if (F16) {
           qabs = abssum4_i8(w1, abssum4_i8(w0, qabs));
+          qsq = __dp4a((int)w1, (int)w1, __dp4a((int)w0, (int)w0, qsq));
           uint4 o;
           i8x4_to_f16x4(w0, o.x, o.y);
           i8x4_to_f16x4(w1, o.z, o.w);
@@ -612,19 +622,20 @@ silu_mul_quant_kernel(const __nv_bfloat16* __restrict__ h, int64_t rows, int64_t
     if (threadIdx.x == 0) sg[row] = rq.s;
     if (F16) {
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) qabs += __shfl_xor_sync(0xffffffffu, qabs, o);
-      if (lane == 0) sh_abs[buf][warp] = qabs;
+      for (int o = 16; o > 0; o >>= 1) {
+        qabs += __shfl_xor_sync(0xffffffffu, qabs, o);
+        qsq += __shfl_xor_sync(0xffffffffu, qsq, o);
+      }
+      if (lane == 0) {
+        sh_abs[buf][warp] = qabs;
+        sh_sq[buf][warp] = qsq;
+      }
       prev = row;
     }
   }
   if (F16) {
     __syncthreads();
-    if (threadIdx.x == 0 && prev >= 0) {
-      int t = 0;
-#pragma unroll
-      for (int i = 0; i < W; ++i) t += sh_abs[buf ^ 1][i];
-      norm_out[prev] = t;
-    }
+    if (threadIdx.x == 0 && prev >= 0) finish(buf ^ 1, prev);
   }
 }
 

@@ -19,7 +19,7 @@ Cases (inputs drawn on the device with a seeded generator; nothing is checked he
   decode1_o      w8a8_linear on one bf16 token row (quantizer fused into the small-M GEMM), N=K=4096
   decode1_qkv    the same with N=6144
   decode8        w8a8_scaled_mm on 8 quantized token rows (staged small-M kernel), N=28672, K=4096
-  moe            the MoE layer: 4096 tokens, 32 experts, top-4
+  moe            the MoE layer: 4096 tokens, 32 experts, top-4 (expert weights' sums of squares given)
   moe_routed     the same layer behind w8a8_moe_route (router logits in, every step on the GPU)
   route          w8a8_moe_route alone: 4096 tokens, 32 experts, top-4
   requant_word   fp8block_to_int8_rowwise_batched over 8 x [3000, 1500] (rows on 4-byte words)
@@ -123,7 +123,8 @@ def case_fn(name):
         tw = torch.rand(T, k, device=dev, generator=g)
         args = (x, order // k, seg, row_of.view(T, k), tw, w13q.view(E, 2 * inter, H), s13.view(E, 2 * inter),
                 w2q.view(E, H, inter), s2.view(E, H))
-        return lambda: w8.moe_forward(*args)
+        kw = dict(w13_sumsq=w8.weight_sumsq(w13q).view(E, 2 * inter), w2_sumsq=w8.weight_sumsq(w2q).view(E, H))
+        return lambda: w8.moe_forward(*args, **kw)
     if name in ("moe_routed", "route"):
         T, H, E, k, inter = 4096, 4096, 32, 4, 1408
         logits = wl.moe_workload(T=T, H=64, E=E, topk=k, inter=64, seed=0, with_weights=False)["logits"].to(dev)
@@ -134,10 +135,12 @@ def case_fn(name):
         w13q, s13 = w8.quantize_weight(_bf16((E * 2 * inter, H), 0.02, 12))
         w2q, s2 = w8.quantize_weight(_bf16((E * H, inter), 0.02, 13))
 
+        w13sq, w2sq = w8.weight_sumsq(w13q).view(E, 2 * inter), w8.weight_sumsq(w2q).view(E, H)
+
         def layer():
             ids, tw, seg, row_index, row_of = w8.moe_route(logits, k, workspace=ws)
             return w8.moe_forward(x, row_index, seg, row_of, tw, w13q.view(E, 2 * inter, H), s13.view(E, 2 * inter),
-                                  w2q.view(E, H, inter), s2.view(E, H))
+                                  w2q.view(E, H, inter), s2.view(E, H), w13_sumsq=w13sq, w2_sumsq=w2sq)
         return layer
     if name == "requant_word":
         g = _gen(14)
