@@ -232,6 +232,10 @@ def run_ours(args, world, rank, pg):
         sx = torch.empty(M_TOKENS, dtype=torch.float32, device=dev)
         y = torch.empty((M_TOKENS, N), dtype=torch.bfloat16, device=dev)
         layers.append(dict(name=name, N=N, K=K, x=x, wq=wq, sw=sw, packed=packed, sx=sx, y=y))
+    # K-split scratch (the tiles past a launch's last full wave of CTA pairs), shared by the
+    # layers: the calls run one after another on one stream
+    split_bytes = max(w8.splitk_workspace_size(M_TOKENS, L["N"], L["K"]) for L in layers)
+    split_ws = torch.empty(max(split_bytes, 256), dtype=torch.uint8, device=dev)
     flush = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev)
     lib = w8.lib()
     stream = torch.cuda.current_stream()
@@ -253,7 +257,8 @@ def run_ours(args, world, rank, pg):
                 e1.record()
             rc |= lib.w8a8_scaled_mm_packed(P(L["packed"].data_ptr()), P(L["wq"].data_ptr()), M_TOKENS, L["N"],
                                             L["K"], 0, P(L["sx"].data_ptr()), None, None, 0,
-                                            P(L["sw"].data_ptr()), None, None, P(L["y"].data_ptr()), None, sptr)
+                                            P(L["sw"].data_ptr()), None, None, P(L["y"].data_ptr()),
+                                            P(split_ws.data_ptr()), split_bytes, None, sptr)
             if record:
                 e2.record()
                 L.setdefault("ev", []).append((e0, e1, e2))
@@ -372,8 +377,8 @@ def run_e2e(args, layers, w8, world, pg):
     dev = "cuda"
     hx = [L["x"].cpu().pin_memory() for L in layers]
     hy = [torch.empty(L["y"].shape, dtype=torch.bfloat16).pin_memory() for L in layers]
-    ws = [torch.empty(max(w8.linear_workspace_size(M_TOKENS, L["K"]), 16), dtype=torch.uint8, device=dev)
-          for L in layers]
+    ws = [torch.empty(max(w8.linear_workspace_size(M_TOKENS, L["K"], "dyn_sym", L["N"]), 16), dtype=torch.uint8,
+                      device=dev) for L in layers]
     dx = [[torch.empty_like(L["x"]) for L in layers] for _ in range(2)]
     dy = [[torch.empty_like(L["y"]) for L in layers] for _ in range(2)]
     s_in, s_comp, s_out = torch.cuda.Stream(), torch.cuda.Stream(), torch.cuda.Stream()

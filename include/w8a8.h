@@ -139,8 +139,8 @@ w8a8_status w8a8_quantize_act(const void* x, int64_t M, int64_t K, int64_t ldx, 
  *           tensor-core engine may then finish more tiles in one exact fp32 pass.  Each
  *           partial sum is at most ||x_m||_2 * ||w_n||_2, and a tile is exact in fp32 when
  *           that stays below 2^24.  Without it, the test is 127 * L1(x_m) < 2^24 alone;
- *           affine codes usually fail that test and their tiles then accumulate in 1024-K
- *           chunks.  Ignored for symmetric modes.
+ *           affine codes, and symmetric codes of rows without outliers, often fail that test
+ *           and their tiles then accumulate in 1024-K chunks.  Used in every mode.
  *   bias    bf16 [N] or NULL.
  *   y       bf16 [M, N] contiguous (output).
  *   workspace  device scratch of at least w8a8_scaled_mm_workspace_size(M, K) bytes,
@@ -164,13 +164,13 @@ w8a8_status w8a8_scaled_mm(const int8_t* xq, const int8_t* wq, int64_t M, int64_
                            size_t workspace_bytes, int32_t* dev_status, cudaStream_t stream);
 
 /*
- * w8a8_splitk_workspace_size -- scratch for K-split GEMMs of few tiles.
+ * w8a8_splitk_workspace_size -- scratch for K-split GEMMs.
  *   The tensor-core engine runs persistent CTA pairs over 256 x 256 output tiles.  A launch
- *   with fewer tiles than two waves of pairs (M of a few hundred rows or less) leaves pairs
- *   idle; with this much scratch it cuts the tiles past its first full wave (all of them
- *   when there is none) along K at 1024-element boundaries, runs the parts on the idle pairs,
- *   and a second kernel adds their int32 partial sums and applies the epilogue: the result
- *   is the same integer, so y is unchanged.
+ *   whose tiles do not fill its last wave of pairs (and one of a few hundred rows, which fills
+ *   no wave) leaves pairs idle; with this much scratch it cuts the tiles past its last full
+ *   wave (all of them when there is none) along K at 1024-element boundaries, into as many
+ *   parts as fill the idle pairs, runs the parts there, and a second kernel adds their int32
+ *   partial sums and applies the epilogue: the result is the same integer, so y is unchanged.
  *   Returns the extra bytes a w8a8_scaled_mm or w8a8_linear call of this shape uses for it on
  *   the current device, placed right after the call's own workspace size (so a workspace of
  *   w8a8_linear_workspace_size(M, K, mode) + w8a8_splitk_workspace_size(M, N, K) bytes).  0
@@ -381,12 +381,15 @@ size_t w8a8_act_packed_size(int64_t M, int64_t K);
 w8a8_status w8a8_quantize_act_packed(const void* x, int64_t M, int64_t K, int64_t ldx, int mode,
                                      void* packed, float* scale, int32_t* zp, cudaStream_t stream);
 
-/* w8a8_scaled_mm reading packed activations (no workspace: nothing is staged). */
+/* w8a8_scaled_mm reading packed activations (nothing is staged).  split_ws: optional K-split
+ * scratch of w8a8_splitk_workspace_size(M, N, K) bytes, 256-byte aligned (NULL or fewer bytes:
+ * no split). */
 w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t M, int64_t N,
                                   int64_t K, int act_mode, const float* s_x, const int32_t* zp,
                                   const int32_t* azp_adj, int w_mode, const float* s_w,
                                   const int32_t* w_sumsq, const void* bias, void* y,
-                                  int32_t* dev_status, cudaStream_t stream);
+                                  void* split_ws, size_t split_bytes, int32_t* dev_status,
+                                  cudaStream_t stream);
 
 /* w8a8_grouped_mm reading packed activations (max_rows: the rows the packed buffer holds). */
 w8a8_status w8a8_grouped_mm_packed(const void* packed, const float* s_x, const int8_t* w,

@@ -121,5 +121,7 @@ def test_noalloc_applies_the_scaled_mm_checks(libpath):
     assert f(p, p, 4, 4, 16, 1, p, p, None, 0, p, None, p, None, None) == 1
     assert f(p, p, 4, 4, 24, 0, p, None, None, 0, p, None, p, None, None) == 3
     g = lib.w8a8_scaled_mm_packed
-    assert g(p, p, 4, 4, 16, 0, p, None, None, 0, p, None, odd, p, None, None) == 3
+    assert g(p, p, 4, 4, 16, 0, p, None, None, 0, p, None, odd, p, None, 0, None, None) == 3
+    # a split scratch that is not 256-byte aligned
+    assert g(p, p, 4, 4, 16, 0, p, None, None, 0, p, None, None, p, odd, 1 << 20, None, None) == 3
     assert f(p, p, 8192, 16, 4096, 0, p, None, None, 0, p, None, p, None, None) == 7

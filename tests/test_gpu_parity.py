@@ -431,14 +431,16 @@ def test_gemm_single_pass_bound(K, fill):
 
 
 def _split_bytes_expected(M, N, K):
-    """The K-split scratch from the plan stated in include/w8a8.h: launches with fewer tiles
-    than two waves of CTA pairs cut the tiles past the first full wave into as many parts as
-    fill the idle pairs, at most one per 1024-K chunk."""
+    """The K-split scratch from the plan stated in include/w8a8.h: the tiles past a launch's
+    last full wave of CTA pairs (all of them when there is none) are cut into as many parts
+    as fill the pairs that wave leaves idle, at most one per 1024-K chunk."""
     pairs = torch.cuda.get_device_properties(0).multi_processor_count // 2
     tiles = -(-M // 256) * -(-N // 256)
-    if M <= 16 or tiles >= 2 * pairs:
+    if M <= 16:
         return 0
-    tail = tiles - (pairs if tiles >= pairs else 0)
+    tail = tiles % pairs
+    if tail == 0:
+        return 0
     f = min(pairs // tail, -(-K // 1024))
     if f < 2:
         return 0
@@ -446,9 +448,36 @@ def _split_bytes_expected(M, N, K):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 4096, 4096), (300, 1000, 14336), (256, 20480, 2048), (17, 520, 3072),
-                                   (130, 8, 1040), (512, 4104, 4096), (64, 256, 1024)])
+                                   (130, 8, 1040), (512, 4104, 4096), (64, 256, 1024), (4096, 6144, 4096),
+                                   (4096, 4096, 14336), (4096, 28672, 4096)])
 def test_splitk_workspace_size(M, N, K):
     assert w8.splitk_workspace_size(M, N, K) == _split_bytes_expected(M, N, K)
+
+
+@pytest.mark.parametrize("M,N,K,act", [(1024, 10240, 2048, "dyn_sym"), (4096, 6144, 4096, "dyn_sym"),
+                                       (1024, 10240, 2048, "dyn_asym")])
+def test_split_last_wave(M, N, K, act):
+    """Launches of several waves cut only the tiles past their last full wave along K
+    (1024 x 10240: 160 tiles = two waves of 76 pairs + 8, in parts; the qkv shape at
+    M = 4096: 384 tiles = five waves + 4).  The result equals the unsplit call bit for bit
+    and, on sampled rows, the oracle."""
+    assert _split_bytes_expected(M, N, K) > 0
+    x = wl.asym_activations(M, K, seed=K + 3) if act == "dyn_asym" else wl.llama_activations(M, K, seed=K + 3)
+    w = wl.weight_bf16(N, K, seed=N + 5)
+    rq, rs = oracle.quantize_weight_per_channel(w.float().numpy())
+    wq = torch.from_numpy(rq).to(DEV)
+    sw = torch.from_numpy(rs).to(DEV)
+    kw = {"azp_adj": w8.azp_adj(wq)} if act == "dyn_asym" else {}
+    xd = x.to(DEV)
+    base = w8.linear_workspace_size(M, K, act)
+    ws_split = torch.empty(base + w8.splitk_workspace_size(M, N, K), dtype=torch.uint8, device=DEV)
+    ws_plain = torch.empty(base, dtype=torch.uint8, device=DEV)
+    y_split = w8.linear(xd, wq, sw, act_mode=act, workspace=ws_split, **kw)
+    y_plain = w8.linear(xd, wq, sw, act_mode=act, workspace=ws_plain, **kw)
+    assert torch.equal(y_split, y_plain)
+    rows = np.concatenate([np.arange(0, M, 61), [M - 1]])
+    r = oracle.w8a8_linear(wl.bits(x)[rows], rq, rs, mode=act)
+    check_bf16(y_split[torch.from_numpy(rows).to(DEV)], r["y_bits"], r["y32"])
 
 
 @pytest.mark.parametrize("act", ["dyn_sym", "dyn_asym", "static_asym"])

@@ -58,7 +58,7 @@ SIGNATURES = {
     "w8a8_moe_combine": (_I, [_P, _P, _P, _I64, _I, _I64, _P, _P]),
     "w8a8_act_packed_size": (_SZ, [_I64, _I64]),
     "w8a8_quantize_act_packed": (_I, [_P, _I64, _I64, _I64, _I, _P, _P, _P, _P]),
-    "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _P]),
+    "w8a8_scaled_mm_packed": (_I, [_P, _P, _I64, _I64, _I64, _I, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P, _P]),
     "w8a8_grouped_mm_packed": (_I, [_P, _P, _P, _P, _P, _P, _I, _I64, _I64, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_gather_packed": (_I, [_P, _I64, _I64, _I64, _P, _I64, _P, _P, _P]),
     "w8a8_moe_quantize_scatter_packed": (_I, [_P, _I64, _I64, _I64, _P, _I, _I64, _P, _P, _P]),
@@ -447,15 +447,17 @@ def quantize_act_packed(x, mode="dyn_sym", scale=None, zp=None, buf=None):
 
 
 def scaled_mm_packed(pa, wq, s_w, act_mode="dyn_sym", azp_adj=None, w_mode=W_CHANNEL, bias=None, out=None,
-                     status=None, w_sumsq=None):
-    """y = epilogue(A @ wq.T) with A given as PackedActivations (scales taken from it)."""
+                     status=None, w_sumsq=None, split_ws=None):
+    """y = epilogue(A @ wq.T) with A given as PackedActivations (scales taken from it).
+    split_ws: optional uint8 CUDA tensor of splitk_workspace_size(M, N, K) bytes."""
     _need(wq, torch.int8, "wq", 2)
     N = wq.shape[0]
     if out is None:
         out = torch.empty((pa.M, N), dtype=torch.bfloat16, device=wq.device)
     code = lib().w8a8_scaled_mm_packed(_ptr(pa.buf), _ptr(wq), pa.M, N, pa.K, _mode(act_mode), _ptr(pa.scale),
                                        _ptr(pa.zp), _ptr(azp_adj), int(w_mode), _ptr(s_w), _ptr(w_sumsq), _ptr(bias),
-                                       _ptr(out), _ptr(status), _stream())
+                                       _ptr(out), _ptr(split_ws), split_ws.numel() if split_ws is not None else 0,
+                                       _ptr(status), _stream())
     _check("w8a8_scaled_mm_packed", code)
     return out
 

@@ -522,11 +522,11 @@ w8a8_status w8a8_quantize_act_packed(const void* x, int64_t M, int64_t K, int64_
 w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t M, int64_t N, int64_t K, int act_mode,
                                   const float* s_x, const int32_t* zp, const int32_t* azp_adj, int w_mode,
                                   const float* s_w, const int32_t* w_sumsq, const void* bias, void* y,
-                                  int32_t* dev_status, cudaStream_t stream) {
+                                  void* split_ws, size_t split_bytes, int32_t* dev_status, cudaStream_t stream) {
   const int8_t* dummy = static_cast<const int8_t*>(packed);
   w8a8_status s = check_scaled_mm_args(dummy, wq, M, N, K, act_mode, s_x, zp, azp_adj, w_mode, s_w, bias, y);
   if (s != W8A8_OK || M == 0 || N == 0) return s;
-  if (!aligned(packed, 256)) return W8A8_ERR_MISALIGNED;
+  if (!aligned(packed, 256) || !aligned(split_ws, 256)) return W8A8_ERR_MISALIGNED;
   s = check_device();
   if (s != W8A8_OK) return s;
   GemmArgs g{};
@@ -545,6 +545,8 @@ w8a8_status w8a8_scaled_mm_packed(const void* packed, const int8_t* wq, int64_t 
   g.bias = bias;
   g.y = y;
   g.status = dev_status;
+  g.split_ws = split_ws;
+  g.split_bytes = split_ws ? split_bytes : 0;
   return run_gemm(g, stream, const_cast<void*>(packed), false, true);
 }
 

@@ -917,9 +917,11 @@ int gemm_tc_max_segments() { return tc::MAX_SEG; }
 
 namespace {
 
-// Work decomposition of a dense launch on `pairs_max` CTA pairs.  Only launches with fewer
-// tiles than two waves split: the tiles past the first full wave (all of them when there is
-// none) are cut into `split` parts, as many as fill the idle pairs, at most one per chunk.
+// Work decomposition of a dense launch on `pairs_max` CTA pairs: the tiles past the last
+// full wave (all of them when there is none) are cut into `split` parts, as many as fill the
+// pairs that wave would leave idle, at most one per chunk.  The 6144-column layer at
+// M = 4096, for instance, has 384 tiles on 76 pairs: five full waves and 4 tiles, which now
+// run as 16 quarter-K parts instead of a sixth wave with 72 idle pairs.
 struct SplitPlan {
   int64_t units;     // work items
   int dp_units;      // whole tiles (first)
@@ -933,10 +935,11 @@ SplitPlan plan_dense(int64_t rows, int64_t N, int64_t K, int64_t pairs_max) {
   const int64_t tiles = ((rows + tc::BM - 1) / tc::BM) * ((N + tc::BN - 1) / tc::BN);
   s.units = tiles;
   s.split = 1;
-  if (pairs_max < 1 || tiles >= 2 * pairs_max) return s;
+  if (pairs_max < 1) return s;
   const int64_t nch = ((K + tc::BK - 1) / tc::BK + tc::CHUNK_STEPS - 1) / tc::CHUNK_STEPS;
-  const int64_t full = tiles >= pairs_max ? pairs_max : 0;
+  const int64_t full = (tiles / pairs_max) * pairs_max;
   const int64_t tail = tiles - full;
+  if (tail == 0) return s;
   int64_t f = pairs_max / tail;
   if (f > nch) f = nch;
   if (f < 2) return s;
