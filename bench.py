@@ -348,7 +348,10 @@ def run_ours(args, world, rank, pg):
         "scaling": "weak", "vs_baseline": None, "dtype": "int8", "data": "synthetic (seeded; random-init weights)",
         "config": bench_config(world),
         "e2e": e2e,
-        "gpu_launches": 2 * len(layers) * args.steps,
+        # per layer: the quantizer, the GEMM and, when its tiles leave a partial last wave of
+        # CTA pairs, the K-split reduce
+        "gpu_launches": sum(2 + (1 if w8.splitk_workspace_size(M_TOKENS, L["N"], L["K"]) > 0 else 0)
+                            for L in layers) * args.steps,
         "roofline": roofline,
         "kernels": {
             # the in-step quantizer writes the GEMM's fp16 operand (4 B per element moved);
