@@ -22,10 +22,10 @@
 // own 128 activation rows and its 128-row half of the weight tile, so a CTA converts only
 // 128 x 64 weight bytes per K step.
 //   activations: fp16 integer codes [rows, K] -> TMA, 128-byte swizzle, straight into the
-//                MMA operand ring (7 stages x 16 KB)
-//   weights:     int8 [E*N, K] -> TMA -> int8 staging ring (4 x 8 KB) -> 4 converter warps,
-//                each owning every 4th K step: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152)
-//                into the swizzled operand layout (4 x 16 KB)
+//                MMA operand ring (6 stages x 16 KB)
+//   weights:     int8 [E*N, K] -> TMA -> int8 staging ring (5 x 8 KB) -> 5 converter warps,
+//                each owning every 5th K step: int8 -> fp16 (exact: 0x6400|(v^0x80) - 1152)
+//                into the swizzled operand layout (5 x 16 KB)
 //   accumulator: two 256-column TMEM buffers per CTA, alternating per single-pass tile
 //   epilogue:    8 warps per CTA read TMEM, apply y = bf16((s_x*s_w) * f32(acc - zp*azp_adj)
 //                + bias), store.
@@ -61,8 +61,8 @@ constexpr int BM_CTA = 128;    // activation rows per CTA
 constexpr int BN = 256;        // weight rows (output columns) per pair tile
 constexpr int BN_CTA = 128;    // weight rows converted and held per CTA
 constexpr int BK = 64;
-constexpr int SA = 7;          // activation ring (fp16 tiles straight from TMA)
-constexpr int CONV_WARPS = 4;  // converter warp w owns the K steps it with it % 4 == w
+constexpr int SA = 6;          // activation ring (fp16 tiles straight from TMA)
+constexpr int CONV_WARPS = 5;  // converter warp w owns the K steps it with it % 5 == w
 constexpr int SB = CONV_WARPS; // converted weight ring: slot w belongs to converter warp w
 constexpr int S8 = CONV_WARPS; // int8 weight staging ring: slot w belongs to converter warp w
 constexpr int CHUNK_STEPS = 16;   // 16 * 64 = 1024 K per exact fp32 chunk
@@ -520,13 +520,18 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         drain_wait(&bars->mma_done, 0, p.status);
       }
     }
-  } else if (warp < 4) {
+  } else if (warp == 5) {
+    // idle: the MMA thread's scheduler partition (warps 1, 5, 9, 13) carries no converter
   } else if (warp < 8) {
     // ---------------------------------------------------------------- converters (each CTA)
-    // Warp w converts whole K steps it = w, w + 4, ...: the 128 x 64 int8 weight tile of the
-    // step (int8 slot w) into the fp16 operand layout (fp16 slot w), so four steps are in
-    // flight at once and the per-step synchronisation latency overlaps.
-    const int cw = warp - 4;
+    // Converter w (warps 2, 3, 4, 6, 7) converts whole K steps it = w, w + 5, ...: the
+    // 128 x 64 int8 weight tile of the step (int8 slot w) into the fp16 operand layout (fp16
+    // slot w), so five steps are in flight at once and the per-step synchronisation latency
+    // overlaps.  The K loop is bound by the hand-off between these warps and the one
+    // MMA-issuing thread (warp 1), not by the conversion itself: keeping the converters off
+    // warp 1's scheduler partition and a fifth step in flight shortened it (gate_up at
+    // M = 4096: 643 -> 589 us).
+    const int cw = warp == 2 ? 0 : warp == 3 ? 1 : warp == 4 ? 2 : warp == 6 ? 3 : 4;
     const uint32_t full16_leader = map_to(su32(&bars->full16[cw]), 0);
     const uint8_t* src = ring8 + cw * B8;
     uint8_t* dst = ringB16 + cw * B16;
