@@ -39,6 +39,9 @@ pins live in tests/test_oracle_*.py and tests/golden/):
                                    illegal scales, hand-worked golden example.
   moe_forward                      pinned: segment == dense per-expert call, combine
                                    == per-token loop, empty experts.
+  moe_combine                      pinned: through moe_forward (above); one slot of
+                                   weight 1 gathers the rows exactly, power-of-two
+                                   weights scale exactly.
   requantize_with_max_scale        pinned: the max-scale partition is unchanged for
                                    every code, power-of-two ratios reduce to
                                    rint(q / 2^j) (ties to even), the half-step bound
@@ -66,6 +69,7 @@ from .w8a8_oracle import (  # noqa: F401
     silu_mul_bf16,
     moe_sort,
     moe_forward,
+    moe_combine,
     moe_route,
     requantize_with_max_scale,
 )

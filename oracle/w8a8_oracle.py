@@ -501,12 +501,25 @@ def moe_forward(x_bits, topk_ids, topk_w, w13_q, s13, w2_q, s2, rows=None):
         acc2 = int8_gemm(gq, w2_q[e])
         ob, _ = scaled_mm_epilogue(acc2, sg, s2[e])
         out_bits[sel] = ob
+    y_bits, y = moe_combine(out_bits, row_of, topk_w, rows=np.nonzero(want)[0])
+    return dict(y_bits=y_bits, y32=y, h_bits=h_bits, out_bits=out_bits, seg=seg, tok=tok, slot=slot)
+
+
+def moe_combine(out_bits, row_of, topk_w, rows=None):
+    """The combine step of the MoE layer: y[t] = bf16( sum over the token's top-k slots,
+    in slot order, of w[t, slot] * out[row_of[t, slot]] ), one float32 multiply and one
+    float32 add per slot, starting from zero.
+    out_bits: bf16 bits [R, H] (expert outputs in sorted-row order); row_of int [T, k];
+    topk_w float32 [T, k]; rows: optional token indices to evaluate (others zero).
+    Returns (y_bits [T, H], y32 [T, H] the float32 sums before the bf16 rounding).
+    """
+    T, k = row_of.shape
+    H = out_bits.shape[1]
     y = np.zeros((T, H), dtype=F32)
-    for t in np.nonzero(want)[0]:
+    for t in (range(T) if rows is None else rows):
         acc = np.zeros(H, dtype=F32)
         for j in range(k):
             o = bf16_bits_to_f32(out_bits[row_of[t, j]])
             acc = (acc + (F32(topk_w[t, j]) * o).astype(F32)).astype(F32)
         y[t] = acc
-    y_bits = f32_to_bf16_bits(y)
-    return dict(y_bits=y_bits, y32=y, h_bits=h_bits, out_bits=out_bits, seg=seg, tok=tok, slot=slot)
+    return f32_to_bf16_bits(y), y

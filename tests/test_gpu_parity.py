@@ -1034,6 +1034,21 @@ def test_moe_quantize_scatter_matches_gather(T, K, topk, E):
     np.testing.assert_array_equal(sa.norms().cpu().numpy(), np.abs(rq.astype(np.int64)).sum(1))
 
 
+@pytest.mark.parametrize("topk", [1, 3, 8, 9, 12])
+def test_moe_combine_slots(topk):
+    """The combine step bit for bit against the oracle: up to 8 slots take the kernel that
+    reads a token's routed rows together, more slots (9, 12) the plain per-slot loop."""
+    T, H = 300, 520
+    R = T * topk
+    g = np.random.default_rng(topk)
+    out = torch.from_numpy(g.standard_normal((R, H)).astype(np.float32)).to(torch.bfloat16)
+    row_of = torch.from_numpy(g.permutation(R).reshape(T, topk).astype(np.int64))
+    tw = torch.from_numpy(g.random((T, topk)).astype(np.float32))
+    y = w8.moe_combine(out.to(DEV), row_of.to(DEV), tw.to(DEV))
+    yb, y32 = oracle.moe_combine(wl.bits(out), row_of.numpy(), tw.numpy())
+    check_bf16(y, yb, y32)
+
+
 def test_moe_route_feeds_moe_forward():
     """The routed outputs drive the MoE layer end to end: the same result as the oracle layer
     given the oracle's routing (the weights within the routing tolerance)."""

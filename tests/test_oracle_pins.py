@@ -385,6 +385,24 @@ def test_moe_segments_and_combine():
     assert abs(oracle.bf16_bits_to_f32(gb)[0] - 3.0 * 2.0 / (1 + math.exp(-2.0))) < 0.02
 
 
+def test_moe_combine_special_cases():
+    """One slot of weight 1 is a gather of the rows (exact); weights 0.5 and 0.25 on two
+    slots scale exactly, so the sum is the exact 0.5 a + 0.25 b rounded once to bf16."""
+    rng = np.random.default_rng(4)
+    out = oracle.f32_to_bf16_bits(rng.standard_normal((7, 40)).astype(np.float32))
+    row_of = np.array([[3], [0], [6], [3]])
+    yb, y32 = oracle.moe_combine(out, row_of, np.ones((4, 1), np.float32))
+    np.testing.assert_array_equal(yb, out[[3, 0, 6, 3]])
+    row_of2 = np.array([[1, 5], [2, 2]])
+    w2 = np.array([[0.5, 0.25], [0.5, 0.25]], np.float32)
+    yb2, y2 = oracle.moe_combine(out, row_of2, w2)
+    a = oracle.bf16_bits_to_f32(out).astype(np.float64)
+    exact = np.stack([0.5 * a[1] + 0.25 * a[5], 0.75 * a[2]])
+    np.testing.assert_array_equal(y2.astype(np.float64), exact)     # no rounding below 2^-24 relative
+    yb3, _ = oracle.moe_combine(out, row_of2, w2, rows=[1])
+    assert not yb3[0].any() and np.array_equal(yb3[1], yb2[1])
+
+
 def test_moe_routing_skew():
     d = wl.moe_workload(T=4096, H=8, E=32, topk=4, inter=8, seed=0, with_weights=False)
     ids = d["topk_ids"].numpy()
