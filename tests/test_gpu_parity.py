@@ -949,6 +949,40 @@ def test_grouped_mm_empty_segments():
         check_bf16(y[a:b], yb, y32)
 
 
+def test_grouped_mm_max_segments():
+    """The largest segment count the tensor-core engine's work list holds (1024): mostly empty
+    segments, single rows, a segment at the very end, and one of 300 rows (two row tiles);
+    a segment count one past the limit is refused.  Bit-exact against the oracle per segment
+    and against the warp-MMA engine."""
+    E, N, K = 1024, 72, 96
+    lens = np.zeros(E, dtype=np.int64)
+    lens[[0, 1, 5, 511, 512, 1000]] = [1, 2, 3, 1, 300, 17]
+    lens[E - 1] = 4
+    seg = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int64))
+    R = int(seg[-1])
+    g = torch.Generator().manual_seed(11)
+    xq = torch.randint(-127, 128, (R, K), dtype=torch.int8, generator=g)
+    wq = torch.randint(-127, 128, (E, N, K), dtype=torch.int8, generator=g)
+    sx = torch.rand(R, dtype=torch.float32, generator=g) * 1e-2
+    sw = torch.rand(E, N, dtype=torch.float32, generator=g) * 1e-3
+    y = w8.grouped_mm(xq.to(DEV), sx.to(DEV), wq.to(DEV), sw.to(DEV), seg.to(DEV))
+    w8.set_gemm_engine(2)
+    y2 = w8.grouped_mm(xq.to(DEV), sx.to(DEV), wq.to(DEV), sw.to(DEV), seg.to(DEV))
+    torch.cuda.synchronize()
+    assert torch.equal(y.view(torch.int16), y2.view(torch.int16))
+    for e in np.nonzero(lens)[0]:
+        a, b = int(seg[e]), int(seg[e + 1])
+        acc = oracle.int8_gemm(xq[a:b].numpy(), wq[e].numpy())
+        yb, y32 = oracle.scaled_mm_epilogue(acc, sx[a:b].numpy(), sw[e].numpy())
+        check_bf16(y[a:b], yb, y32)
+    w8.set_gemm_engine(0)
+    seg2 = torch.cat([seg, seg[-1:]])
+    wq2 = torch.zeros((E + 1, N, K), dtype=torch.int8)
+    sw2 = torch.zeros((E + 1, N), dtype=torch.float32)
+    with pytest.raises(w8.W8A8Error):
+        w8.grouped_mm(xq.to(DEV), sx.to(DEV), wq2.to(DEV), sw2.to(DEV), seg2.to(DEV))
+
+
 @pytest.mark.parametrize("widths,K", [([4096, 1024, 1024], 4096), ([300, 77, 0, 129], 1500), ([64], 512),
                                       ([3, 5], 4112)])
 def test_requantize_max_scale(widths, K):
